@@ -1,0 +1,494 @@
+"""Benchmark of the W4A16 GEMM hot path on one GB300 (or N replicas).
+
+One step = the whole decode-shaped sweep of an 8B-class decoder layer: the
+four layer shapes (K, N) = (4096, 6144), (4096, 4096), (4096, 28672),
+(14336, 4096) times M in {1, 4, 16}, asymmetric int4, group 128, fp16
+activations and output, fp32 accumulation: 12 GEMM launches through the
+C-ABI library, with the packed weights (offline repack, timed separately)
+and the activations resident in HBM.  Weight copies are rotated so that no
+launch finds its weights in L2 (distinct weight bytes per step exceed the
+L2 size; even and odd steps use disjoint copy sets).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(numpy dequant + float64 matmul) on the host cores on a column sample of the
+same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "decode_8b"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--tune", action="store_true", help="run tm_tune for every (shape, M) first")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def weight_bytes(K: int, N: int, group: int, symmetric: bool) -> float:
+    """Algorithmic weight bytes: 4-bit codes + 16-bit scale (+ 4-bit zero) per group."""
+    per_group = 2.0 + (0.0 if symmetric else 0.5)
+    return K * N / 2 + (K / group) * N * per_group
+
+
+def problem_bytes(M: int, K: int, N: int, group: int, symmetric: bool) -> float:
+    """Algorithmic bytes of one GEMM: weights + A (fp16) + C (fp16)."""
+    return weight_bytes(K, N, group, symmetric) + 2.0 * M * K + 2.0 * M * N
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "w4a16_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def gpu_id(dev) -> str:
+    """nvidia-smi -i selector of a torch device (its UUID when torch exposes it)."""
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (200 ms period)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows: list[list[str]] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        rows = [r for r in self.rows if len(r) >= 10]
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        loaded = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for name, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(loaded[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank: int, world: int):
+    import numpy as np
+    import torch
+
+    from w4a16_gemm_gb300 import binding, build, synth
+
+    build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[WORKLOAD]
+    dt = torch.float16
+    L2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    # inputs: quantized weights (synthetic, seeded), packed once per copy
+    shapes = list(wl.shapes)
+    problems = []          # (shape_idx, M)
+    for si in range(len(shapes)):
+        for M in wl.ms:
+            problems.append((si, M))
+    n_sets = 2
+    packed = {}            # (set, shape_idx, M) -> PackedW4
+    acts, outs = {}, {}
+    pack_times = {}
+    dev_inputs = {}
+    for si, (K, N) in enumerate(shapes):
+        qw = synth.weight(WORKLOAD, si)
+        p = binding.to_device(qw, dev)
+        dev_inputs[si] = p
+        for s in range(n_sets):
+            for M in wl.ms:
+                packed[(s, si, M)] = binding.pack(p.q, p.scales, p.zeros, qw.group)
+        # time the offline repack (a1) on its own
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record()
+        tmp = binding.pack(p.q, p.scales, p.zeros, qw.group)
+        ev1.record()
+        torch.cuda.synchronize()
+        pack_times[si] = ev0.elapsed_time(ev1) * 1e-3
+        tmp.free()
+        for M in wl.ms:
+            acts[(si, M)] = binding.acts_to_device(synth.activations(WORKLOAD, si, M), dt, dev)
+            outs[(si, M)] = torch.empty((M, N), dtype=dt, device=dev)
+    del dev_inputs
+    torch.cuda.synchronize()
+
+    if args.tune:
+        for si in range(len(shapes)):
+            binding.tune(packed[(0, si, wl.ms[0])], list(wl.ms))
+
+    variants = {(si, M): binding.select(packed[(0, si, M)], M) for si, M in problems}
+
+    def variant_name(v):
+        if v["kernel"] == "gemv":
+            return f"gemv_kernel<f16,{v['block_m']}>"
+        return f"tc_gemm_kernel<f16,{v['block_m']},{v['dq_warps']}>"
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch_step(step: int, events=None):
+        s = step % n_sets
+        for j, (si, M) in enumerate(problems):
+            if events is not None:
+                events[j][0].record(stream)
+            binding.gemm(acts[(si, M)], packed[(s, si, M)], out=outs[(si, M)], stream=stream)
+            if events is not None:
+                events[j][1].record(stream)
+
+    # warm-up (also sizes the split-K workspace of this stream outside capture)
+    with torch.cuda.stream(stream):
+        for w in range(max(args.warmup, 3)):
+            launch_step(w)
+    torch.cuda.synchronize()
+    binding.poll_error(stream)
+
+    K_steps = args.steps
+    # graph A: all K timed steps back to back (the `value` timing)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(K_steps):
+            launch_step(k)
+    # graph B: the same K steps with a timing-event pair around every launch
+    # (event record nodes), for per-kernel durations
+    external_ok = True
+    try:
+        ev = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+               for _ in problems] for _ in range(K_steps)]
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev, stream=stream):
+            for k in range(K_steps):
+                launch_step(k, ev[k])
+    except (TypeError, RuntimeError):
+        external_ok = False
+        ev = None
+        graph_ev = None
+    # clock-sampled warm replays, then the timed replays
+    sampler = ClockSampler(gpu_id(dev))
+    sampler.start()
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        graph.replay()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed = t0.elapsed_time(t1) * 1e-3
+    ev_elapsed = None
+    if graph_ev is not None:
+        t0.record(stream)
+        graph_ev.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        ev_elapsed = t0.elapsed_time(t1) * 1e-3
+    clocks = sampler.stop()
+    binding.poll_error(stream)
+
+    # per-launch durations
+    per = {}   # variant -> [total seconds, total algorithmic bytes, launches]
+    if external_ok:
+        for k in range(K_steps):
+            for j, (si, M) in enumerate(problems):
+                d = ev[k][j][0].elapsed_time(ev[k][j][1]) * 1e-3
+                K, N = shapes[si]
+                vname = variant_name(variants[(si, M)])
+                rec = per.setdefault(vname, [0.0, 0.0, 0])
+                rec[0] += d
+                rec[1] += problem_bytes(M, K, N, wl.group, wl.symmetric)
+                rec[2] += 1
+
+    # whole-job numbers
+    wbytes_step = sum(weight_bytes(*shapes[si], wl.group, wl.symmetric) for si, M in problems)
+    flops_step = sum(2.0 * M * shapes[si][0] * shapes[si][1] for si, M in problems)
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    value = world * K_steps * wbytes_step / elapsed / 1e9
+    ms_per_step = elapsed / K_steps * 1e3
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    a_host = {k: v.cpu().pin_memory() for k, v in acts.items()}
+    c_host = {k: torch.empty(v.shape, dtype=dt).pin_memory() for k, v in outs.items()}
+    h2d = sum(v.numel() * 2 for v in a_host.values())
+    d2h = sum(v.numel() * 2 for v in c_host.values())
+    a_dev = {k: torch.empty_like(v) for k, v in acts.items()}
+    with torch.cuda.stream(stream):
+        e_steps = max(10, K_steps // 4)
+        for w in range(3):
+            for si, M in problems:
+                a_dev[(si, M)].copy_(a_host[(si, M)], non_blocking=True)
+                binding.gemm(a_dev[(si, M)], packed[(w % n_sets, si, M)], out=outs[(si, M)], stream=stream)
+                c_host[(si, M)].copy_(outs[(si, M)], non_blocking=True)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(e_steps):
+            for si, M in problems:
+                a_dev[(si, M)].copy_(a_host[(si, M)], non_blocking=True)
+                binding.gemm(a_dev[(si, M)], packed[(k % n_sets, si, M)], out=outs[(si, M)],
+                             stream=stream)
+                c_host[(si, M)].copy_(outs[(si, M)], non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_s = e0.elapsed_time(e1) * 1e-3
+    e2e_value = world * e_steps * wbytes_step / e2e_s / 1e9
+
+    peaks, peak_src = load_peaks()
+    roof = None
+    if per:
+        dom = max(per, key=lambda k: per[k][0])
+        tot_s, tot_b, n_l = per[dom]
+        achieved = tot_b / tot_s / 1e9
+        traffic = None
+        tp = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tp):
+            with open(tp) as f:
+                tj = json.load(f)
+            ent = tj.get(WORKLOAD, {})
+            if ent.get("source_hash") == kernel_source_hash() and ent.get("kernel") == dom:
+                traffic = ent.get("dram_bytes_per_launch")
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "kernel": dom, "launches": n_l, "avg_launch_us": round(tot_s / n_l * 1e6, 3),
+                "algorithmic_bytes_per_launch": round(tot_b / n_l),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s"}
+    per_problem = None
+    if external_ok:
+        per_problem = []
+        for j, (si, M) in enumerate(problems):
+            ds = [ev[k][j][0].elapsed_time(ev[k][j][1]) * 1e-3 for k in range(K_steps)]
+            d = statistics.median(ds)
+            K, N = shapes[si]
+            per_problem.append({"K": K, "N": N, "M": M, "variant": variants[(si, M)],
+                                "us": round(d * 1e6, 2),
+                                "weight_gbs": round(weight_bytes(K, N, wl.group, wl.symmetric) / d / 1e9, 1),
+                                "tflops": round(2.0 * M * K * N / d / 1e12, 3)})
+
+    line = {
+        "metric": "W4A16 GEMM weight GB/s, 8B-class decode sweep (4 layer shapes x M in {1,4,16})",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K_steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1) fp16 activations; N(0,0.02) weights RTN-quantized to int4)",
+        "config": {"workload": "decode_8b: (K,N) in (4096,6144),(4096,4096),(4096,28672),(14336,4096); "
+                               "M in {1,4,16}; asym uint4 G=128 fp16 scales; fp16 in/out, fp32 accumulate",
+                   "launches_per_step": len(problems),
+                   "l2": f"inputs larger than L2: {n_sets} disjoint weight-copy sets, "
+                         f"{wbytes_step / 1e6:.0f} MB distinct weights per step vs L2 {L2 / 1e6:.0f} MB",
+                   "timing": "one CUDA graph of all timed steps, CUDA events on the launch stream",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tflops": round(world * K_steps * flops_step / elapsed / 1e12, 4),
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e_steps,
+                "how": "eager C-ABI calls via the Python binding; A copied from pinned host, C copied back, every call"},
+        "gpu_launches": K_steps * len(problems),
+        "ms_per_step_event_graph": None if ev_elapsed is None else round(ev_elapsed / K_steps * 1e3, 4),
+        "clocks": clocks,
+        "pack": {"seconds_per_shape": {f"{shapes[si][0]}x{shapes[si][1]}": round(t * 1e6, 1)
+                                       for si, t in pack_times.items()},
+                 "unit": "us", "note": "offline repack (tm_pack_w4), timed once per shape"},
+        "per_problem": per_problem,
+    }
+    return line
+
+
+# ------------------------------------------------------------- the oracle
+def oracle_sample_step(col_frac: float):
+    """Runs the oracle on a column sample of every problem of one step.
+
+    Returns (seconds, weight bytes processed)."""
+    import numpy as np
+
+    import oracle
+    from w4a16_gemm_gb300 import synth
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    total_t, total_b = 0.0, 0.0
+    for si, (K, N) in enumerate(wl.shapes):
+        qw = _ORACLE_CACHE.get(si)
+        if qw is None:
+            qw = synth.weight(WORKLOAD, si)
+            _ORACLE_CACHE[si] = qw
+        ncols = max(16, int(N * col_frac))
+        cols = slice(0, ncols)
+        for M in wl.ms:
+            a = _ORACLE_ACTS.setdefault((si, M), synth.activations(WORKLOAD, si, M))
+            t0 = time.perf_counter()
+            w = oracle.dequant_bits(qw.q[:, cols], qw.scales[:, cols], qw.zeros[:, cols], qw.group, qw.dtype)
+            c = oracle.gemm_ref(a, w, qw.dtype)
+            total_t += time.perf_counter() - t0
+            total_b += weight_bytes(K, ncols, qw.group, False)
+            del w, c
+    return total_t, total_b
+
+
+_ORACLE_CACHE: dict = {}
+_ORACLE_ACTS: dict = {}
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(target_s: float) -> dict:
+    probe_t, _ = oracle_sample_step(1 / 256)
+    frac = min(1.0, max(1 / 256, (target_s / max(probe_t, 1e-3)) / 256))
+    t, b = oracle_sample_step(frac)
+    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"all 12 problems of one decode_8b step restricted to the first "
+                      f"{frac * 100:.2f}% of the N columns; numpy dequant (RNE) + float64 matmul; "
+                      f"{t:.1f} s of CPU time"}
+
+
+def run_reference(args) -> dict:
+    K_steps, W = args.steps, args.warmup
+    probe_t, _ = oracle_sample_step(1 / 256)
+    budget = 120.0
+    per_step_target = budget / max(1, K_steps + W)
+    frac = min(1.0, max(1 / 1024, (per_step_target / max(probe_t, 1e-3)) / 256))
+    for _ in range(W):
+        oracle_sample_step(frac)
+    t_tot, b_tot = 0.0, 0.0
+    for _ in range(K_steps):
+        t, b = oracle_sample_step(frac)
+        t_tot += t
+        b_tot += b
+    value = b_tot / t_tot / 1e9
+    sample = (f"each step: all 12 decode_8b problems restricted to the first {frac * 100:.3f}% "
+              f"of the N columns; numpy dequant (RNE) + float64 matmul")
+    return {
+        "impl": "reference",
+        "metric": "W4A16 GEMM weight GB/s, 8B-class decode sweep (4 layer shapes x M in {1,4,16})",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": K_steps, "warmup": W,
+        "ms_per_step": round(t_tot / K_steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": "decode_8b (column sample), CPU oracle on the host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * tmw4.h -- C ABI of the GB300 (sm_103a) W4A16 GEMM library (libtmw4.so).
+ *
+ * The library implements the mixed-precision GEMM pipeline of the TurboMind
+ * engine ("Efficient Mixed-Precision Large Language Model Inference with
+ * TurboMind", arXiv 2508.15601; abstract: a GEMM pipeline made of "offline
+ * weight packing" and "online acceleration"):
+ *
+ *   offline:  tm_pack_w4     int4 codes + scales + zeros -> packed weight
+ *   online:   tm_gemm_w4a16  C[M,N] = A[M,K] * W[K,N],
+ *                            W[k,n] = T(s[k/G,n] * (q[k,n] - z[k/G,n]))
+ *
+ * Conventions used by every call:
+ *   - All matrices are row-major.  The logical weight W is [K, N]; A is
+ *     [M, K]; C is [M, N]; q is [K, N] (one code 0..15 per byte); scales and
+ *     zeros are [K/G, N].  T is the 16-bit float type of A, scales and C.
+ *   - "device" pointers are CUDA device addresses on the current device;
+ *     "host" pointers are ordinary CPU memory.  Streams are passed as
+ *     `void *` holding a cudaStream_t (NULL = the legacy default stream).
+ *   - Every call is stream-ordered and asynchronous unless stated; none
+ *     synchronises the device.  No call throws, exits or traps.  On a
+ *     non-OK status, tm_last_error() returns a message for the calling
+ *     thread.
+ *   - Conditions found on the device (a code byte above 15, a bounded wait
+ *     that gave up) are recorded in a per-device error word and reported by
+ *     tm_poll_error().
+ */
+#ifndef TMW4_H
+#define TMW4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TM_OK = 0,
+  TM_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or handle        */
+  TM_ERR_UNSUPPORTED = 2, /* valid request this build cannot run           */
+  TM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed             */
+  TM_ERR_OOM = 4,         /* device allocation failed                       */
+  TM_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up            */
+} tm_status;
+
+typedef enum { TM_F16 = 0, TM_BF16 = 1 } tm_dtype;
+
+/* Kernel families (tm_config.kernel). */
+enum {
+  TM_KERNEL_AUTO = 0, /* pick from the tuned table, else the built-in rule */
+  TM_KERNEL_GEMV = 1, /* CUDA-core split-K GEMV, M <= 8                    */
+  TM_KERNEL_TC = 2    /* tcgen05/TMEM/TMA kernel, any M                     */
+};
+
+/* A kernel variant: family, rows of A per CTA tile (TC: 16..256, a
+ * multiple of 16; GEMV: ignored) and the number of K splits (>= 1). */
+typedef struct {
+  int32_t kernel;
+  int32_t block_m;
+  int32_t split_k;
+  int32_t dq_warps; /* TC: dequant warps per CTA, 4 or 8 (0 = default) */
+} tm_config;
+
+/* Opaque packed weight, owned by the library until tm_packed_free. */
+typedef struct tm_packed tm_packed;
+
+/* Read-only view of a packed weight (for inspection and tests).
+ *
+ * Packed weight layout (the library's own Blackwell order; the pages'
+ * packing -- pith.science review, Figures 6 and 7 -- permutes each thread's
+ * eight int4 values into MMA order and stores fragments in load order):
+ *   qweight: K*N/2 bytes.  The weight is cut into 64x64 atoms; atom
+ *     (kb, na) covers k in [64kb, 64kb+64), n in [64na, 64na+64) and starts
+ *     at byte (kb*(N/64) + na)*2048.  An atom holds 512 little-endian 32-bit
+ *     words; word h*256 + nl*4 + j (h in {0,1}, nl in [0,64), j in [0,4))
+ *     holds q[64kb + 8(4h+j) + e][64na + nl] for e = 0..7, value e in bits
+ *     [4p, 4p+4) with p = (0,4,1,5,2,6,3,7)[e] -- the word order of
+ *     pith.science review Figures 23/24 (e7 e5 e3 e1 e6 e4 e2 e0).  Every
+ *     16-byte chunk is 32 consecutive K values of one column.
+ *   scales: [K/G][N] 16-bit values of type `dtype`, as given to tm_pack_w4.
+ *   zeros:  [K/G][N/2] bytes, column 2i in the low nibble, 2i+1 in the high
+ *     nibble; NULL for the symmetric format (implicit zero 8). */
+typedef struct {
+  int32_t K, N, group;
+  int32_t dtype;     /* tm_dtype */
+  int32_t symmetric; /* 1: no stored zeros, zero point 8 */
+  int32_t device;
+  const void *qweight; /* device */
+  const void *scales;  /* device */
+  const void *zeros;   /* device, NULL if symmetric */
+  size_t qweight_bytes, scales_bytes, zeros_bytes;
+} tm_packed_info;
+
+/* Offline repack (TurboMind paper, arXiv abstract: "offline weight
+ * packing"; pith.science review, Figures 6/7: steps (i)-(iv) load, place,
+ * permute and store fragments).
+ *   q      device, [K][N] uint8 codes 0..15 (a code > 15 is masked to 4
+ *          bits and reported by tm_poll_error as TM_ERR_INVALID_ARG)
+ *   scales device, [K/group][N] 16-bit values of type dtype
+ *   zeros  device, [K/group][N] uint8 zero points 0..15, or NULL for the
+ *          symmetric format (zero point 8)
+ *   K % group == 0, group in {64, 128}, K % 64 == 0, N % 128 == 0, K, N > 0;
+ *   all pointers 16-byte aligned.
+ *   On TM_OK *out receives a new handle; the inputs may be reused once
+ *   `stream` has passed this call.  The handle's storage is allocated with
+ *   cudaMallocAsync on `stream`. */
+tm_status tm_pack_w4(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N,
+                     int group, tm_dtype dtype, void *stream, tm_packed **out);
+
+/* Online GEMM (TurboMind paper, arXiv abstract: "online acceleration";
+ * pith.science review, Figure 9: dequantization overlapped with the MMA).
+ *   A  device, [M][K] values of the handle's dtype, 16-byte aligned
+ *   W  packed weight from tm_pack_w4 with matching K and N
+ *   C  device, [M][N] output of the handle's dtype (caller-allocated),
+ *      16-byte aligned; fp32 accumulation, one round-to-nearest-even at
+ *      the end.  Results do not depend on the split or launch order.
+ *   M == 0 is a no-op.  M <= 65535*256.
+ *   Uses a library-owned split-K workspace per (device, stream), grown on
+ *   demand; a call that would need to grow it while `stream` is being
+ *   captured into a CUDA graph returns TM_ERR_UNSUPPORTED -- make one call
+ *   of the same shape outside capture first.  Calls on the same stream are
+ *   ordered; calls on different streams use different workspaces. */
+tm_status tm_gemm_w4a16(const void *A, const tm_packed *W, void *C, int M, int N, int K,
+                        void *stream);
+
+/* As tm_gemm_w4a16 with an explicit kernel variant (cfg != NULL); used by
+ * the tuner, the tests and the benchmark.  TM_ERR_UNSUPPORTED if the
+ * variant cannot run this shape. */
+tm_status tm_gemm_w4a16_ex(const void *A, const tm_packed *W, void *C, int M, int N, int K,
+                           const tm_config *cfg, void *stream);
+
+/* Dequant-only: W_out [K][N] (device, handle's dtype) = T(s*(q - z)),
+ * bit-exact with a single round-to-nearest-even per element. */
+tm_status tm_dequant_w4(const tm_packed *W, void *W_out, void *stream);
+
+/* Releases a packed weight (stream-ordered cudaFreeAsync). NULL is OK. */
+tm_status tm_packed_free(tm_packed *W, void *stream);
+
+/* Fills *info (host) with the handle's shape and device pointers. */
+tm_status tm_packed_get(const tm_packed *W, tm_packed_info *info);
+
+/* The variant tm_gemm_w4a16 would run for this handle and M (host only). */
+tm_status tm_select(const tm_packed *W, int M, tm_config *out);
+
+/* Variant selection by measured throughput (the pages give no selection
+ * rule; it follows from the measured crossover between the GEMV and
+ * tensor-core kernels).  Times every legal variant for each M in Ms[0..nM)
+ * with CUDA events on `stream` (synchronises it), flushing L2 between
+ * timings, and records the fastest (ties: lowest index) in the process-wide
+ * table used by tm_gemm_w4a16.  If the environment variable TM_TUNE_CACHE
+ * names a file, the table is saved there.  best_out (host, may be NULL)
+ * receives nM configs. */
+tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *stream, tm_config *best_out);
+
+/* Loads/saves the tuned table (JSON lines) from/to a host path. */
+tm_status tm_tune_load(const char *path);
+tm_status tm_tune_save(const char *path);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word: TM_ERR_TIMEOUT if a bounded wait gave up, TM_ERR_INVALID_ARG if a
+ * code byte was above 15, TM_OK otherwise. */
+tm_status tm_poll_error(void *stream);
+
+/* Self-test of the bounded wait used by every kernel: launches one CTA
+ * that waits on a barrier nothing will complete, with a limit of
+ * `limit_ns` nanoseconds (1000..10^9).  The wait gives up, records
+ * TM_ERR_TIMEOUT in the error word and the kernel returns normally; read
+ * it with tm_poll_error. */
+tm_status tm_selftest_wait_timeout(long long limit_ns, void *stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char *tm_last_error(void);
+
+/* Library version string. */
+const char *tm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TMW4_H */

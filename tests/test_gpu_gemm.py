@@ -1,0 +1,227 @@
+"""GPU parity of the W4A16 GEMM against the CPU oracle.
+
+Tolerance (per element, fp32 accumulation): |C - C_ref| <= 1e-2 (|C_ref| +
+rms(C_ref)), C_ref the float64 oracle GEMM of A with W = RNE_T(s*(q-z)).
+Exact cases: q == z gives C == 0, one-hot rows reproduce W's rows, and
+power-of-two scales with small-integer activations give C == C_ref exactly.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._util import TORCH_DT, gemm_poisoned, bits_of, c_values, oracle_sampled, packed_from, sample_indices
+from w4a16_gemm_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _run(qw, a_bits, config=None):
+    W = packed_from(qw)
+    A = binding.acts_to_device(a_bits, TORCH_DT[qw.dtype])
+    C = gemm_poisoned(A, W, config=config)
+    torch.cuda.synchronize()
+    binding.poll_error()
+    return C, W
+
+
+def _variants(M):
+    out = []
+    if M <= 8:
+        out += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
+    for bm in (16, 32, 64, 128, 256):
+        for sk in (1, 3):
+            for dq in (4, 8):
+                if bm >= 128 and dq == 8 and sk == 3:
+                    continue
+                out.append(dict(kernel="tc", block_m=bm, split_k=sk, dq_warps=dq))
+    return out
+
+
+SMALL = [
+    # M, K, N, G, dtype, sym
+    (1, 512, 384, 128, "f16", False),
+    (3, 512, 256, 128, "bf16", False),
+    (16, 1024, 384, 64, "f16", True),
+    (17, 512, 256, 128, "f16", False),
+    (100, 768, 256, 128, "bf16", False),
+    (257, 512, 384, 64, "f16", True),
+]
+
+
+@pytest.mark.parametrize("M,K,N,G,dt,sym", SMALL)
+def test_small_all_variants(M, K, N, G, dt, sym):
+    qw, a = synth.random_problem(M + K + N, M, K, N, G, dt, sym,
+                                 act_dist="student_t3" if sym else "normal")
+    w = oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, dt)
+    c_ref = oracle.gemm_ref(a, w, dt)
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, TORCH_DT[dt])
+    for cfg in _variants(M):
+        C = gemm_poisoned(A, W, config=cfg)
+        torch.cuda.synchronize()
+        binding.poll_error()
+        r = oracle.max_err_ratio(c_values(C), c_ref, rel=TOL)
+        assert r <= 1.0, (cfg, r)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64, 200])
+def test_auto_selection_is_deterministic(M):
+    qw, a = synth.random_problem(11, M, 2048, 512)
+    C1, W = _run(qw, a)
+    A = binding.acts_to_device(a, torch.float16)
+    C2 = gemm_poisoned(A, W)
+    torch.cuda.synchronize()
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, 128, "f16"), "f16")
+    assert oracle.max_err_ratio(c_values(C1), c_ref, rel=TOL) <= 1.0
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_q_equal_zero_gives_exact_zero(dt):
+    M, K, N, G = 40, 512, 256, 128
+    qw, a = synth.random_problem(3, M, K, N, G, dt)
+    q = np.repeat(qw.zeros, G, axis=0)
+    qz = synth.QuantWeight(q, qw.scales, qw.zeros, G, dt)
+    W = packed_from(qz)
+    A = binding.acts_to_device(a, TORCH_DT[dt])
+    for cfg in [None, dict(kernel="gemv", split_k=2) if M <= 8 else None,
+                dict(kernel="tc", block_m=64, split_k=2)]:
+        C = gemm_poisoned(A, W, config=cfg)
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(C.float()) == 0
+
+
+def test_one_hot_rows_reproduce_dequantized_weight():
+    K, N, G = 512, 256, 128
+    qw, _ = synth.random_problem(4, 1, K, N, G)
+    w = oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, "f16")
+    ks = [0, 1, 63, 64, 127, 128, 255, 256, 511]
+    a = np.zeros((len(ks), K), np.uint16)
+    for i, k in enumerate(ks):
+        a[i, k] = 0x3C00
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, torch.float16)
+    for cfg in [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=4),
+                dict(kernel="tc", block_m=16, split_k=1), dict(kernel="tc", block_m=16, split_k=3),
+                dict(kernel="tc", block_m=128, split_k=1, dq_warps=8)]:
+        if cfg["kernel"] == "gemv" and len(ks) > 8:
+            continue
+        C = gemm_poisoned(A, W, config=cfg)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits_of(C), w[ks]), cfg
+
+
+def test_identity_activation_reproduces_weight():
+    """A = I (M = K = 256): C == W exactly (tensor-core path)."""
+    K = N = 256
+    qw, _ = synth.random_problem(6, 1, K, N, 128)
+    w = oracle.dequant_bits(qw.q, qw.scales, qw.zeros, 128, "f16")
+    a = np.where(np.eye(K, dtype=bool), np.uint16(0x3C00), np.uint16(0))
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, torch.float16)
+    for bm in (64, 128, 256):
+        C = gemm_poisoned(A, W, config=dict(kernel="tc", block_m=bm))
+        torch.cuda.synchronize()
+        assert np.array_equal(bits_of(C), w), bm
+
+
+@pytest.mark.parametrize("M", [1, 5, 48, 300])
+def test_power_of_two_scales_are_exact(M):
+    """Scales 2^-e and integer activations keep every partial sum exact."""
+    K, N, G = 512, 256, 64
+    rng = np.random.default_rng(M)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    z = rng.integers(6, 10, size=(K // G, N), dtype=np.uint8)
+    s = oracle.rne_f16_bits(np.exp2(-rng.integers(6, 10, size=(K // G, N)).astype(np.float64)))
+    a_int = rng.integers(-2, 3, size=(M, K))
+    a_int[rng.random((M, K)) < 0.75] = 0
+    a = oracle.rne_f16_bits(a_int.astype(np.float64))
+    qw = synth.QuantWeight(q, s, z, G, "f16")
+    c_ref = oracle.gemm_ref(a, oracle.dequant_bits(q, s, z, G, "f16"), "f16")
+    assert np.all(np.abs(c_ref) < 2048)
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, torch.float16)
+    cfgs = [None, dict(kernel="tc", block_m=16, split_k=4), dict(kernel="tc", block_m=64, split_k=2),
+            dict(kernel="tc", block_m=256)]
+    if M <= 8:
+        cfgs += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
+    for cfg in cfgs:
+        C = gemm_poisoned(A, W, config=cfg)
+        torch.cuda.synchronize()
+        assert np.array_equal(c_values(C), c_ref), cfg
+
+
+def test_symmetric_equals_asymmetric_with_zero_eight():
+    M, K, N, G = 24, 512, 256, 64
+    qw, a = synth.random_problem(8, M, K, N, G, "f16", True)
+    Ws = packed_from(qw)
+    Wa = packed_from(synth.QuantWeight(qw.q, qw.scales, np.full((K // G, N), 8, np.uint8), G, "f16"))
+    A = binding.acts_to_device(a, torch.float16)
+    assert torch.equal(binding.dequant(Ws).view(torch.int16), binding.dequant(Wa).view(torch.int16))
+    for cfg in [None, dict(kernel="tc", block_m=32, split_k=2)]:
+        Cs = gemm_poisoned(A, Ws, config=cfg)
+        Ca = gemm_poisoned(A, Wa, config=cfg)
+        torch.cuda.synchronize()
+        assert torch.equal(Cs.view(torch.int16), Ca.view(torch.int16))
+
+
+def test_m_zero_is_noop_and_argument_errors():
+    qw, a = synth.random_problem(9, 4, 256, 256)
+    W = packed_from(qw)
+    A = torch.zeros((0, 256), dtype=torch.float16, device="cuda")
+    C = gemm_poisoned(A, W)
+    assert C.shape == (0, 256)
+    A = binding.acts_to_device(a, torch.float16)
+    A9 = binding.acts_to_device(np.zeros((9, 256), np.uint16), torch.float16)
+    with pytest.raises(binding.TmError) as e:
+        binding.gemm(A9, W, config=dict(kernel="gemv"))     # GEMV takes M <= 8
+    assert e.value.status == binding.TM_ERR_UNSUPPORTED
+    with pytest.raises(binding.TmError) as e:
+        binding.gemm(A, W, config=dict(kernel="tc", block_m=48))
+    assert e.value.status == binding.TM_ERR_UNSUPPORTED
+    with pytest.raises(binding.TmError) as e:
+        binding.gemm(A, W, config=dict(kernel="tc", block_m=16, split_k=5))
+    assert e.value.status == binding.TM_ERR_UNSUPPORTED
+    Abig = torch.zeros(4 * 256 + 8, dtype=torch.float16, device="cuda")[1:1 + 4 * 256].view(4, 256)
+    with pytest.raises(binding.TmError) as e:
+        gemm_poisoned(Abig, W)
+    assert e.value.status == binding.TM_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- full size
+FULL = [(wl, si, M) for wl in ("decode_8b", "prefill_8b", "class_70b", "sym_g64")
+        for si in range(len(synth.WORKLOADS[wl].shapes)) for M in synth.WORKLOADS[wl].ms]
+
+
+@pytest.fixture(scope="module")
+def weight_cache():
+    cache = {}
+    yield cache
+    cache.clear()
+
+
+@pytest.mark.parametrize("wl,si,M", FULL, ids=lambda x: str(x))
+def test_full_size_sampled(wl, si, M, weight_cache):
+    """Every (workload, shape, M) at full size, in the launch configuration the
+    benchmark times (tm_gemm_w4a16's own selection); sampled rows and columns
+    are checked against the oracle."""
+    key = (wl, si)
+    if key not in weight_cache:
+        weight_cache.clear()
+        qw = synth.weight(wl, si)
+        weight_cache[key] = (qw, packed_from(qw))
+    qw, W = weight_cache[key]
+    a = synth.activations(wl, si, M)
+    A = binding.acts_to_device(a, TORCH_DT[qw.dtype])
+    C = gemm_poisoned(A, W)
+    torch.cuda.synchronize()
+    binding.poll_error()
+    rows = sample_indices(M, 96, seed=M)
+    cols = sample_indices(qw.N, 192, seed=qw.N + si)
+    c_ref = oracle_sampled(qw, a, rows, cols)
+    r = oracle.max_err_ratio(c_values(C, rows, cols), c_ref, rel=TOL)
+    assert r <= 1.0, r

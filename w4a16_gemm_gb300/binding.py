@@ -1,0 +1,270 @@
+"""ctypes binding of libtmw4.so (argument marshalling only).
+
+Every step of the W4A16 path runs in the library's CUDA kernels; this module
+turns torch tensors into device pointers and the current CUDA stream into a
+``cudaStream_t``, calls the C ABI declared in ``include/tmw4.h`` and raises
+:class:`TmError` on a non-OK status.  There is no fallback: if the library is
+missing, :func:`lib` raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtmw4.so")
+
+TM_OK, TM_ERR_INVALID_ARG, TM_ERR_UNSUPPORTED, TM_ERR_CUDA, TM_ERR_OOM, TM_ERR_TIMEOUT = range(6)
+TM_F16, TM_BF16 = 0, 1
+TM_KERNEL_AUTO, TM_KERNEL_GEMV, TM_KERNEL_TC = 0, 1, 2
+STATUS_NAMES = {0: "TM_OK", 1: "TM_ERR_INVALID_ARG", 2: "TM_ERR_UNSUPPORTED", 3: "TM_ERR_CUDA",
+                4: "TM_ERR_OOM", 5: "TM_ERR_TIMEOUT"}
+
+
+class TmError(RuntimeError):
+    """A non-OK tm_status, with the library's message."""
+
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class TmConfig(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("block_m", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("dq_warps", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {"kernel": {1: "gemv", 2: "tc"}.get(self.kernel, self.kernel),
+                "block_m": self.block_m, "split_k": self.split_k, "dq_warps": self.dq_warps}
+
+
+class TmPackedInfo(ctypes.Structure):
+    _fields_ = [("K", ctypes.c_int32), ("N", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("symmetric", ctypes.c_int32), ("device", ctypes.c_int32),
+                ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p),
+                ("qweight_bytes", ctypes.c_size_t), ("scales_bytes", ctypes.c_size_t),
+                ("zeros_bytes", ctypes.c_size_t)]
+
+
+_LIB = None
+
+#: (name, restype, argtypes) of every entry point in include/tmw4.h
+_VP, _I, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+SIGNATURES = [
+    ("tm_pack_w4", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
+    ("tm_gemm_w4a16", _I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
+    ("tm_gemm_w4a16_ex", _I, [_VP, _VP, _VP, _I, _I, _I, ctypes.POINTER(TmConfig), _VP]),
+    ("tm_dequant_w4", _I, [_VP, _VP, _VP]),
+    ("tm_packed_free", _I, [_VP, _VP]),
+    ("tm_packed_get", _I, [_VP, ctypes.POINTER(TmPackedInfo)]),
+    ("tm_select", _I, [_VP, _I, ctypes.POINTER(TmConfig)]),
+    ("tm_tune", _I, [ctypes.POINTER(_I), _I, _VP, _VP, ctypes.POINTER(TmConfig)]),
+    ("tm_tune_load", _I, [ctypes.c_char_p]),
+    ("tm_tune_save", _I, [ctypes.c_char_p]),
+    ("tm_poll_error", _I, [_VP]),
+    ("tm_selftest_wait_timeout", _I, [_LL, _VP]),
+    ("tm_last_error", ctypes.c_char_p, []),
+    ("tm_version", ctypes.c_char_p, []),
+]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libtmw4.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m w4a16_gemm_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int) -> None:
+    if status != TM_OK:
+        raise TmError(status, lib().tm_last_error().decode())
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+_DT = {torch.float16: TM_F16, torch.bfloat16: TM_BF16}
+_TORCH_DT = {TM_F16: torch.float16, TM_BF16: torch.bfloat16}
+
+
+class PackedW4:
+    """Library-owned packed int4 weight (freed on ``free()`` or garbage collection)."""
+
+    def __init__(self, handle: int, K: int, N: int, group: int, dtype: torch.dtype, symmetric: bool,
+                 device: torch.device):
+        self.handle = handle
+        self.K, self.N, self.group, self.dtype = K, N, group, dtype
+        self.symmetric = symmetric
+        self.device = device
+
+    def info(self) -> TmPackedInfo:
+        inf = TmPackedInfo()
+        _check(lib().tm_packed_get(self.handle, ctypes.byref(inf)))
+        return inf
+
+    def free(self, stream=None) -> None:
+        if self.handle:
+            with torch.cuda.device(self.device):
+                _check(lib().tm_packed_free(self.handle, _stream(stream)))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if self.handle and _LIB is not None:
+                with torch.cuda.device(self.device):
+                    _LIB.tm_packed_free(self.handle, None)
+                self.handle = None
+        except Exception:  # interpreter shutdown
+            pass
+
+    def raw_bytes(self) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor | None]:
+        """Device copies of (qweight u8, scales u8, zeros u8 or None) for inspection."""
+        inf = self.info()
+        torch.cuda.synchronize(self.device)
+        out = []
+        for ptr, n in ((inf.qweight, inf.qweight_bytes), (inf.scales, inf.scales_bytes),
+                       (inf.zeros, inf.zeros_bytes)):
+            if not ptr:
+                out.append(None)
+                continue
+            out.append(_copy_device_range(ptr, n, self.device))
+        return tuple(out)
+
+
+class _DevBuf:
+    """Exposes a raw device range through __cuda_array_interface__ (view; never written through)."""
+
+    def __init__(self, ptr: int, nbytes: int):
+        self.__cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
+def _copy_device_range(ptr: int, nbytes: int, device) -> torch.Tensor:
+    """A torch copy of nbytes at device address ptr."""
+    view = torch.as_tensor(_DevBuf(ptr, nbytes), device=device)
+    return view.clone()
+
+
+def pack(q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | None, group: int,
+         stream=None) -> PackedW4:
+    """tm_pack_w4: q [K,N] uint8, scales [K/G,N] fp16/bf16, zeros [K/G,N] uint8 or None."""
+    if q.dtype != torch.uint8 or q.dim() != 2 or not q.is_cuda:
+        raise ValueError("q must be a 2-D uint8 CUDA tensor")
+    if scales.dtype not in _DT:
+        raise ValueError("scales must be float16 or bfloat16")
+    K, N = q.shape
+    q = q.contiguous()
+    scales = scales.contiguous()
+    zp = None
+    if zeros is not None:
+        zeros = zeros.contiguous()
+        zp = zeros.data_ptr()
+    h = ctypes.c_void_p()
+    with torch.cuda.device(q.device):
+        _check(lib().tm_pack_w4(q.data_ptr(), scales.data_ptr(), zp, K, N, group, _DT[scales.dtype],
+                                _stream(stream), ctypes.byref(h)))
+    return PackedW4(h.value, K, N, group, scales.dtype, zeros is None, q.device)
+
+
+def gemm(A: torch.Tensor, W: PackedW4, out: torch.Tensor | None = None, config: dict | None = None,
+         stream=None) -> torch.Tensor:
+    """tm_gemm_w4a16 (or _ex with an explicit variant): C = A @ dequant(W)."""
+    if A.dim() != 2 or A.dtype != W.dtype or not A.is_cuda:
+        raise ValueError("A must be a 2-D CUDA tensor of the weight's dtype")
+    M, K = A.shape
+    A = A.contiguous()
+    if out is None:
+        out = torch.empty((M, W.N), dtype=W.dtype, device=A.device)
+    st = _stream(stream)
+    if config is None:
+        _check(lib().tm_gemm_w4a16(A.data_ptr(), W.handle, out.data_ptr(), M, W.N, K, st))
+    else:
+        c = make_config(**config)
+        _check(lib().tm_gemm_w4a16_ex(A.data_ptr(), W.handle, out.data_ptr(), M, W.N, K,
+                                      ctypes.byref(c), st))
+    return out
+
+
+def make_config(kernel="tc", block_m=16, split_k=1, dq_warps=0) -> TmConfig:
+    k = {"auto": TM_KERNEL_AUTO, "gemv": TM_KERNEL_GEMV, "tc": TM_KERNEL_TC}.get(kernel, kernel)
+    return TmConfig(int(k), int(block_m), int(split_k), int(dq_warps))
+
+
+def dequant(W: PackedW4, stream=None) -> torch.Tensor:
+    """tm_dequant_w4: the full [K, N] 16-bit weight."""
+    out = torch.empty((W.K, W.N), dtype=W.dtype, device=W.device)
+    _check(lib().tm_dequant_w4(W.handle, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def select(W: PackedW4, M: int) -> dict:
+    """The variant tm_gemm_w4a16 runs for this weight and M."""
+    c = TmConfig()
+    _check(lib().tm_select(W.handle, int(M), ctypes.byref(c)))
+    return c.as_dict()
+
+
+def tune(W: PackedW4, Ms, stream=None) -> list[dict]:
+    """tm_tune: measure every legal variant for each M; returns the chosen variants."""
+    Ms = [int(m) for m in Ms]
+    arr = (ctypes.c_int * len(Ms))(*Ms)
+    best = (TmConfig * len(Ms))()
+    _check(lib().tm_tune(arr, len(Ms), W.handle, _stream(stream), best))
+    return [b.as_dict() for b in best]
+
+
+def poll_error(stream=None) -> None:
+    """tm_poll_error: raise TmError if a device-side condition was recorded."""
+    _check(lib().tm_poll_error(_stream(stream)))
+
+
+def poll_status(stream=None) -> int:
+    """tm_poll_error as a plain status code."""
+    return int(lib().tm_poll_error(_stream(stream)))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(lib().tm_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def version() -> str:
+    return lib().tm_version().decode()
+
+
+@dataclass
+class Problem:
+    """Device tensors of one quantized weight (helper for tests and the bench)."""
+
+    q: torch.Tensor
+    scales: torch.Tensor
+    zeros: torch.Tensor | None
+    group: int
+    dtype: torch.dtype
+
+
+def to_device(qw, device="cuda") -> Problem:
+    """Moves a synth.QuantWeight to the GPU as torch tensors."""
+    dt = torch.float16 if qw.dtype == "f16" else torch.bfloat16
+    q = torch.from_numpy(qw.q).to(device)
+    s = torch.from_numpy(qw.scales.view("int16")).to(device).view(dt)
+    z = None if qw.zeros is None else torch.from_numpy(qw.zeros).to(device)
+    return Problem(q, s, z, qw.group, dt)
+
+
+def acts_to_device(a_bits, dtype: torch.dtype, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(a_bits.view("int16")).to(device).view(dtype)

@@ -1,0 +1,711 @@
+// api.cu -- the C ABI of libtmw4 (declared in include/tmw4.h): argument
+// validation, the packed-weight handle, the per-device error word, the
+// per-(device, stream) split-K workspace, TMA descriptor creation, variant
+// selection and the measured-throughput tuner.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "kernels.h"
+#include "tmw4.h"
+#include "tmw4_device.cuh"
+
+using namespace tmw4;
+
+// ----------------------------------------------------------------- handle
+static constexpr uint32_t kPackedMagic = 0x34574D54u;  // "TMW4"
+
+struct tm_packed {
+  uint32_t magic;
+  int K, N, group;
+  tm_dtype dtype;
+  int symmetric;
+  int device;
+  uint8_t *qw;
+  uint16_t *scales;
+  uint8_t *zeros;
+  size_t qw_bytes, scales_bytes, zeros_bytes;
+};
+
+// ------------------------------------------------------------ last error
+static thread_local std::string g_last_error;
+
+static tm_status fail(tm_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+static tm_status fail_cuda(cudaError_t e, const char *what) {
+  return fail(e == cudaErrorMemoryAllocation ? TM_ERR_OOM : TM_ERR_CUDA, "%s: %s (%s)", what,
+              cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define TM_CUDA(call, what)                      \
+  do {                                           \
+    cudaError_t _e = (call);                     \
+    if (_e != cudaSuccess) return fail_cuda(_e, what); \
+  } while (0)
+
+// Bounded waits give up after this long (nanoseconds); TM_WAIT_LIMIT_NS
+// overrides it.  No legitimate wait comes near it.
+static unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char *e = getenv("TM_WAIT_LIMIT_NS");
+    unsigned long long x = e ? strtoull(e, nullptr, 10) : 0ull;
+    return (x >= 1000ull && x <= 60000000000ull) ? x : 4000000000ull;
+  }();
+  return v;
+}
+
+// --------------------------------------------------- per-device state
+static std::mutex g_mu;
+static constexpr int kMaxDevices = 64;
+static unsigned int *g_err_word[kMaxDevices] = {};
+
+static tm_status current_device(int *dev) {
+  TM_CUDA(cudaGetDevice(dev), "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(TM_ERR_UNSUPPORTED, "device index %d", *dev);
+  return TM_OK;
+}
+
+static tm_status error_word(int dev, unsigned int **out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_word[dev] == nullptr) {
+    unsigned int *p = nullptr;
+    TM_CUDA(cudaMalloc(&p, sizeof(unsigned int)), "cudaMalloc(error word)");
+    TM_CUDA(cudaMemset(p, 0, sizeof(unsigned int)), "cudaMemset(error word)");
+    g_err_word[dev] = p;
+  }
+  *out = g_err_word[dev];
+  return TM_OK;
+}
+
+struct Workspace {
+  float *ws = nullptr;
+  size_t ws_bytes = 0;
+  unsigned int *counters = nullptr;
+  size_t n_counters = 0;
+};
+static std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+static bool stream_capturing(cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return false;
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+// Workspace of (dev, st) with at least the given sizes; grows outside capture.
+static tm_status get_workspace(int dev, cudaStream_t st, size_t ws_bytes, size_t n_counters,
+                               Workspace **out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace &w = g_ws[{dev, st}];
+  if (w.ws_bytes < ws_bytes || w.n_counters < n_counters) {
+    if (stream_capturing(st))
+      return fail(TM_ERR_UNSUPPORTED,
+                  "split-K workspace must grow (%zu B) while the stream is being captured; "
+                  "run this shape once outside capture first",
+                  ws_bytes);
+    // the old buffers may still be in use by queued work on this stream
+    TM_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+    if (w.ws_bytes < ws_bytes) {
+      if (w.ws) cudaFree(w.ws);
+      w.ws = nullptr;
+      w.ws_bytes = 0;
+      size_t sz = std::max(ws_bytes, static_cast<size_t>(1) << 20);
+      TM_CUDA(cudaMalloc(&w.ws, sz), "cudaMalloc(split-K workspace)");
+      w.ws_bytes = sz;
+    }
+    if (w.n_counters < n_counters) {
+      if (w.counters) cudaFree(w.counters);
+      w.counters = nullptr;
+      w.n_counters = 0;
+      size_t n = std::max(n_counters, static_cast<size_t>(4096));
+      TM_CUDA(cudaMalloc(&w.counters, n * sizeof(unsigned int)), "cudaMalloc(counters)");
+      TM_CUDA(cudaMemsetAsync(w.counters, 0, n * sizeof(unsigned int), st), "cudaMemsetAsync");
+      TM_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+      w.n_counters = n;
+    }
+  }
+  *out = &w;
+  return TM_OK;
+}
+
+// ------------------------------------------------------------ TMA encode
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static tm_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr)
+      return fail(TM_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *fn = g_encode;
+  return TM_OK;
+}
+
+// 2-D map over A [M][K] (K innermost), box 64 x block_m, 128-byte swizzle;
+// rows past M read as zero.
+static tm_status encode_act_map(const void *A, int M, int K, bool bf16, int block_m,
+                                CUtensorMap *map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  tm_status s = get_encoder(&enc);
+  if (s != TM_OK) return s;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_m)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   2, const_cast<void *>(A), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return TM_OK;
+}
+
+// ------------------------------------------------------------ validation
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static tm_status check_handle(const tm_packed *W) {
+  if (W == nullptr) return fail(TM_ERR_INVALID_ARG, "packed weight handle is NULL");
+  if (W->magic != kPackedMagic) return fail(TM_ERR_INVALID_ARG, "not a packed weight handle");
+  return TM_OK;
+}
+
+// -------------------------------------------------------- variant choice
+struct TuneKey {
+  int N, K, group, dtype, sym, M;
+  bool operator<(const TuneKey &o) const {
+    return std::tie(N, K, group, dtype, sym, M) < std::tie(o.N, o.K, o.group, o.dtype, o.sym, o.M);
+  }
+};
+struct TuneVal {
+  tm_config cfg;
+  double us;
+};
+static std::map<TuneKey, TuneVal> g_tune;
+static bool g_tune_loaded = false;
+
+static int sm_count(int dev) {
+  static int cached[kMaxDevices] = {};
+  if (cached[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
+static int gemv_rows_tmpl(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+// Is cfg runnable for this shape?  (Fills defaults for zero fields.)
+static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::string *why) {
+  const int KB = W->K / 64;
+  if (c->split_k <= 0) c->split_k = 1;
+  if (c->split_k > KB) {
+    if (why) *why = "split_k larger than K/64";
+    return false;
+  }
+  if (c->kernel == TM_KERNEL_GEMV) {
+    if (M > 8) {
+      if (why) *why = "GEMV handles M <= 8";
+      return false;
+    }
+    const int kb_per = (KB + c->split_k - 1) / c->split_k;
+    if (gemv_smem_bytes(gemv_rows_tmpl(M), kb_per) > 200 * 1024) {
+      if (why) *why = "GEMV K range too long for shared memory; raise split_k";
+      return false;
+    }
+    c->block_m = gemv_rows_tmpl(M);
+    c->dq_warps = 0;
+    return true;
+  }
+  if (c->kernel == TM_KERNEL_TC) {
+    if (c->block_m != 16 && c->block_m != 32 && c->block_m != 64 && c->block_m != 128 &&
+        c->block_m != 256) {
+      if (why) *why = "TC block_m must be 16, 32, 64, 128 or 256";
+      return false;
+    }
+    if (c->dq_warps == 0) c->dq_warps = 4;
+    if (c->dq_warps != 4 && c->dq_warps != 8) {
+      if (why) *why = "TC dq_warps must be 4 or 8";
+      return false;
+    }
+    if ((M + c->block_m - 1) / c->block_m > 65535) {
+      if (why) *why = "too many row tiles";
+      return false;
+    }
+    return true;
+  }
+  if (why) *why = "unknown kernel family";
+  return false;
+}
+
+// Built-in rule used when the tuned table has no entry for this shape.
+static tm_config default_config(const tm_packed *W, int M, int dev) {
+  tm_config c{};
+  c.kernel = TM_KERNEL_TC;
+  c.block_m = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  c.dq_warps = 4;
+  const int KB = W->K / 64;
+  const int sms = sm_count(dev);
+  const int per_sm = c.block_m <= 64 ? 2 : 1;
+  const int tiles = (W->N / 128) * ((M + c.block_m - 1) / c.block_m);
+  int s = 1;
+  if (tiles < sms * per_sm) {
+    s = (sms * per_sm + tiles - 1) / tiles;
+    s = std::min(s, std::max(1, KB / 4));
+    s = std::min(s, 32);
+  }
+  c.split_k = s;
+  std::string why;
+  normalize_config(W, M, &c, &why);
+  return c;
+}
+
+static void load_tune_env_once();
+
+static tm_config select_config(const tm_packed *W, int M, int dev) {
+  load_tune_env_once();
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_tune.find(TuneKey{W->N, W->K, W->group, (int)W->dtype, W->symmetric, M});
+    if (it != g_tune.end()) return it->second.cfg;
+  }
+  return default_config(W, M, dev);
+}
+
+// ------------------------------------------------------------ GEMM launch
+static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, const tm_config &cfg,
+                          cudaStream_t st) {
+  unsigned int *err = nullptr;
+  tm_status s = error_word(W->device, &err);
+  if (s != TM_OK) return s;
+  const int KB = W->K / 64;
+  GemmArgs a{};
+  a.qw = W->qw;
+  a.scales = W->scales;
+  a.zeros = W->symmetric ? nullptr : W->zeros;
+  a.A = static_cast<const uint16_t *>(A);
+  a.C = static_cast<uint16_t *>(C);
+  a.err = err;
+  a.M = M;
+  a.N = W->N;
+  a.K = W->K;
+  a.group = W->group;
+  a.splits = cfg.split_k;
+  a.kb_per_split = (KB + cfg.split_k - 1) / cfg.split_k;
+  // trailing splits may be empty: shrink so every split has work
+  a.splits = (KB + a.kb_per_split - 1) / a.kb_per_split;
+  a.limit_ns = wait_limit_ns();
+  const bool bf16 = W->dtype == TM_BF16;
+  if (a.splits > 1) {
+    Workspace *ws = nullptr;
+    const size_t ws_bytes = sizeof(float) * static_cast<size_t>(a.splits) * M * W->N;
+    const size_t tiles = cfg.kernel == TM_KERNEL_GEMV
+                             ? static_cast<size_t>(W->N / 64)
+                             : static_cast<size_t>(W->N / 128) * ((M + cfg.block_m - 1) / cfg.block_m);
+    s = get_workspace(W->device, st, ws_bytes, tiles, &ws);
+    if (s != TM_OK) return s;
+    a.ws = ws->ws;
+    a.counters = ws->counters;
+  }
+  cudaError_t e;
+  if (cfg.kernel == TM_KERNEL_GEMV) {
+    e = launch_gemv(a, bf16, gemv_rows_tmpl(M), st);
+  } else {
+    CUtensorMap map;
+    s = encode_act_map(A, M, W->K, bf16, cfg.block_m, &map);
+    if (s != TM_OK) return s;
+    e = launch_tc(a, map, bf16, cfg.block_m, cfg.dq_warps, st);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return TM_OK;
+}
+
+static tm_status check_gemm_args(const void *A, const tm_packed *W, const void *C, int M, int N,
+                                 int K) {
+  tm_status s = check_handle(W);
+  if (s != TM_OK) return s;
+  if (N != W->N || K != W->K)
+    return fail(TM_ERR_INVALID_ARG, "shape (N=%d, K=%d) does not match the packed weight (N=%d, K=%d)",
+                N, K, W->N, W->K);
+  if (M < 0) return fail(TM_ERR_INVALID_ARG, "M must be >= 0");
+  if (M > 65535 * 256) return fail(TM_ERR_UNSUPPORTED, "M too large");
+  if (M == 0) return TM_OK;
+  if (A == nullptr || C == nullptr) return fail(TM_ERR_INVALID_ARG, "A and C must not be NULL");
+  if (!aligned16(A) || !aligned16(C))
+    return fail(TM_ERR_INVALID_ARG, "A and C must be 16-byte aligned");
+  int dev = -1;
+  s = current_device(&dev);
+  if (s != TM_OK) return s;
+  if (dev != W->device)
+    return fail(TM_ERR_INVALID_ARG, "packed weight lives on device %d, current device is %d",
+                W->device, dev);
+  return TM_OK;
+}
+
+// ================================================================ C ABI
+extern "C" {
+
+const char *tm_version(void) { return "tmw4 0.1 (sm_103a)"; }
+
+const char *tm_last_error(void) { return g_last_error.c_str(); }
+
+tm_status tm_pack_w4(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N,
+                     int group, tm_dtype dtype, void *stream, tm_packed **out) {
+  if (out == nullptr) return fail(TM_ERR_INVALID_ARG, "out must not be NULL");
+  *out = nullptr;
+  if (q == nullptr || scales == nullptr) return fail(TM_ERR_INVALID_ARG, "q and scales must not be NULL");
+  if (dtype != TM_F16 && dtype != TM_BF16) return fail(TM_ERR_INVALID_ARG, "dtype must be TM_F16 or TM_BF16");
+  if (K <= 0 || N <= 0) return fail(TM_ERR_INVALID_ARG, "K and N must be positive");
+  if (group != 64 && group != 128) return fail(TM_ERR_INVALID_ARG, "group must be 64 or 128");
+  if (K % group != 0) return fail(TM_ERR_INVALID_ARG, "K (%d) must be a multiple of group (%d)", K, group);
+  if (N % 128 != 0) return fail(TM_ERR_INVALID_ARG, "N (%d) must be a multiple of 128", N);
+  if (!aligned16(q) || !aligned16(scales) || (zeros && !aligned16(zeros)))
+    return fail(TM_ERR_INVALID_ARG, "q, scales and zeros must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = -1;
+  tm_status s = current_device(&dev);
+  if (s != TM_OK) return s;
+  unsigned int *err = nullptr;
+  s = error_word(dev, &err);
+  if (s != TM_OK) return s;
+
+  tm_packed *W = new tm_packed{};
+  W->magic = kPackedMagic;
+  W->K = K;
+  W->N = N;
+  W->group = group;
+  W->dtype = dtype;
+  W->symmetric = zeros == nullptr ? 1 : 0;
+  W->device = dev;
+  W->qw_bytes = static_cast<size_t>(K) * N / 2;
+  W->scales_bytes = static_cast<size_t>(K / group) * N * 2;
+  W->zeros_bytes = zeros ? static_cast<size_t>(K / group) * (N / 2) : 0;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&W->qw), W->qw_bytes, st);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void **>(&W->scales), W->scales_bytes, st);
+  if (e == cudaSuccess && zeros)
+    e = cudaMallocAsync(reinterpret_cast<void **>(&W->zeros), W->zeros_bytes, st);
+  if (e == cudaSuccess) e = launch_repack(q, W->qw, K, N, err, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(W->scales, scales, W->scales_bytes, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && zeros) e = launch_pack_zeros(zeros, W->zeros, K / group, N, err, st);
+  if (e != cudaSuccess) {
+    if (W->qw) cudaFreeAsync(W->qw, st);
+    if (W->scales) cudaFreeAsync(W->scales, st);
+    if (W->zeros) cudaFreeAsync(W->zeros, st);
+    W->magic = 0;
+    delete W;
+    return fail_cuda(e, "tm_pack_w4");
+  }
+  *out = W;
+  return TM_OK;
+}
+
+tm_status tm_packed_free(tm_packed *W, void *stream) {
+  if (W == nullptr) return TM_OK;
+  tm_status s = check_handle(W);
+  if (s != TM_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (W->qw) cudaFreeAsync(W->qw, st);
+  if (W->scales) cudaFreeAsync(W->scales, st);
+  if (W->zeros) cudaFreeAsync(W->zeros, st);
+  W->magic = 0;
+  delete W;
+  return TM_OK;
+}
+
+tm_status tm_packed_get(const tm_packed *W, tm_packed_info *info) {
+  tm_status s = check_handle(W);
+  if (s != TM_OK) return s;
+  if (info == nullptr) return fail(TM_ERR_INVALID_ARG, "info must not be NULL");
+  info->K = W->K;
+  info->N = W->N;
+  info->group = W->group;
+  info->dtype = W->dtype;
+  info->symmetric = W->symmetric;
+  info->device = W->device;
+  info->qweight = W->qw;
+  info->scales = W->scales;
+  info->zeros = W->zeros;
+  info->qweight_bytes = W->qw_bytes;
+  info->scales_bytes = W->scales_bytes;
+  info->zeros_bytes = W->zeros_bytes;
+  return TM_OK;
+}
+
+tm_status tm_dequant_w4(const tm_packed *W, void *W_out, void *stream) {
+  tm_status s = check_handle(W);
+  if (s != TM_OK) return s;
+  if (W_out == nullptr || !aligned16(W_out))
+    return fail(TM_ERR_INVALID_ARG, "W_out must be a 16-byte aligned device pointer");
+  cudaError_t e = launch_dequant(W->qw, W->scales, W->symmetric ? nullptr : W->zeros,
+                                 static_cast<uint16_t *>(W_out), W->K, W->N, W->group,
+                                 W->dtype == TM_BF16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "tm_dequant_w4");
+  return TM_OK;
+}
+
+tm_status tm_select(const tm_packed *W, int M, tm_config *out) {
+  tm_status s = check_handle(W);
+  if (s != TM_OK) return s;
+  if (out == nullptr) return fail(TM_ERR_INVALID_ARG, "out must not be NULL");
+  if (M <= 0) return fail(TM_ERR_INVALID_ARG, "M must be positive");
+  *out = select_config(W, M, W->device);
+  return TM_OK;
+}
+
+tm_status tm_gemm_w4a16(const void *A, const tm_packed *W, void *C, int M, int N, int K,
+                        void *stream) {
+  tm_status s = check_gemm_args(A, W, C, M, N, K);
+  if (s != TM_OK || M == 0) return s;
+  const tm_config cfg = select_config(W, M, W->device);
+  return run_gemm(A, W, C, M, cfg, static_cast<cudaStream_t>(stream));
+}
+
+tm_status tm_gemm_w4a16_ex(const void *A, const tm_packed *W, void *C, int M, int N, int K,
+                           const tm_config *cfg, void *stream) {
+  if (cfg == nullptr) return tm_gemm_w4a16(A, W, C, M, N, K, stream);
+  tm_status s = check_gemm_args(A, W, C, M, N, K);
+  if (s != TM_OK || M == 0) return s;
+  tm_config c = *cfg;
+  if (c.kernel == TM_KERNEL_AUTO) c = select_config(W, M, W->device);
+  std::string why;
+  if (!normalize_config(W, M, &c, &why))
+    return fail(TM_ERR_UNSUPPORTED, "variant cannot run this shape: %s", why.c_str());
+  return run_gemm(A, W, C, M, c, static_cast<cudaStream_t>(stream));
+}
+
+tm_status tm_poll_error(void *stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TM_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  int dev = -1;
+  tm_status s = current_device(&dev);
+  if (s != TM_OK) return s;
+  unsigned int *err = nullptr;
+  s = error_word(dev, &err);
+  if (s != TM_OK) return s;
+  unsigned int v = 0;
+  TM_CUDA(cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost), "cudaMemcpy(error word)");
+  if (v != 0) {
+    TM_CUDA(cudaMemset(err, 0, sizeof(unsigned int)), "cudaMemset(error word)");
+    // a kernel that gave up may have left split-K arrival counters raised
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto &kv : g_ws)
+      if (kv.first.first == dev && kv.second.counters)
+        TM_CUDA(cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(unsigned int)),
+                "cudaMemset(counters)");
+  }
+  if (v & TM_DEVERR_TIMEOUT) return fail(TM_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (v & TM_DEVERR_BAD_CODE) return fail(TM_ERR_INVALID_ARG, "a packed code or zero exceeded 15");
+  return TM_OK;
+}
+
+tm_status tm_selftest_wait_timeout(long long limit_ns, void *stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000LL)
+    return fail(TM_ERR_INVALID_ARG, "limit_ns must be in [1000, 1e9]");
+  int dev = -1;
+  tm_status s = current_device(&dev);
+  if (s != TM_OK) return s;
+  unsigned int *err = nullptr;
+  s = error_word(dev, &err);
+  if (s != TM_OK) return s;
+  cudaError_t e = launch_wait_selftest(err, static_cast<unsigned long long>(limit_ns),
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "tm_selftest_wait_timeout");
+  return TM_OK;
+}
+
+// ------------------------------------------------------------- tuning
+static bool parse_int(const char *line, const char *key, int *out) {
+  const char *p = strstr(line, key);
+  if (!p) return false;
+  p += strlen(key);
+  while (*p == '"' || *p == ':' || *p == ' ') ++p;
+  *out = static_cast<int>(strtol(p, nullptr, 10));
+  return true;
+}
+
+tm_status tm_tune_load(const char *path) {
+  if (path == nullptr) return fail(TM_ERR_INVALID_ARG, "path must not be NULL");
+  FILE *f = fopen(path, "r");
+  if (!f) return fail(TM_ERR_INVALID_ARG, "cannot open %s", path);
+  char line[512];
+  std::lock_guard<std::mutex> lk(g_mu);
+  while (fgets(line, sizeof(line), f)) {
+    TuneKey k{};
+    TuneVal v{};
+    if (parse_int(line, "\"N\"", &k.N) && parse_int(line, "\"K\"", &k.K) &&
+        parse_int(line, "\"group\"", &k.group) && parse_int(line, "\"dtype\"", &k.dtype) &&
+        parse_int(line, "\"sym\"", &k.sym) && parse_int(line, "\"M\"", &k.M) &&
+        parse_int(line, "\"kernel\"", &v.cfg.kernel) &&
+        parse_int(line, "\"block_m\"", &v.cfg.block_m) &&
+        parse_int(line, "\"split_k\"", &v.cfg.split_k) &&
+        parse_int(line, "\"dq_warps\"", &v.cfg.dq_warps)) {
+      g_tune[k] = v;
+    }
+  }
+  fclose(f);
+  return TM_OK;
+}
+
+tm_status tm_tune_save(const char *path) {
+  if (path == nullptr) return fail(TM_ERR_INVALID_ARG, "path must not be NULL");
+  FILE *f = fopen(path, "w");
+  if (!f) return fail(TM_ERR_INVALID_ARG, "cannot write %s", path);
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const auto &kv : g_tune) {
+    const TuneKey &k = kv.first;
+    const TuneVal &v = kv.second;
+    fprintf(f,
+            "{\"N\": %d, \"K\": %d, \"group\": %d, \"dtype\": %d, \"sym\": %d, \"M\": %d, "
+            "\"kernel\": %d, \"block_m\": %d, \"split_k\": %d, \"dq_warps\": %d, \"us\": %.3f}\n",
+            k.N, k.K, k.group, k.dtype, k.sym, k.M, v.cfg.kernel, v.cfg.block_m, v.cfg.split_k,
+            v.cfg.dq_warps, v.us);
+  }
+  fclose(f);
+  return TM_OK;
+}
+
+}  // extern "C"
+
+static void load_tune_env_once() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char *p = getenv("TM_TUNE_CACHE");
+    if (p && *p) {
+      FILE *f = fopen(p, "r");
+      if (f) {
+        fclose(f);
+        tm_tune_load(p);
+      }
+    }
+    g_tune_loaded = true;
+  });
+}
+
+static std::vector<tm_config> candidates(const tm_packed *W, int M) {
+  std::vector<tm_config> out;
+  const int KB = W->K / 64;
+  const int splits[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32};
+  if (M <= 8) {
+    for (int s : splits) {
+      tm_config c{TM_KERNEL_GEMV, 0, s, 0};
+      if (normalize_config(W, M, &c, nullptr)) out.push_back(c);
+    }
+  }
+  const int bms[] = {16, 32, 64, 128, 256};
+  for (int bm : bms) {
+    if (bm > 16 && bm / 2 >= M) continue;        // at most one mostly empty tile size
+    const int tiles = (W->N / 128) * ((M + bm - 1) / bm);
+    for (int s : splits) {
+      if (s > KB || (s > 1 && tiles * s > 8 * 152)) continue;
+      for (int dq : {4, 8}) {
+        tm_config c{TM_KERNEL_TC, bm, s, dq};
+        if (normalize_config(W, M, &c, nullptr)) out.push_back(c);
+      }
+    }
+  }
+  return out;
+}
+
+extern "C" tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *stream,
+                             tm_config *best_out) {
+  tm_status s = check_handle(W);
+  if (s != TM_OK) return s;
+  if (Ms == nullptr || nM <= 0) return fail(TM_ERR_INVALID_ARG, "Ms must hold nM > 0 values");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (stream_capturing(st)) return fail(TM_ERR_UNSUPPORTED, "tm_tune cannot run during capture");
+  int maxM = 0;
+  for (int i = 0; i < nM; ++i) {
+    if (Ms[i] <= 0) return fail(TM_ERR_INVALID_ARG, "Ms values must be positive");
+    maxM = std::max(maxM, Ms[i]);
+  }
+  int l2 = 0;
+  cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, W->device);
+  const size_t flush_bytes = std::max<size_t>(static_cast<size_t>(l2) * 2, 64u << 20);
+  void *A = nullptr, *C = nullptr, *flush = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  auto cleanup = [&]() {
+    if (A) cudaFree(A);
+    if (C) cudaFree(C);
+    if (flush) cudaFree(flush);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+  };
+  cudaError_t e = cudaMalloc(&A, static_cast<size_t>(maxM) * W->K * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&C, static_cast<size_t>(maxM) * W->N * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&flush, flush_bytes);
+  if (e == cudaSuccess) e = cudaMemsetAsync(A, 0, static_cast<size_t>(maxM) * W->K * 2, st);
+  if (e == cudaSuccess) e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  if (e != cudaSuccess) {
+    cleanup();
+    return fail_cuda(e, "tm_tune setup");
+  }
+  for (int i = 0; i < nM; ++i) {
+    const int M = Ms[i];
+    std::vector<tm_config> cands = candidates(W, M);
+    double best_us = 1e30;
+    tm_config best{};
+    for (const tm_config &c : cands) {
+      // warm-up (also sizes the workspace)
+      s = run_gemm(A, W, C, M, c, st);
+      if (s != TM_OK) continue;
+      float times[3];
+      bool good = true;
+      for (int r = 0; r < 3 && good; ++r) {
+        cudaMemsetAsync(flush, r, flush_bytes, st);
+        cudaEventRecord(e0, st);
+        good = run_gemm(A, W, C, M, c, st) == TM_OK;
+        cudaEventRecord(e1, st);
+        if (cudaEventSynchronize(e1) != cudaSuccess) good = false;
+        cudaEventElapsedTime(&times[r], e0, e1);
+      }
+      if (!good) continue;
+      std::sort(times, times + 3);
+      const double us = times[1] * 1000.0;
+      if (us < best_us) {
+        best_us = us;
+        best = c;
+      }
+    }
+    if (best_us >= 1e29) {
+      cleanup();
+      return fail(TM_ERR_CUDA, "no variant ran for M=%d", M);
+    }
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      g_tune[TuneKey{W->N, W->K, W->group, (int)W->dtype, W->symmetric, M}] = TuneVal{best, best_us};
+    }
+    if (best_out) best_out[i] = best;
+  }
+  cleanup();
+  tm_status perr = tm_poll_error(stream);
+  if (perr != TM_OK) return perr;
+  const char *p = getenv("TM_TUNE_CACHE");
+  if (p && *p) return tm_tune_save(p);
+  return TM_OK;
+}

@@ -1,0 +1,225 @@
+// gemv.cu -- split-K GEMV for small M on the CUDA cores.
+//
+// Each CTA owns one 64-column strip of the packed weight (one atom column)
+// and one K range.  Its eight warps stream whole 2 KB atoms with 128-bit
+// non-coherent loads (512 contiguous bytes per warp instruction: coalesced,
+// pith.science review, Figure 22), dequantize in registers exactly as the
+// dequant-only kernel does, and accumulate in fp32 against activations held
+// in shared memory.  Partials of the eight warps are summed in a fixed order;
+// with split-K, partials go to the workspace and the last CTA of a strip to
+// arrive sums them in split order, so results do not depend on scheduling.
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "dequant.cuh"
+#include "kernels.h"
+
+namespace tmw4 {
+
+template <bool BF16>
+__device__ __forceinline__ float2 pair_to_float2(uint32_t v) {
+  if constexpr (BF16) {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  } else {
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    return __half22float2(h);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t float_to_16(float x) {
+  if constexpr (BF16) {
+    __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&b);
+  } else {
+    __half h = __float2half_rn(x);
+    return *reinterpret_cast<uint16_t *>(&h);
+  }
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+constexpr int GEMV_WARPS = 8;
+
+template <bool BF16, int MT>
+__global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
+  extern __shared__ float4 smem_f4[];
+  float *smem = reinterpret_cast<float *>(smem_f4);
+  const int na = blockIdx.x, split = blockIdx.y;
+  const int KB = p.K / ATOM_K;
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(KB, kb0 + p.kb_per_split);
+  const int ldA = p.kb_per_split * ATOM_K;
+  float *As = smem;                       // [MT][ldA]
+  float *red = smem + MT * ldA;           // [GEMV_WARPS][MT][64]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int M = p.M, N = p.N;
+
+  // activations of this K range -> fp32 shared memory (rows >= M are zero)
+  const int klen = (kb1 - kb0) * ATOM_K;
+  for (int idx = tid; idx < MT * (klen / 2); idx += blockDim.x) {
+    const int m = idx / (klen / 2), kk = (idx % (klen / 2)) * 2;
+    float2 f = make_float2(0.f, 0.f);
+    if (m < M) {
+      const uint32_t v = *reinterpret_cast<const uint32_t *>(p.A + static_cast<size_t>(m) * p.K +
+                                                             kb0 * ATOM_K + kk);
+      f = pair_to_float2<BF16>(v);
+    }
+    As[m * ldA + kk] = f.x;
+    As[m * ldA + kk + 1] = f.y;
+  }
+  __syncthreads();
+
+  float acc[MT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
+
+  const int nA = na * ATOM_N + lane, nB = nA + 32;
+  for (int kb = kb0 + warp; kb < kb1; kb += GEMV_WARPS) {
+    const uint4 *atom =
+        reinterpret_cast<const uint4 *>(p.qw + (static_cast<size_t>(kb) * (N / ATOM_N) + na) * ATOM_BYTES);
+    uint4 c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = ldg_stream(atom + lane + 32 * i);
+    const int g = (kb * ATOM_K) / p.group;
+    const uint16_t *srow = p.scales + static_cast<size_t>(g) * N;
+    const uint8_t *zrow = p.zeros ? p.zeros + static_cast<size_t>(g) * (N / 2) : nullptr;
+    const uint32_t s2[2] = {dup16(__ldg(srow + nA)), dup16(__ldg(srow + nB))};
+    const uint32_t zm2[2] = {zero_magic2<BF16>(zero_of(zrow, nA)),
+                             zero_magic2<BF16>(zero_of(zrow, nB))};
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+      const int col = ci & 1, h = ci >> 1;
+      const uint32_t w[4] = {c[ci].x, c[ci].y, c[ci].z, c[ci].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t d[4];
+        dequant_word<BF16>(w[j], zm2[col], s2[col], d);
+        float wf[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = pair_to_float2<BF16>(d[i]);
+          wf[2 * i] = f.x;
+          wf[2 * i + 1] = f.y;
+        }
+        const int kloc = (kb - kb0) * ATOM_K + 32 * h + 8 * j;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const float4 a0 = *reinterpret_cast<const float4 *>(As + m * ldA + kloc);
+          const float4 a1 = *reinterpret_cast<const float4 *>(As + m * ldA + kloc + 4);
+          float s = acc[m][ci];
+          s = fmaf(wf[0], a0.x, s);
+          s = fmaf(wf[1], a0.y, s);
+          s = fmaf(wf[2], a0.z, s);
+          s = fmaf(wf[3], a0.w, s);
+          s = fmaf(wf[4], a1.x, s);
+          s = fmaf(wf[5], a1.y, s);
+          s = fmaf(wf[6], a1.z, s);
+          s = fmaf(wf[7], a1.w, s);
+          acc[m][ci] = s;
+        }
+      }
+    }
+  }
+  // per-warp partials -> shared memory, then a fixed-order sum over warps
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    red[(warp * MT + m) * 64 + lane] = acc[m][0] + acc[m][2];
+    red[(warp * MT + m) * 64 + lane + 32] = acc[m][1] + acc[m][3];
+  }
+  __syncthreads();
+  __shared__ int s_last;
+  // thread t handles outputs (m, cl) = divmod(t + 256 i, 64), i = 0..MT/4
+  constexpr int PER_THREAD = (MT * 64 + 255) / 256;
+  float sum[PER_THREAD];
+#pragma unroll
+  for (int i = 0; i < PER_THREAD; ++i) {
+    const int idx = tid + 256 * i;
+    sum[i] = 0.f;
+    if (idx < MT * 64) {
+      const int m = idx / 64, cl = idx % 64;
+#pragma unroll
+      for (int w = 0; w < GEMV_WARPS; ++w) sum[i] += red[(w * MT + m) * 64 + cl];
+    }
+  }
+  if (p.splits == 1) {
+#pragma unroll
+    for (int i = 0; i < PER_THREAD; ++i) {
+      const int idx = tid + 256 * i, m = idx / 64, n = na * ATOM_N + idx % 64;
+      if (idx < MT * 64 && m < M) p.C[static_cast<size_t>(m) * N + n] = float_to_16<BF16>(sum[i]);
+    }
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < PER_THREAD; ++i) {
+    const int idx = tid + 256 * i, m = idx / 64, n = na * ATOM_N + idx % 64;
+    if (idx < MT * 64 && m < M) p.ws[(static_cast<size_t>(split) * M + m) * N + n] = sum[i];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(p.counters + na, 1u);
+    s_last = (prev == static_cast<unsigned>(p.splits - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+#pragma unroll
+  for (int i = 0; i < PER_THREAD; ++i) {
+    const int idx = tid + 256 * i, m = idx / 64, n = na * ATOM_N + idx % 64;
+    if (idx < MT * 64 && m < M) {
+      float t = 0.f;
+      for (int s = 0; s < p.splits; ++s)
+        t += __ldcg(p.ws + (static_cast<size_t>(s) * M + m) * N + n);
+      p.C[static_cast<size_t>(m) * N + n] = float_to_16<BF16>(t);
+    }
+  }
+  if (tid == 0) p.counters[na] = 0u;
+}
+
+size_t gemv_smem_bytes(int rows_tmpl, int kb_per_split) {
+  return sizeof(float) * (static_cast<size_t>(rows_tmpl) * kb_per_split * ATOM_K +
+                          static_cast<size_t>(GEMV_WARPS) * rows_tmpl * 64);
+}
+
+template <bool BF16, int MT>
+static cudaError_t launch_gemv_t(const GemmArgs &a, cudaStream_t st) {
+  const size_t smem = gemv_smem_bytes(MT, a.kb_per_split);
+  static size_t attr_bytes = 0;  // largest opt-in set so far (per process)
+  static int attr_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (attr_device != dev || smem > attr_bytes) {
+    const size_t want = 200 * 1024;
+    e = cudaFuncSetAttribute(gemv_kernel<BF16, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(want));
+    if (e != cudaSuccess) return e;
+    attr_bytes = want;
+    attr_device = dev;
+  }
+  dim3 grid(a.N / ATOM_N, a.splits);
+  gemv_kernel<BF16, MT><<<grid, 256, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, cudaStream_t st) {
+  switch (rows_tmpl) {
+    case 1: return bf16 ? launch_gemv_t<true, 1>(a, st) : launch_gemv_t<false, 1>(a, st);
+    case 2: return bf16 ? launch_gemv_t<true, 2>(a, st) : launch_gemv_t<false, 2>(a, st);
+    case 4: return bf16 ? launch_gemv_t<true, 4>(a, st) : launch_gemv_t<false, 4>(a, st);
+    case 8: return bf16 ? launch_gemv_t<true, 8>(a, st) : launch_gemv_t<false, 8>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace tmw4

@@ -1,0 +1,49 @@
+// kernels.h -- launch entry points of the device kernels (host-callable).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace tmw4 {
+
+cudaError_t launch_repack(const uint8_t *q, uint8_t *qw, int K, int N, unsigned int *err,
+                          cudaStream_t st);
+cudaError_t launch_pack_zeros(const uint8_t *z, uint8_t *zp, int rows, int N, unsigned int *err,
+                              cudaStream_t st);
+cudaError_t launch_dequant(const uint8_t *qw, const uint16_t *scales, const uint8_t *zeros,
+                           uint16_t *out, int K, int N, int group, bool bf16, cudaStream_t st);
+
+// Shared arguments of the GEMM kernels.  ws/counters are the split-K
+// workspace (partials [splits][M][N] fp32 and one self-resetting arrival
+// counter per output tile); unused when splits == 1.
+struct GemmArgs {
+  const uint8_t *qw;
+  const uint16_t *scales;
+  const uint8_t *zeros;  // nullptr: symmetric
+  const uint16_t *A;
+  uint16_t *C;
+  float *ws;
+  unsigned int *counters;
+  unsigned int *err;
+  int M, N, K, group;
+  int splits;
+  int kb_per_split;  // 64-wide K blocks per split
+  unsigned long long limit_ns;
+};
+
+// GEMV (CUDA cores): rows_tmpl in {1,2,4,8} >= M.  Shared memory bytes:
+size_t gemv_smem_bytes(int rows_tmpl, int kb_per_split);
+cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, cudaStream_t st);
+
+// tcgen05 kernel.  block_m in {16,32,64,128,256}, dq_warps in {4,8}.
+size_t tc_smem_bytes(int block_m);
+int tc_stages(int block_m);
+cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
+                      int dq_warps, cudaStream_t st);
+
+// Bounded-wait self-test kernel.
+cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t st);
+
+}  // namespace tmw4

@@ -1,0 +1,124 @@
+// pack.cu -- offline repack of int4 codes into the library's packed layout,
+// nibble-packing of zero points, and the dequant-only kernel.
+//
+// Repack follows the pages' offline packing (TurboMind paper, pith.science
+// review, Figures 6/7: load a tile, place each thread's eight values, permute
+// them into MMA order and store fragments in the order the runtime loads
+// them).  Here one CTA moves one 64x64 atom: a coalesced 4 KB load of codes
+// into shared memory, then 512 packed words written contiguously.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dequant.cuh"
+#include "kernels.h"
+#include "tmw4_device.cuh"
+
+namespace tmw4 {
+
+// NIBBLE_POS of the layout: value e of a word sits at nibble kNibPos[e].
+__device__ __constant__ int kNibPos[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+
+__global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ q,
+                                                     uint8_t *__restrict__ qw, int K, int N,
+                                                     unsigned int *err) {
+  __shared__ uint8_t tile[ATOM_K][ATOM_N + 4];
+  const int na = blockIdx.x, kb = blockIdx.y, t = threadIdx.x;
+  const int k0 = kb * ATOM_K, n0 = na * ATOM_N;
+  // 64 rows x 64 bytes, 16 bytes per thread
+  {
+    const int row = t >> 2, col = (t & 3) * 16;
+    const uint4 v = *reinterpret_cast<const uint4 *>(q + static_cast<size_t>(k0 + row) * N + n0 + col);
+    if (((v.x | v.y | v.z | v.w) & 0xF0F0F0F0u) != 0u) atomicOr(err, TM_DEVERR_BAD_CODE);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) tile[row][col + 4 * i + b] = (w[i] >> (8 * b)) & 0xFu;
+    }
+  }
+  __syncthreads();
+  uint32_t *out = reinterpret_cast<uint32_t *>(qw + (static_cast<size_t>(kb) * (N / ATOM_N) + na) * ATOM_BYTES);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int widx = t + 256 * r;
+    const int h = widx >> 8, nl = (widx & 255) >> 2, j = widx & 3;
+    const int o = 4 * h + j;
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) word |= static_cast<uint32_t>(tile[8 * o + e][nl]) << (4 * kNibPos[e]);
+    out[widx] = word;
+  }
+}
+
+__global__ void pack_zeros_kernel(const uint8_t *__restrict__ z, uint8_t *__restrict__ zp,
+                                  int rows, int N, unsigned int *err) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t total = static_cast<size_t>(rows) * (N / 2);
+  if (i >= total) return;
+  const size_t g = i / (N / 2), c = i % (N / 2);
+  const uint32_t lo = z[g * N + 2 * c], hi = z[g * N + 2 * c + 1];
+  if ((lo | hi) > 15u) atomicOr(err, TM_DEVERR_BAD_CODE);
+  zp[i] = static_cast<uint8_t>((lo & 0xFu) | ((hi & 0xFu) << 4));
+}
+
+// One thread per 16-byte chunk: 32 consecutive K values of one column.
+template <bool BF16>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ qw,
+                                                      const uint16_t *__restrict__ scales,
+                                                      const uint8_t *__restrict__ zeros,
+                                                      uint16_t *__restrict__ out, int K, int N,
+                                                      int group) {
+  const size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t nchunks = static_cast<size_t>(K) * N / 32;
+  if (c >= nchunks) return;
+  const size_t atom = c >> 7;
+  const int cidx = static_cast<int>(c & 127), h = cidx >> 6, nl = cidx & 63;
+  const int natoms_n = N / ATOM_N;
+  const int kb = static_cast<int>(atom / natoms_n), na = static_cast<int>(atom % natoms_n);
+  const int k0 = kb * ATOM_K + 32 * h, n = na * ATOM_N + nl;
+  const int g = k0 / group;
+  const uint32_t s2 = dup16(scales[static_cast<size_t>(g) * N + n]);
+  const uint32_t zm2 = zero_magic2<BF16>(
+      zero_of(zeros ? zeros + static_cast<size_t>(g) * (N / 2) : nullptr, n));
+  const uint4 v = *reinterpret_cast<const uint4 *>(qw + c * 16);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t d[4];
+    dequant_word<BF16>(w[j], zm2, s2, d);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const size_t k = static_cast<size_t>(k0 + 8 * j + 2 * i);
+      out[k * N + n] = static_cast<uint16_t>(d[i] & 0xFFFFu);
+      out[(k + 1) * N + n] = static_cast<uint16_t>(d[i] >> 16);
+    }
+  }
+}
+
+cudaError_t launch_repack(const uint8_t *q, uint8_t *qw, int K, int N, unsigned int *err,
+                          cudaStream_t st) {
+  dim3 grid(N / ATOM_N, K / ATOM_K);
+  repack_kernel<<<grid, 256, 0, st>>>(q, qw, K, N, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_zeros(const uint8_t *z, uint8_t *zp, int rows, int N, unsigned int *err,
+                              cudaStream_t st) {
+  const size_t total = static_cast<size_t>(rows) * (N / 2);
+  const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
+  pack_zeros_kernel<<<blocks, 256, 0, st>>>(z, zp, rows, N, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint8_t *qw, const uint16_t *scales, const uint8_t *zeros,
+                           uint16_t *out, int K, int N, int group, bool bf16, cudaStream_t st) {
+  const size_t nchunks = static_cast<size_t>(K) * N / 32;
+  const unsigned blocks = static_cast<unsigned>((nchunks + 255) / 256);
+  if (bf16)
+    dequant_kernel<true><<<blocks, 256, 0, st>>>(qw, scales, zeros, out, K, N, group);
+  else
+    dequant_kernel<false><<<blocks, 256, 0, st>>>(qw, scales, zeros, out, K, N, group);
+  return cudaGetLastError();
+}
+
+}  // namespace tmw4
