@@ -247,29 +247,31 @@ def run_ours(args, rank: int, world: int):
     # clock-sampled warm replays, then the timed replays
     sampler = ClockSampler(gpu_id(dev))
     sampler.start()
-    t_end = time.time() + 1.5
-    while time.time() < t_end:
-        graph.replay()
+    # graphs replay on the current stream: make it the launch stream
+    with torch.cuda.stream(stream):
+        t_end = time.time() + 1.5
+        while time.time() < t_end:
+            graph.replay()
+            torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    graph.replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    elapsed = t0.elapsed_time(t1) * 1e-3
-    ev_elapsed = None
-    if graph_ev is not None:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        graph_ev.replay()
+        graph.replay()
         t1.record(stream)
         torch.cuda.synchronize()
-        ev_elapsed = t0.elapsed_time(t1) * 1e-3
+        if world > 1:
+            torch.distributed.barrier()
+        elapsed = t0.elapsed_time(t1) * 1e-3
+        ev_elapsed = None
+        if graph_ev is not None:
+            t0.record(stream)
+            graph_ev.replay()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            ev_elapsed = t0.elapsed_time(t1) * 1e-3
     clocks = sampler.stop()
     binding.poll_error(stream)
 

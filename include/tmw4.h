@@ -59,7 +59,8 @@ typedef struct {
   int32_t kernel;
   int32_t block_m;
   int32_t split_k;
-  int32_t dq_warps; /* TC: dequant warps per CTA, 4 or 8 (0 = default) */
+  int32_t dq_warps; /* TC: dequant warps per CTA, 4, 8 or 16 (0 = default);
+                       each group of 4 dequantizes every (dq_warps/4)-th stage */
 } tm_config;
 
 /* Opaque packed weight, owned by the library until tm_packed_free. */
@@ -70,17 +71,19 @@ typedef struct tm_packed tm_packed;
  * Packed weight layout (the library's own Blackwell order; the pages'
  * packing -- pith.science review, Figures 6 and 7 -- permutes each thread's
  * eight int4 values into MMA order and stores fragments in load order):
- *   qweight: K*N/2 bytes.  The weight is cut into 64x64 atoms; atom
- *     (kb, na) covers k in [64kb, 64kb+64), n in [64na, 64na+64) and starts
- *     at byte (kb*(N/64) + na)*2048.  An atom holds 512 little-endian 32-bit
- *     words; word h*256 + nl*4 + j (h in {0,1}, nl in [0,64), j in [0,4))
- *     holds q[64kb + 8(4h+j) + e][64na + nl] for e = 0..7, value e in bits
+ *   qweight: K*N/2 bytes.  Columns form 128-wide tiles; tile nt and K-block
+ *     kb (64 values of K) is a 4096-byte block at byte (nt*(K/64) + kb)*4096,
+ *     so all of a tile's K is contiguous.  The block holds two 2048-byte
+ *     atoms, a = 0 for the tile's columns [0,64), a = 1 for [64,128).  An
+ *     atom holds 512 little-endian 32-bit words; word h*256 + nl*4 + j
+ *     (h in {0,1}, nl in [0,64), j in [0,4)) holds
+ *     q[64kb + 8(4h+j) + e][128nt + 64a + nl] for e = 0..7, value e in bits
  *     [4p, 4p+4) with p = (0,4,1,5,2,6,3,7)[e] -- the word order of
  *     pith.science review Figures 23/24 (e7 e5 e3 e1 e6 e4 e2 e0).  Every
  *     16-byte chunk is 32 consecutive K values of one column.
- *   scales: [K/G][N] 16-bit values of type `dtype`, as given to tm_pack_w4.
- *   zeros:  [K/G][N/2] bytes, column 2i in the low nibble, 2i+1 in the high
- *     nibble; NULL for the symmetric format (implicit zero 8). */
+ *   scales: tile-major [N/128][K/G][128] 16-bit values of type `dtype`.
+ *   zeros:  tile-major [N/128][K/G][64] bytes, each byte two columns (even
+ *     column in the low nibble); NULL for the symmetric format (zero 8). */
 typedef struct {
   int32_t K, N, group;
   int32_t dtype;     /* tm_dtype */

@@ -16,6 +16,7 @@ with figure captions).
 from .w4a16 import (  # noqa: F401
     ATOM_K,
     ATOM_N,
+    TILE_N,
     NIBBLE_POS,
     f16_bits_to_f64,
     bf16_bits_to_f64,
@@ -28,6 +29,8 @@ from .w4a16 import (  # noqa: F401
     gemm_ref_rows,
     pack_ref,
     unpack_ref,
+    pack_scales_ref,
+    unpack_scales_ref,
     pack_zeros_ref,
     unpack_zeros_ref,
     rms,

@@ -206,18 +206,23 @@ def tolerance_ok(c, c_ref, rms_value: float | None = None, rel: float = 1e-2) ->
 # one mask yields two 16-bit lanes.  This library keeps that word order and
 # defines its own tile order for its tcgen05 and GEMV consumers:
 #
-#   * K and N are multiples of 64.  The weight is cut into 64x64 atoms;
-#     atom (kb, na) covers k in [64kb, 64kb+64), n in [64na, 64na+64) and
-#     starts at byte (kb * (N/64) + na) * 2048.
-#   * Inside an atom there are 512 little-endian 32-bit words.  Word
-#     h*256 + nl*4 + j (h in {0,1}, nl in [0,64), j in [0,4)) holds the eight
-#     values q[64kb + 8o + e, 64na + nl], e = 0..7, with o = 4h + j.
+#   * K is a multiple of 64 and N of 128.  Columns form 128-wide tiles; tile
+#     nt, K-block kb (64 values of K) is a 4096-byte block at byte
+#     (nt * (K/64) + kb) * 4096, so all K of a tile is contiguous.
+#   * A block holds two 2048-byte atoms, a = 0 for columns [0, 64) of the
+#     tile and a = 1 for [64, 128).  An atom holds 512 little-endian 32-bit
+#     words; word h*256 + nl*4 + j (h in {0,1}, nl in [0,64), j in [0,4))
+#     holds the eight values q[64kb + 8o + e, 128nt + 64a + nl], e = 0..7,
+#     with o = 4h + j.
 #   * Value e sits at bits [4p, 4p+4) with p = NIBBLE_POS[e].
-#   * Scales are stored as given, [K/G, N] 16-bit patterns.  Zeros are
-#     packed two per byte, [K/G, N/2]: column 2i in the low nibble, 2i+1 in
-#     the high nibble; the symmetric format stores no zeros.
+#   * Scales are reordered tile-major: [N/128][K/G][128] 16-bit patterns,
+#     i.e. scale (g, n) at index (n//128 * (K/G) + g) * 128 + n%128.
+#   * Zeros are nibble-packed, tile-major: [N/128][K/G][64] bytes; byte
+#     (nt, g, i) holds column 128nt + 2i in the low nibble and 128nt + 2i + 1
+#     in the high nibble.  The symmetric format stores no zeros.
 # ---------------------------------------------------------------------------
 
+TILE_N = 128
 ATOM_K = 64
 ATOM_N = 64
 #: nibble position of element e (0..7) inside its 32-bit word
@@ -229,18 +234,18 @@ def _atom_word_coords(K: int, N: int):
 
     Returns two int64 arrays of length K*N/8 in packed-word order.
     """
-    if K % ATOM_K or N % ATOM_N:
-        raise ValueError("K and N must be multiples of 64")
-    nkb, nna = K // ATOM_K, N // ATOM_N
+    if K % ATOM_K or N % TILE_N:
+        raise ValueError("K must be a multiple of 64 and N of 128")
+    nkb = K // ATOM_K
     w = np.arange(K * N // 8, dtype=np.int64)
-    atom, widx = w // 512, w % 512
-    kb, na = atom // nna, atom % nna
+    block, inblk = w // 1024, w % 1024
+    nt, kb = block // nkb, block % nkb
+    a, widx = inblk // 512, inblk % 512
     h, rem = widx // 256, widx % 256
     nl, j = rem // 4, rem % 4
     o = 4 * h + j
     k0 = ATOM_K * kb + 8 * o
-    n = ATOM_N * na + nl
-    assert k0.max(initial=0) < K and n.max(initial=0) < N and nkb > 0
+    n = TILE_N * nt + ATOM_N * a + nl
     return k0, n
 
 
@@ -272,18 +277,36 @@ def unpack_ref(packed: np.ndarray, K: int, N: int) -> np.ndarray:
     return q
 
 
+def pack_scales_ref(scales: np.ndarray) -> np.ndarray:
+    """scales [K/G, N] (16-bit patterns) -> tile-major [N/128, K/G, 128] (flattened)."""
+    s = np.asarray(scales, dtype=np.uint16)
+    G_rows, N = s.shape
+    if N % TILE_N:
+        raise ValueError("N must be a multiple of 128")
+    return s.reshape(G_rows, N // TILE_N, TILE_N).transpose(1, 0, 2).reshape(-1).copy()
+
+
+def unpack_scales_ref(sp: np.ndarray, G_rows: int, N: int) -> np.ndarray:
+    """Inverse of ``pack_scales_ref``."""
+    sp = np.asarray(sp, dtype=np.uint16).reshape(N // TILE_N, G_rows, TILE_N)
+    return sp.transpose(1, 0, 2).reshape(G_rows, N).copy()
+
+
 def pack_zeros_ref(zeros: np.ndarray) -> np.ndarray:
-    """zeros [K/G, N] uint8 (0..15) -> [K/G, N/2] bytes, even column low nibble."""
+    """zeros [K/G, N] uint8 (0..15) -> tile-major nibble bytes [N/128, K/G, 64] (flattened)."""
     z = np.asarray(zeros, dtype=np.uint8)
-    if z.shape[1] % 2:
-        raise ValueError("N must be even")
-    return (z[:, 0::2] & 0xF) | ((z[:, 1::2] & 0xF) << 4)
+    G_rows, N = z.shape
+    if N % TILE_N:
+        raise ValueError("N must be a multiple of 128")
+    pairs = (z[:, 0::2] & 0xF) | ((z[:, 1::2] & 0xF) << 4)          # [K/G, N/2]
+    return pairs.reshape(G_rows, N // TILE_N, TILE_N // 2).transpose(1, 0, 2).reshape(-1).copy()
 
 
-def unpack_zeros_ref(zp: np.ndarray) -> np.ndarray:
+def unpack_zeros_ref(zp: np.ndarray, G_rows: int, N: int) -> np.ndarray:
     """Inverse of ``pack_zeros_ref``."""
-    zp = np.asarray(zp, dtype=np.uint8)
-    z = np.empty((zp.shape[0], zp.shape[1] * 2), dtype=np.uint8)
-    z[:, 0::2] = zp & 0xF
-    z[:, 1::2] = zp >> 4
+    zp = np.asarray(zp, dtype=np.uint8).reshape(N // TILE_N, G_rows, TILE_N // 2)
+    pairs = zp.transpose(1, 0, 2).reshape(G_rows, N // 2)
+    z = np.empty((G_rows, N), dtype=np.uint8)
+    z[:, 0::2] = pairs & 0xF
+    z[:, 1::2] = pairs >> 4
     return z

@@ -34,8 +34,8 @@ def _variants(M):
         out += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
     for bm in (16, 32, 64, 128, 256):
         for sk in (1, 3):
-            for dq in (4, 8):
-                if bm >= 128 and dq == 8 and sk == 3:
+            for dq in (4, 8, 16):
+                if bm >= 128 and dq != 8 and sk == 3:
                     continue
                 out.append(dict(kernel="tc", block_m=bm, split_k=sk, dq_warps=dq))
     return out
@@ -107,7 +107,8 @@ def test_one_hot_rows_reproduce_dequantized_weight():
     A = binding.acts_to_device(a, torch.float16)
     for cfg in [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=4),
                 dict(kernel="tc", block_m=16, split_k=1), dict(kernel="tc", block_m=16, split_k=3),
-                dict(kernel="tc", block_m=128, split_k=1, dq_warps=8)]:
+                dict(kernel="tc", block_m=128, split_k=1, dq_warps=8),
+                dict(kernel="tc", block_m=32, split_k=5, dq_warps=16)]:
         if cfg["kernel"] == "gemv" and len(ks) > 8:
             continue
         C = gemm_poisoned(A, W, config=cfg)

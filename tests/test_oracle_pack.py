@@ -30,7 +30,7 @@ def test_nibble_order_matches_pages_figure():
 
 def test_two_lanes_per_mask():
     """One mask 0x000F000F isolates an (even, odd) pair of consecutive values."""
-    q = np.zeros((64, 64), np.uint8)
+    q = np.zeros((64, 128), np.uint8)
     q[0:8, 0] = np.arange(1, 9)                  # values 1..8 for k = 0..7 of column 0
     word = int(oracle.pack_ref(q)[:4].view("<u4")[0])
     for pair in range(4):
@@ -39,7 +39,7 @@ def test_two_lanes_per_mask():
         assert (lo, hi) == (2 * pair + 1, 2 * pair + 2)
 
 
-@pytest.mark.parametrize("K,N", [(64, 64), (128, 192), (256, 128), (192, 320)])
+@pytest.mark.parametrize("K,N", [(64, 128), (128, 256), (256, 128), (192, 384)])
 def test_roundtrip_random(K, N):
     rng = np.random.default_rng(K * 1000 + N)
     q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
@@ -95,13 +95,36 @@ def test_zero_pack_roundtrip():
     rng = np.random.default_rng(4)
     z = rng.integers(0, 16, size=(8, 256), dtype=np.uint8)
     zp = oracle.pack_zeros_ref(z)
-    assert zp.shape == (8, 128)
-    assert np.array_equal(oracle.unpack_zeros_ref(zp), z)
-    assert zp[0, 0] == (z[0, 0] | (z[0, 1] << 4))
+    assert zp.shape == (8 * 128,)
+    assert np.array_equal(oracle.unpack_zeros_ref(zp, 8, 256), z)
+    assert zp[0] == (z[0, 0] | (z[0, 1] << 4))
+    assert zp[64] == (z[1, 0] | (z[1, 1] << 4))          # next group row of tile 0
+    assert zp[8 * 64] == (z[0, 128] | (z[0, 129] << 4))  # first row of tile 1
+
+
+def test_scale_pack_roundtrip_and_tile_order():
+    rng = np.random.default_rng(5)
+    s = rng.integers(0, 0x7C00, size=(6, 384), dtype=np.uint16)
+    sp = oracle.pack_scales_ref(s)
+    assert np.array_equal(oracle.unpack_scales_ref(sp, 6, 384), s)
+    # one tile's scales for consecutive groups are contiguous
+    assert np.array_equal(sp[128:256], s[1, 0:128])
+    assert np.array_equal(sp[6 * 128:7 * 128], s[0, 128:256])
+
+
+def test_tile_blocks_are_contiguous_in_k():
+    """A 128-column tile's consecutive 64-K blocks follow each other (4 KB apart)."""
+    K, N = 256, 256
+    kk, nn = np.meshgrid(np.arange(K), np.arange(N), indexing="ij")
+    p = oracle.pack_ref(((kk // 64) + 4 * (nn // 128)).astype(np.uint8))
+    words = p.view("<u4").reshape(-1, 1024)                  # 4 KB blocks
+    block_val = words & 0xF                                   # value e0 of each word
+    assert np.all(block_val == block_val[:, :1])
+    assert block_val[:, 0].tolist() == [0, 1, 2, 3, 4, 5, 6, 7]
 
 
 def test_pack_rejects_bad_input():
     with pytest.raises(ValueError):
         oracle.pack_ref(np.full((64, 64), 16, np.uint8))
     with pytest.raises(ValueError):
-        oracle.pack_ref(np.zeros((64, 96), np.uint8))
+        oracle.pack_ref(np.zeros((64, 64), np.uint8))

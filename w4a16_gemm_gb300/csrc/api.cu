@@ -164,22 +164,44 @@ static tm_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
   return TM_OK;
 }
 
-// 2-D map over A [M][K] (K innermost), box 64 x block_m, 128-byte swizzle;
-// rows past M read as zero.
-static tm_status encode_act_map(const void *A, int M, int K, bool bf16, int block_m,
-                                CUtensorMap *map) {
+// Activation tensor map with the 128-byte swizzle; rows past M read as
+// zero.  Preferred form: 3-D (64 x M x K/64, strides K*2 and 128 bytes) so
+// that one copy brings `kbs` consecutive 64-K blocks of BLOCK_M rows, each
+// block landing as its own swizzled [block_m][64] tile.  If the driver
+// rejects that map, a 2-D map (box 64 x block_m, one copy per 64-K block)
+// is used instead and *is_3d is 0.
+static int g_map3d_ok = -1;   // -1 unknown, 0 rejected, 1 accepted
+
+static tm_status encode_act_map(const void *A, int M, int K, bool bf16, int block_m, int kbs,
+                                CUtensorMap *map, int *is_3d) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   tm_status s = get_encoder(&enc);
   if (s != TM_OK) return s;
+  const CUtensorMapDataType dt =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (g_map3d_ok != 0) {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(block_m), static_cast<cuuint32_t>(kbs)};
+    CUresult r = enc(map, dt, 3, const_cast<void *>(A), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+      g_map3d_ok = 1;
+      *is_3d = 1;
+      return TM_OK;
+    }
+    g_map3d_ok = 0;
+  }
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_m)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                   2, const_cast<void *>(A), dims, strides, box, estr,
+  CUresult r = enc(map, dt, 2, const_cast<void *>(A), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(TM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  *is_3d = 0;
   return TM_OK;
 }
 
@@ -204,7 +226,6 @@ struct TuneVal {
   double us;
 };
 static std::map<TuneKey, TuneVal> g_tune;
-static bool g_tune_loaded = false;
 
 static int sm_count(int dev) {
   static int cached[kMaxDevices] = {};
@@ -247,9 +268,9 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
       if (why) *why = "TC block_m must be 16, 32, 64, 128 or 256";
       return false;
     }
-    if (c->dq_warps == 0) c->dq_warps = 4;
-    if (c->dq_warps != 4 && c->dq_warps != 8) {
-      if (why) *why = "TC dq_warps must be 4 or 8";
+    if (c->dq_warps == 0) c->dq_warps = 8;
+    if (c->dq_warps != 4 && c->dq_warps != 8 && c->dq_warps != 16) {
+      if (why) *why = "TC dq_warps must be 4, 8 or 16";
       return false;
     }
     if ((M + c->block_m - 1) / c->block_m > 65535) {
@@ -267,7 +288,7 @@ static tm_config default_config(const tm_packed *W, int M, int dev) {
   tm_config c{};
   c.kernel = TM_KERNEL_TC;
   c.block_m = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-  c.dq_warps = 4;
+  c.dq_warps = 8;
   const int KB = W->K / 64;
   const int sms = sm_count(dev);
   const int per_sm = c.block_m <= 64 ? 2 : 1;
@@ -296,6 +317,15 @@ static tm_config select_config(const tm_packed *W, int M, int dev) {
   return default_config(W, M, dev);
 }
 
+#ifdef TMW4_TRACE
+// debug builds only: device buffer that receives the per-stage cycle stamps
+static long long *g_trace = nullptr;
+extern "C" tm_status tm_debug_set_trace(void *p) {
+  g_trace = static_cast<long long *>(p);
+  return TM_OK;
+}
+#endif
+
 // ------------------------------------------------------------ GEMM launch
 static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, const tm_config &cfg,
                           cudaStream_t st) {
@@ -314,11 +344,17 @@ static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, con
   a.N = W->N;
   a.K = W->K;
   a.group = W->group;
-  a.splits = cfg.split_k;
-  a.kb_per_split = (KB + cfg.split_k - 1) / cfg.split_k;
-  // trailing splits may be empty: shrink so every split has work
-  a.splits = (KB + a.kb_per_split - 1) / a.kb_per_split;
+  // the TC kernel moves whole stages of `gran` 64-K blocks: split on stage
+  // boundaries; trailing splits that would be empty are dropped
+  const int gran = cfg.kernel == TM_KERNEL_TC ? tc_kblocks_per_stage(cfg.block_m) : 1;
+  int per = (KB + cfg.split_k - 1) / cfg.split_k;
+  per = (per + gran - 1) / gran * gran;
+  a.kb_per_split = per;
+  a.splits = (KB + per - 1) / per;
   a.limit_ns = wait_limit_ns();
+#ifdef TMW4_TRACE
+  a.trace = g_trace;
+#endif
   const bool bf16 = W->dtype == TM_BF16;
   if (a.splits > 1) {
     Workspace *ws = nullptr;
@@ -336,7 +372,8 @@ static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, con
     e = launch_gemv(a, bf16, gemv_rows_tmpl(M), st);
   } else {
     CUtensorMap map;
-    s = encode_act_map(A, M, W->K, bf16, cfg.block_m, &map);
+    s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_kblocks_per_stage(cfg.block_m), &map,
+                       &a.act_map_3d);
     if (s != TM_OK) return s;
     e = launch_tc(a, map, bf16, cfg.block_m, cfg.dq_warps, st);
   }
@@ -410,7 +447,7 @@ tm_status tm_pack_w4(const uint8_t *q, const void *scales, const uint8_t *zeros,
     e = cudaMallocAsync(reinterpret_cast<void **>(&W->zeros), W->zeros_bytes, st);
   if (e == cudaSuccess) e = launch_repack(q, W->qw, K, N, err, st);
   if (e == cudaSuccess)
-    e = cudaMemcpyAsync(W->scales, scales, W->scales_bytes, cudaMemcpyDeviceToDevice, st);
+    e = launch_pack_scales(static_cast<const uint16_t *>(scales), W->scales, K / group, N, st);
   if (e == cudaSuccess && zeros) e = launch_pack_zeros(zeros, W->zeros, K / group, N, err, st);
   if (e != cudaSuccess) {
     if (W->qw) cudaFreeAsync(W->qw, st);
@@ -602,7 +639,6 @@ static void load_tune_env_once() {
         tm_tune_load(p);
       }
     }
-    g_tune_loaded = true;
   });
 }
 
@@ -622,7 +658,7 @@ static std::vector<tm_config> candidates(const tm_packed *W, int M) {
     const int tiles = (W->N / 128) * ((M + bm - 1) / bm);
     for (int s : splits) {
       if (s > KB || (s > 1 && tiles * s > 8 * 152)) continue;
-      for (int dq : {4, 8}) {
+      for (int dq : {4, 8, 16}) {
         tm_config c{TM_KERNEL_TC, bm, s, dq};
         if (normalize_config(W, M, &c, nullptr)) out.push_back(c);
       }

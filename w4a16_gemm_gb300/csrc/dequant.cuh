@@ -40,11 +40,11 @@ __device__ __forceinline__ uint32_t zero_magic2(uint32_t z) {
 
 __device__ __forceinline__ uint32_t dup16(uint32_t h) { return (h & 0xFFFFu) | (h << 16); }
 
-// Zero point of column n in group row `zrow` (nibble-packed, even column in
-// the low nibble); 8 for the symmetric format (zrow == nullptr).
-__device__ __forceinline__ uint32_t zero_of(const uint8_t *zrow, int n) {
-  if (zrow == nullptr) return 8u;
-  return (static_cast<uint32_t>(zrow[n >> 1]) >> ((n & 1) * 4)) & 0xFu;
+// Zero point of column n in group g from the tile-major nibble array; 8 for
+// the symmetric format (zeros == nullptr).
+__device__ __forceinline__ uint32_t zero_of(const uint8_t *zeros, int g, int n, int G_rows) {
+  if (zeros == nullptr) return 8u;
+  return (static_cast<uint32_t>(zeros[zero_byte(g, n, G_rows)]) >> ((n & 1) * 4)) & 0xFu;
 }
 
 }  // namespace tmw4

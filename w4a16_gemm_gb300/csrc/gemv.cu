@@ -84,26 +84,34 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
     for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
 
   const int nA = na * ATOM_N + lane, nB = nA + 32;
-  for (int kb = kb0 + warp; kb < kb1; kb += GEMV_WARPS) {
-    const uint4 *atom =
-        reinterpret_cast<const uint4 *>(p.qw + (static_cast<size_t>(kb) * (N / ATOM_N) + na) * ATOM_BYTES);
-    uint4 c[4];
+  const int G_rows = p.K / p.group;
+  // register double buffer: the next atom's four 128-bit loads (and its
+  // scales) are in flight while the current atom is dequantized
+  uint4 cur[4], nxt[4];
+  uint32_t s2c[2], zmc[2], s2n[2], zmn[2];
+  auto fetch = [&](int kb, uint4 (&c)[4], uint32_t (&s2)[2], uint32_t (&zm2)[2]) {
+    const uint4 *atom = reinterpret_cast<const uint4 *>(p.qw + atom_offset(kb, na, KB));
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = ldg_stream(atom + lane + 32 * i);
     const int g = (kb * ATOM_K) / p.group;
-    const uint16_t *srow = p.scales + static_cast<size_t>(g) * N;
-    const uint8_t *zrow = p.zeros ? p.zeros + static_cast<size_t>(g) * (N / 2) : nullptr;
-    const uint32_t s2[2] = {dup16(__ldg(srow + nA)), dup16(__ldg(srow + nB))};
-    const uint32_t zm2[2] = {zero_magic2<BF16>(zero_of(zrow, nA)),
-                             zero_magic2<BF16>(zero_of(zrow, nB))};
+    s2[0] = dup16(__ldg(p.scales + scale_index(g, nA, G_rows)));
+    s2[1] = dup16(__ldg(p.scales + scale_index(g, nB, G_rows)));
+    zm2[0] = zero_magic2<BF16>(zero_of(p.zeros, g, nA, G_rows));
+    zm2[1] = zero_magic2<BF16>(zero_of(p.zeros, g, nB, G_rows));
+  };
+  int kb = kb0 + warp;
+  if (kb < kb1) fetch(kb, cur, s2c, zmc);
+  for (; kb < kb1; kb += GEMV_WARPS) {
+    const int kbn = kb + GEMV_WARPS;
+    if (kbn < kb1) fetch(kbn, nxt, s2n, zmn);
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
       const int col = ci & 1, h = ci >> 1;
-      const uint32_t w[4] = {c[ci].x, c[ci].y, c[ci].z, c[ci].w};
+      const uint32_t w[4] = {cur[ci].x, cur[ci].y, cur[ci].z, cur[ci].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         uint32_t d[4];
-        dequant_word<BF16>(w[j], zm2[col], s2[col], d);
+        dequant_word<BF16>(w[j], zmc[col], s2c[col], d);
         float wf[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -129,6 +137,12 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
         }
       }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+    s2c[0] = s2n[0];
+    s2c[1] = s2n[1];
+    zmc[0] = zmn[0];
+    zmc[1] = zmn[1];
   }
   // per-warp partials -> shared memory, then a fixed-order sum over warps
 #pragma unroll

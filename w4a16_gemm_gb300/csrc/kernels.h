@@ -12,6 +12,7 @@ cudaError_t launch_repack(const uint8_t *q, uint8_t *qw, int K, int N, unsigned 
                           cudaStream_t st);
 cudaError_t launch_pack_zeros(const uint8_t *z, uint8_t *zp, int rows, int N, unsigned int *err,
                               cudaStream_t st);
+cudaError_t launch_pack_scales(const uint16_t *s, uint16_t *sp, int rows, int N, cudaStream_t st);
 cudaError_t launch_dequant(const uint8_t *qw, const uint16_t *scales, const uint8_t *zeros,
                            uint16_t *out, int K, int N, int group, bool bf16, cudaStream_t st);
 
@@ -29,8 +30,12 @@ struct GemmArgs {
   unsigned int *err;
   int M, N, K, group;
   int splits;
-  int kb_per_split;  // 64-wide K blocks per split
+  int kb_per_split;  // 64-wide K blocks per split (a multiple of the TC stage's k-blocks)
+  int act_map_3d;    // TC: the activation tensor map is 3-D (64 x M x K/64)
   unsigned long long limit_ns;
+  // Debug builds compiled with -DTMW4_TRACE record per-stage SM cycle
+  // stamps of CTA (0,0,0) here ([8][256] slots); nullptr otherwise.
+  long long *trace;
 };
 
 // GEMV (CUDA cores): rows_tmpl in {1,2,4,8} >= M.  Shared memory bytes:
@@ -40,6 +45,7 @@ cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, cudaStream_
 // tcgen05 kernel.  block_m in {16,32,64,128,256}, dq_warps in {4,8}.
 size_t tc_smem_bytes(int block_m);
 int tc_stages(int block_m);
+int tc_kblocks_per_stage(int block_m);
 cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                       int dq_warps, cudaStream_t st);
 

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
     }
   }
   __syncthreads();
-  uint32_t *out = reinterpret_cast<uint32_t *>(qw + (static_cast<size_t>(kb) * (N / ATOM_N) + na) * ATOM_BYTES);
+  uint32_t *out = reinterpret_cast<uint32_t *>(qw + atom_offset(kb, na, K / ATOM_K));
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int widx = t + 256 * r;
@@ -50,15 +50,26 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
   }
 }
 
+// zeros [K/G][N] bytes -> tile-major nibbles; one thread per output byte.
 __global__ void pack_zeros_kernel(const uint8_t *__restrict__ z, uint8_t *__restrict__ zp,
                                   int rows, int N, unsigned int *err) {
   const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t total = static_cast<size_t>(rows) * (N / 2);
   if (i >= total) return;
   const size_t g = i / (N / 2), c = i % (N / 2);
-  const uint32_t lo = z[g * N + 2 * c], hi = z[g * N + 2 * c + 1];
+  const int n = static_cast<int>(2 * c);
+  const uint32_t lo = z[g * N + n], hi = z[g * N + n + 1];
   if ((lo | hi) > 15u) atomicOr(err, TM_DEVERR_BAD_CODE);
-  zp[i] = static_cast<uint8_t>((lo & 0xFu) | ((hi & 0xFu) << 4));
+  zp[zero_byte(static_cast<int>(g), n, rows)] = static_cast<uint8_t>((lo & 0xFu) | ((hi & 0xFu) << 4));
+}
+
+// scales [K/G][N] -> tile-major [N/128][K/G][128]; one thread per scale.
+__global__ void pack_scales_kernel(const uint16_t *__restrict__ s, uint16_t *__restrict__ sp,
+                                   int rows, int N) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<size_t>(rows) * N) return;
+  const int g = static_cast<int>(i / N), n = static_cast<int>(i % N);
+  sp[scale_index(g, n, rows)] = s[i];
 }
 
 // One thread per 16-byte chunk: 32 consecutive K values of one column.
@@ -71,15 +82,14 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
   const size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nchunks = static_cast<size_t>(K) * N / 32;
   if (c >= nchunks) return;
-  const size_t atom = c >> 7;
-  const int cidx = static_cast<int>(c & 127), h = cidx >> 6, nl = cidx & 63;
-  const int natoms_n = N / ATOM_N;
-  const int kb = static_cast<int>(atom / natoms_n), na = static_cast<int>(atom % natoms_n);
-  const int k0 = kb * ATOM_K + 32 * h, n = na * ATOM_N + nl;
+  const int KB = K / ATOM_K, G_rows = K / group;
+  const size_t block = c >> 8;                     // 4096-byte tile block
+  const int nt = static_cast<int>(block / KB), kb = static_cast<int>(block % KB);
+  const int inblk = static_cast<int>(c & 255), a = inblk >> 7, h = (inblk >> 6) & 1, nl = inblk & 63;
+  const int k0 = kb * ATOM_K + 32 * h, n = nt * TILE_N + a * ATOM_N + nl;
   const int g = k0 / group;
-  const uint32_t s2 = dup16(scales[static_cast<size_t>(g) * N + n]);
-  const uint32_t zm2 = zero_magic2<BF16>(
-      zero_of(zeros ? zeros + static_cast<size_t>(g) * (N / 2) : nullptr, n));
+  const uint32_t s2 = dup16(scales[scale_index(g, n, G_rows)]);
+  const uint32_t zm2 = zero_magic2<BF16>(zero_of(zeros, g, n, G_rows));
   const uint4 v = *reinterpret_cast<const uint4 *>(qw + c * 16);
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -107,6 +117,13 @@ cudaError_t launch_pack_zeros(const uint8_t *z, uint8_t *zp, int rows, int N, un
   const size_t total = static_cast<size_t>(rows) * (N / 2);
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
   pack_zeros_kernel<<<blocks, 256, 0, st>>>(z, zp, rows, N, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_scales(const uint16_t *s, uint16_t *sp, int rows, int N, cudaStream_t st) {
+  const size_t total = static_cast<size_t>(rows) * N;
+  const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
+  pack_scales_kernel<<<blocks, 256, 0, st>>>(s, sp, rows, N);
   return cudaGetLastError();
 }
 

@@ -14,7 +14,8 @@
 //   warp 1      TMEM allocator and the single MMA-issuing thread:
 //               tcgen05.mma kind::f16, D[128 x BLOCK_M] (fp32, TMEM) +=
 //               A[128 x 16] (TMEM) * B[16 x BLOCK_M] (shared memory).
-//   warps 2..   dequant warps: thread i owns weight column n0+i (TMEM lane i),
+//   warps 2..   dequant warpgroups (stage i goes to warpgroup i % count); in
+//               each, thread i owns weight column n0+i (TMEM lane i),
 //               reads its 32-byte slice of the stage with two 128-bit shared
 //               loads, dequantizes exactly (w = T(s*(q-z))) and writes the
 //               32 packed pairs to a TMEM A stage with tcgen05.st; they then
@@ -38,28 +39,35 @@ namespace tmw4 {
 namespace {
 
 constexpr int BLOCK_N = 128;               // weight columns per CTA = MMA M
-constexpr int BLOCK_K = 64;                // K per stage = one atom row
-constexpr int W_STAGE_BYTES = BLOCK_N * BLOCK_K / 2;  // 4096
-constexpr int SC_STAGE_BYTES = BLOCK_N * 2;            // 256
-constexpr int ZP_STAGE_BYTES = BLOCK_N / 2;            // 64
-constexpr int TMEM_A_STAGES = 4;
-constexpr int TMEM_A_COLS = BLOCK_K / 2;   // 32 columns of packed pairs per stage
+constexpr int BLOCK_K = 64;                // K per k-block (one TMEM A slot)
+constexpr int W_KB_BYTES = BLOCK_N * BLOCK_K / 2;     // 4096: one tile block
+constexpr int SC_GROUP_BYTES = BLOCK_N * 2;           // 256: one group row of scales
+constexpr int ZP_GROUP_BYTES = BLOCK_N / 2;           // 64: one group row of zeros
+constexpr int TMEM_A_COLS = BLOCK_K / 2;   // 32 columns of packed pairs per k-block
 
-__host__ __device__ constexpr int stages_for(int block_m) {
-  return block_m <= 16 ? 16 : block_m <= 32 ? 12 : block_m <= 64 ? 8 : block_m <= 128 ? 8 : 5;
+// k-blocks per shared-memory stage: small tiles move more weight per stage so
+// that one stage (one bulk copy of contiguous tile blocks) amortises the
+// fixed cost of issuing its copies.
+__host__ __device__ constexpr int kbs_for(int block_m) {
+  return block_m <= 32 ? 4 : block_m <= 64 ? 2 : 1;
 }
-__host__ __device__ constexpr int a_stage_bytes(int block_m) { return block_m * BLOCK_K * 2; }
+__host__ __device__ constexpr int a_kb_bytes(int block_m) { return block_m * BLOCK_K * 2; }
+__host__ __device__ constexpr int stage_bytes(int block_m) {
+  return kbs_for(block_m) * (a_kb_bytes(block_m) + W_KB_BYTES + SC_GROUP_BYTES + ZP_GROUP_BYTES);
+}
+__host__ __device__ constexpr int stages_for(int block_m) {
+  return block_m <= 16 ? 4 : block_m <= 32 ? 3 : block_m <= 64 ? 4 : block_m <= 128 ? 8 : 5;
+}
+// TMEM: D occupies columns [0, max(32, BLOCK_M)); the rest of a 256-column
+// (BLOCK_M <= 128) or 512-column allocation is a ring of k-block A slots.
 __host__ __device__ constexpr int tmem_a_col0(int block_m) { return block_m < 32 ? 32 : block_m; }
-__host__ __device__ constexpr int tmem_cols(int block_m) {
-  // power of two >= D columns + A stages
-  return (tmem_a_col0(block_m) + TMEM_A_STAGES * TMEM_A_COLS) <= 128   ? 128
-         : (tmem_a_col0(block_m) + TMEM_A_STAGES * TMEM_A_COLS) <= 256 ? 256
-                                                                       : 512;
+__host__ __device__ constexpr int tmem_cols(int block_m) { return block_m <= 128 ? 256 : 512; }
+__host__ __device__ constexpr int tmem_a_stages(int block_m) {
+  return (tmem_cols(block_m) - tmem_a_col0(block_m)) / TMEM_A_COLS;
 }
 __host__ __device__ constexpr size_t smem_bytes_for(int block_m) {
   return 1024 /* alignment slack */ +
-         static_cast<size_t>(stages_for(block_m)) *
-             (a_stage_bytes(block_m) + W_STAGE_BYTES + SC_STAGE_BYTES + ZP_STAGE_BYTES) +
+         static_cast<size_t>(stages_for(block_m)) * stage_bytes(block_m) +
          512 /* barriers and flags */;
 }
 
@@ -80,53 +88,78 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 }  // namespace
 
-template <bool BF16, int BLOCK_M, int DQ_WARPS>
-__global__ void __launch_bounds__(64 + 32 * DQ_WARPS, 1)
+#ifdef TMW4_TRACE
+#define TMW4_STAMP(slot, idx)                                                              \
+  do {                                                                                     \
+    if (p.trace != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&     \
+        (idx) < 256)                                                                       \
+      p.trace[(slot) * 256 + (idx)] = clock64();                                           \
+  } while (0)
+#else
+#define TMW4_STAMP(slot, idx) \
+  do {                        \
+  } while (0)
+#endif
+
+// DQ_WG dequant warpgroups; warpgroup g dequantizes the shared-memory stages
+// j with j % DQ_WG == g, so DQ_WG stages are in flight in the ALUs at once.
+template <bool BF16, int BLOCK_M, int DQ_WG>
+__global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
   constexpr int STAGES = stages_for(BLOCK_M);
-  constexpr int A_BYTES = a_stage_bytes(BLOCK_M);
+  constexpr int KBS = kbs_for(BLOCK_M);
+  constexpr int A_KB = a_kb_bytes(BLOCK_M);
+  constexpr int A_STAGE = KBS * A_KB;
+  constexpr int W_STAGE = KBS * W_KB_BYTES;
+  constexpr int SC_STAGE = KBS * SC_GROUP_BYTES;   // room for KBS groups (G = 64)
+  constexpr int ZP_STAGE = KBS * ZP_GROUP_BYTES;
   constexpr int TMEM_COLS = tmem_cols(BLOCK_M);
   constexpr int A_COL0 = tmem_a_col0(BLOCK_M);
+  constexpr int TS = tmem_a_stages(BLOCK_M);
   constexpr uint32_t IDESC = idesc_f16(BF16 ? 1u : 0u, 128u, static_cast<uint32_t>(BLOCK_M));
-  constexpr int DQ_THREADS = 32 * DQ_WARPS;
-  constexpr int PARTS = DQ_WARPS / 4;       // dequant warps per TMEM lane quarter
-  constexpr int HALVES_PER_PART = 2 / PARTS;
+  constexpr int DQ_THREADS = 128 * DQ_WG;
   static_assert(BLOCK_M % 16 == 0 && BLOCK_M >= 16 && BLOCK_M <= 256, "MMA N");
-  static_assert(DQ_WARPS == 4 || DQ_WARPS == 8, "dequant warps");
+  static_assert(DQ_WG == 1 || DQ_WG == 2 || DQ_WG == 4, "dequant warpgroups");
+  static_assert(TS >= 2, "TMEM A slots");
+  static_assert(A_KB % 1024 == 0, "swizzle atoms");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *sA = smem;                                         // [STAGES][A_BYTES]
-  uint8_t *sW = sA + STAGES * A_BYTES;                        // [STAGES][4096]
-  uint8_t *sSC = sW + STAGES * W_STAGE_BYTES;                 // [STAGES][256]
-  uint8_t *sZP = sSC + STAGES * SC_STAGE_BYTES;               // [STAGES][64]
-  uint64_t *full_bar = reinterpret_cast<uint64_t *>(sZP + STAGES * ZP_STAGE_BYTES);
+  uint8_t *sA = smem;                              // [STAGES][KBS][BLOCK_M x 128 B]
+  uint8_t *sW = sA + STAGES * A_STAGE;             // [STAGES][KBS][4096]
+  uint8_t *sSC = sW + STAGES * W_STAGE;            // [STAGES][groups][256]
+  uint8_t *sZP = sSC + STAGES * SC_STAGE;          // [STAGES][groups][64]
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(sZP + STAGES * ZP_STAGE);
   uint64_t *empty_bar = full_bar + STAGES;
   uint64_t *afull_bar = empty_bar + STAGES;
-  uint64_t *aempty_bar = afull_bar + TMEM_A_STAGES;
-  uint64_t *accum_bar = aempty_bar + TMEM_A_STAGES;
+  uint64_t *aempty_bar = afull_bar + TS;
+  uint64_t *accum_bar = aempty_bar + TS;
   uint64_t *drain_bar = accum_bar + 1;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   int *last_flag = reinterpret_cast<int *>(tmem_holder + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BLOCK_N;
+  const int nt = blockIdx.x;
+  const int n0 = nt * BLOCK_N;
   const int m0 = blockIdx.y * BLOCK_M;
   const int split = blockIdx.z;
   const int KB = p.K / BLOCK_K;
+  const int G_rows = p.K / p.group;
   const int kb0 = split * p.kb_per_split;
   const int nkb = max(0, min(KB, kb0 + p.kb_per_split) - kb0);
+  const int nstages = (nkb + KBS - 1) / KBS;
   const int N = p.N, M = p.M;
 
   if (threadIdx.x == 0) {
+    TMW4_STAMP(7, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar + s, 1);
-      mbar_init(empty_bar + s, 1 + DQ_WARPS);
+      mbar_init(empty_bar + s, 1 + 4);   // MMA commit + the 4 warps of one warpgroup
     }
-    for (int t = 0; t < TMEM_A_STAGES; ++t) {
-      mbar_init(afull_bar + t, DQ_WARPS);
+    for (int t = 0; t < TS; ++t) {
+      mbar_init(afull_bar + t, 4);
       mbar_init(aempty_bar + t, 1);
     }
     mbar_init(accum_bar, 1);
@@ -144,32 +177,43 @@ __global__ void __launch_bounds__(64 + 32 * DQ_WARPS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  if (threadIdx.x == 0) TMW4_STAMP(7, 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint32_t tx = A_BYTES + W_STAGE_BYTES + SC_STAGE_BYTES +
-                          (p.zeros != nullptr ? ZP_STAGE_BYTES : 0);
       int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (i >= STAGES &&
+      for (int j = 0; j < nstages; ++j) {
+        const int s = j % STAGES;
+        const uint32_t ph = (j / STAGES) & 1;
+        if (j >= STAGES &&
             !mbar_wait_bounded(empty_bar + s, ph ^ 1u, p.limit_ns, abort_flag, p.err))
           break;
-        const int kb = kb0 + i;
-        const int g = (kb * BLOCK_K) / p.group;
+        const int kbf = kb0 + j * KBS;
+        const int nb = min(KBS, nkb - j * KBS);
+        const int gf = (kbf * BLOCK_K) / p.group;
+        const int gl = ((kbf + nb) * BLOCK_K - 1) / p.group;
+        const int ng = gl - gf + 1;
+        const uint32_t a_bytes = (p.act_map_3d ? KBS : nb) * A_KB;
+        const uint32_t tx = a_bytes + nb * W_KB_BYTES + ng * SC_GROUP_BYTES +
+                            (p.zeros != nullptr ? ng * ZP_GROUP_BYTES : 0);
         mbar_arrive_expect_tx(full_bar + s, tx);
-        tma_load_2d(sA + s * A_BYTES, &tmap_a, kb * BLOCK_K, m0, full_bar + s);
-        tma_bulk_g2s(sW + s * W_STAGE_BYTES,
-                     p.qw + (static_cast<size_t>(kb) * (N / ATOM_N) + n0 / ATOM_N) * ATOM_BYTES,
-                     W_STAGE_BYTES, full_bar + s);
-        tma_bulk_g2s(sSC + s * SC_STAGE_BYTES, p.scales + static_cast<size_t>(g) * N + n0,
-                     SC_STAGE_BYTES, full_bar + s);
+        if (p.act_map_3d) {
+          tma_load_3d(sA + s * A_STAGE, &tmap_a, 0, m0, kbf, full_bar + s);
+        } else {
+          for (int b = 0; b < nb; ++b)
+            tma_load_2d(sA + s * A_STAGE + b * A_KB, &tmap_a, (kbf + b) * BLOCK_K, m0, full_bar + s);
+        }
+        tma_bulk_g2s(sW + s * W_STAGE, p.qw + (static_cast<size_t>(nt) * KB + kbf) * W_KB_BYTES,
+                     nb * W_KB_BYTES, full_bar + s);
+        tma_bulk_g2s(sSC + s * SC_STAGE, p.scales + (static_cast<size_t>(nt) * G_rows + gf) * BLOCK_N,
+                     ng * SC_GROUP_BYTES, full_bar + s);
         if (p.zeros != nullptr)
-          tma_bulk_g2s(sZP + s * ZP_STAGE_BYTES, p.zeros + static_cast<size_t>(g) * (N / 2) + n0 / 2,
-                       ZP_STAGE_BYTES, full_bar + s);
-        issued = i + 1;
+          tma_bulk_g2s(sZP + s * ZP_STAGE,
+                       p.zeros + (static_cast<size_t>(nt) * G_rows + gf) * ZP_GROUP_BYTES,
+                       ng * ZP_GROUP_BYTES, full_bar + s);
+        TMW4_STAMP(0, j);
+        issued = j + 1;
       }
       // drain: every copy issued must have landed before the CTA exits
       for (int s = 0; s < STAGES && s < issued; ++s) {
@@ -181,25 +225,33 @@ __global__ void __launch_bounds__(64 + 32 * DQ_WARPS, 1)
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       bool any = false, ok = true;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        const int t = i % TMEM_A_STAGES;
-        if (!mbar_wait_bounded(full_bar + s, (i / STAGES) & 1, p.limit_ns, abort_flag, p.err) ||
-            !mbar_wait_bounded(afull_bar + t, (i / TMEM_A_STAGES) & 1, p.limit_ns, abort_flag,
-                               p.err)) {
+      for (int j = 0; j < nstages && ok; ++j) {
+        const int s = j % STAGES;
+        if (!mbar_wait_bounded(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t a_base = smem_u32(sA + s * A_BYTES);
+        const int nb = min(KBS, nkb - j * KBS);
+        for (int b = 0; b < nb; ++b) {
+          const int i = j * KBS + b;
+          const int t = i % TS;
+          if (!mbar_wait_bounded(afull_bar + t, (i / TS) & 1, p.limit_ns, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          TMW4_STAMP(4, i);
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + s * A_STAGE + b * A_KB);
 #pragma unroll
-        for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
-          tc_mma_ts(tmem, tmem + A_COL0 + t * TMEM_A_COLS + kk * 8,
-                    smem_desc_k128(a_base + kk * 32), IDESC, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
+            tc_mma_ts(tmem, tmem + A_COL0 + t * TMEM_A_COLS + kk * 8,
+                      smem_desc_k128(a_base + kk * 32), IDESC, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(aempty_bar + t);
+          TMW4_STAMP(5, i);
+          any = true;
         }
-        tc_commit(empty_bar + s);
-        tc_commit(aempty_bar + t);
-        any = true;
+        if (ok) tc_commit(empty_bar + s);
       }
       if (ok && any) {
         tc_commit(accum_bar);
@@ -211,71 +263,93 @@ __global__ void __launch_bounds__(64 + 32 * DQ_WARPS, 1)
   } else {
     // ------------------------------------------------- dequant + epilogue
     const int dw = warp - 2;
+    const int wg = dw >> 2;                   // this warp's warpgroup
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-    const int part = dw / 4;                  // which K half(s) of the stage
     const int r = quarter * 32 + lane;        // weight column within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int atom = r >> 6, nl = r & 63;
+    const uint8_t *wsrc = sW + atom * ATOM_BYTES + nl * 16;
     bool ok = true;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % STAGES;
-      const int t = i % TMEM_A_STAGES;
+    for (int j = wg; j < nstages && ok; j += DQ_WG) {
+      const int s = j % STAGES;
       // every lane waits (acquire for its own loads); the warp then agrees,
       // so tcgen05.st below is always executed by the whole warp
-      bool got = mbar_wait_bounded(full_bar + s, (i / STAGES) & 1, p.limit_ns, abort_flag, p.err);
-      if (got && i >= TMEM_A_STAGES)
-        got = mbar_wait_bounded(aempty_bar + t, ((i / TMEM_A_STAGES) & 1) ^ 1u, p.limit_ns,
-                                abort_flag, p.err);
+      const bool got =
+          mbar_wait_bounded(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err);
       if (!__all_sync(0xFFFFFFFFu, got)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const uint16_t sc = reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE_BYTES)[r];
-      const uint32_t z = p.zeros != nullptr
-                             ? (static_cast<uint32_t>(sZP[s * ZP_STAGE_BYTES + (r >> 1)]) >>
-                                ((r & 1) * 4)) & 0xFu
-                             : 8u;
-      uint4 v[HALVES_PER_PART];
-#pragma unroll
-      for (int hh = 0; hh < HALVES_PER_PART; ++hh) {
-        const int h = part * HALVES_PER_PART + hh;
-        v[hh] = *reinterpret_cast<const uint4 *>(sW + s * W_STAGE_BYTES + atom * ATOM_BYTES +
-                                                 h * 1024 + nl * 16);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar + s);
-      const uint32_t s2 = dup16(sc), zm2 = zero_magic2<BF16>(z);
-      __syncwarp();
-#pragma unroll
-      for (int hh = 0; hh < HALVES_PER_PART; ++hh) {
-        const int h = part * HALVES_PER_PART + hh;
-        uint32_t d[16];
-        const uint32_t w[4] = {v[hh].x, v[hh].y, v[hh].z, v[hh].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t o[4];
-          dequant_word<BF16>(w[j], zm2, s2, o);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) d[4 * j + q] = o[q];
+      if (quarter == 2 && lane == 0) TMW4_STAMP(1, j);
+      const int kbf = kb0 + j * KBS;
+      const int nb = min(KBS, nkb - j * KBS);
+      const int gf = (kbf * BLOCK_K) / p.group;
+      for (int b = 0; b < nb; ++b) {
+        const int i = j * KBS + b;
+        const int t = i % TS;
+        if (i >= TS) {
+          const bool free_slot = mbar_wait_bounded(aempty_bar + t, ((i / TS) & 1) ^ 1u,
+                                                   p.limit_ns, abort_flag, p.err);
+          if (!__all_sync(0xFFFFFFFFu, free_slot)) {
+            ok = false;
+            break;
+          }
         }
-        tmem_st_16(tmem + lane_addr + A_COL0 + t * TMEM_A_COLS + h * 16, d);
+        tc_fence_after();
+        if (quarter == 2 && lane == 0) TMW4_STAMP(2, i);
+        const int gi = ((kbf + b) * BLOCK_K) / p.group - gf;
+        const uint16_t sc =
+            reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + gi * SC_GROUP_BYTES)[r];
+        const uint32_t z =
+            p.zeros != nullptr
+                ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + gi * ZP_GROUP_BYTES + (r >> 1)]) >>
+                   ((r & 1) * 4)) & 0xFu
+                : 8u;
+        const uint8_t *src = wsrc + s * W_STAGE + b * W_KB_BYTES;
+        const uint4 v0 = *reinterpret_cast<const uint4 *>(src);
+        const uint4 v1 = *reinterpret_cast<const uint4 *>(src + 1024);
+        if (b == nb - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar + s);   // last read of this stage done
+        }
+        const uint32_t s2 = dup16(sc), zm2 = zero_magic2<BF16>(z);
+        uint32_t d0[16], d1[16];
+        {
+          const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+          const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t o[4];
+            dequant_word<BF16>(w0[q4], zm2, s2, o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d0[4 * q4 + q] = o[q];
+            dequant_word<BF16>(w1[q4], zm2, s2, o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d1[4 * q4 + q] = o[q];
+          }
+        }
+        __syncwarp();
+        const uint32_t ta = tmem + lane_addr + A_COL0 + t * TMEM_A_COLS;
+        tmem_st_16(ta, d0);
+        tmem_st_16(ta + 16, d1);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (quarter == 2 && lane == 0) TMW4_STAMP(3, i);
+        if (lane == 0) mbar_arrive(afull_bar + t);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(afull_bar + t);
     }
 
     // ------------------------------------------------------------ epilogue
     if (ok && nkb > 0) ok = mbar_wait_bounded(accum_bar, 0, p.limit_ns, abort_flag, p.err);
     ok = __all_sync(0xFFFFFFFFu, ok);
+    if (dw == 0 && lane == 0) TMW4_STAMP(6, 0);
     tc_fence_after();
     const int n = n0 + r;
     const bool direct = (p.splits == 1);
     if (ok) {
-      // columns of D are rows m of C; each part takes alternate 16-column chunks
-      for (int c0 = part * 16; c0 < BLOCK_M; c0 += 16 * PARTS) {
+      // columns of D are rows m of C; warpgroups take alternate 16-column chunks
+      for (int c0 = wg * 16; c0 < BLOCK_M; c0 += 16 * DQ_WG) {
         if (m0 + c0 >= M) break;  // warp-uniform
         uint32_t v[16];
         __syncwarp();
@@ -310,12 +384,22 @@ __global__ void __launch_bounds__(64 + 32 * DQ_WARPS, 1)
       named_bar_sync(1, DQ_THREADS);
       if (*last_flag) {
         __threadfence();
-        for (int c0 = part; c0 < BLOCK_M; c0 += PARTS) {
-          const int m = m0 + c0;
+        // fixed split order per element; 8 independent loads in flight
+        const size_t split_stride = static_cast<size_t>(M) * N;
+        for (int c = wg; c < BLOCK_M; c += DQ_WG) {
+          const int m = m0 + c;
           if (m >= M) break;
+          const float *src = p.ws + static_cast<size_t>(m) * N + n;
           float acc = 0.f;
-          for (int s = 0; s < p.splits; ++s)
-            acc += __ldcg(p.ws + (static_cast<size_t>(s) * M + m) * N + n);
+          int sp = 0;
+          for (; sp + 8 <= p.splits; sp += 8) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (sp + j) * split_stride);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc += v[j];
+          }
+          for (; sp < p.splits; ++sp) acc += __ldcg(src + sp * split_stride);
           p.C[static_cast<size_t>(m) * N + n] = f32_to_16<BF16>(acc);
         }
         if (dw == 0 && lane == 0) *ctr = 0u;
@@ -325,6 +409,7 @@ __global__ void __launch_bounds__(64 + 32 * DQ_WARPS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) TMW4_STAMP(6, 1);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -334,10 +419,11 @@ __global__ void __launch_bounds__(64 + 32 * DQ_WARPS, 1)
 
 size_t tc_smem_bytes(int block_m) { return smem_bytes_for(block_m); }
 int tc_stages(int block_m) { return stages_for(block_m); }
+int tc_kblocks_per_stage(int block_m) { return kbs_for(block_m); }
 
-template <bool BF16, int BLOCK_M, int DQ_WARPS>
+template <bool BF16, int BLOCK_M, int DQ_WG>
 static cudaError_t launch_tc_t(const GemmArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
-  auto kern = tc_gemm_kernel<BF16, BLOCK_M, DQ_WARPS>;
+  auto kern = tc_gemm_kernel<BF16, BLOCK_M, DQ_WG>;
   const size_t smem = smem_bytes_for(BLOCK_M);
   static int attr_device = -1;  // shared-memory opt-in, once per device
   int dev = 0;
@@ -349,34 +435,32 @@ static cudaError_t launch_tc_t(const GemmArgs &a, const CUtensorMap &tmap, cudaS
     attr_device = dev;
   }
   dim3 grid(a.N / BLOCK_N, (a.M + BLOCK_M - 1) / BLOCK_M, a.splits);
-  kern<<<grid, 64 + 32 * DQ_WARPS, smem, st>>>(tmap, a);
+  kern<<<grid, 64 + 128 * DQ_WG, smem, st>>>(tmap, a);
   return cudaGetLastError();
+}
+
+template <bool BF16, int BLOCK_M>
+static cudaError_t launch_tc_bm(const GemmArgs &a, const CUtensorMap &tmap, int dq_warps,
+                                cudaStream_t st) {
+  switch (dq_warps) {
+    case 4: return launch_tc_t<BF16, BLOCK_M, 1>(a, tmap, st);
+    case 8: return launch_tc_t<BF16, BLOCK_M, 2>(a, tmap, st);
+    case 16: return launch_tc_t<BF16, BLOCK_M, 4>(a, tmap, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <bool BF16>
 static cudaError_t launch_tc_dtype(const GemmArgs &a, const CUtensorMap &tmap, int block_m,
                                    int dq, cudaStream_t st) {
-  if (dq == 4) {
-    switch (block_m) {
-      case 16: return launch_tc_t<BF16, 16, 4>(a, tmap, st);
-      case 32: return launch_tc_t<BF16, 32, 4>(a, tmap, st);
-      case 64: return launch_tc_t<BF16, 64, 4>(a, tmap, st);
-      case 128: return launch_tc_t<BF16, 128, 4>(a, tmap, st);
-      case 256: return launch_tc_t<BF16, 256, 4>(a, tmap, st);
-      default: return cudaErrorInvalidValue;
-    }
+  switch (block_m) {
+    case 16: return launch_tc_bm<BF16, 16>(a, tmap, dq, st);
+    case 32: return launch_tc_bm<BF16, 32>(a, tmap, dq, st);
+    case 64: return launch_tc_bm<BF16, 64>(a, tmap, dq, st);
+    case 128: return launch_tc_bm<BF16, 128>(a, tmap, dq, st);
+    case 256: return launch_tc_bm<BF16, 256>(a, tmap, dq, st);
+    default: return cudaErrorInvalidValue;
   }
-  if (dq == 8) {
-    switch (block_m) {
-      case 16: return launch_tc_t<BF16, 16, 8>(a, tmap, st);
-      case 32: return launch_tc_t<BF16, 32, 8>(a, tmap, st);
-      case 64: return launch_tc_t<BF16, 64, 8>(a, tmap, st);
-      case 128: return launch_tc_t<BF16, 128, 8>(a, tmap, st);
-      case 256: return launch_tc_t<BF16, 256, 8>(a, tmap, st);
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,

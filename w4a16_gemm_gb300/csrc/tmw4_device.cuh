@@ -10,10 +10,28 @@ namespace tmw4 {
 constexpr unsigned int TM_DEVERR_TIMEOUT = 1u;   // a bounded wait gave up
 constexpr unsigned int TM_DEVERR_BAD_CODE = 2u;  // a code byte above 15 was packed
 
-// Geometry of the packed weight (see include/tmw4.h).
+// Geometry of the packed weight (see include/tmw4.h): 128-column tiles,
+// each tile's 64-K blocks contiguous (4096 bytes = two 2048-byte atoms of
+// 64 columns); scales [N/128][K/G][128], zeros [N/128][K/G][64 bytes].
 constexpr int ATOM_K = 64;
 constexpr int ATOM_N = 64;
 constexpr int ATOM_BYTES = ATOM_K * ATOM_N / 2;  // 2048
+constexpr int TILE_N = 128;
+constexpr int BLOCK_BYTES = 2 * ATOM_BYTES;      // one tile x one 64-K block
+
+// Byte offset of atom (kb, na) (na = 64-column index) in the packed stream.
+__host__ __device__ __forceinline__ size_t atom_offset(int kb, int na, int KB) {
+  return (static_cast<size_t>(na >> 1) * KB + kb) * BLOCK_BYTES +
+         static_cast<size_t>(na & 1) * ATOM_BYTES;
+}
+// Index of scale (g, n) in the tile-major scale array (G_rows = K/G).
+__host__ __device__ __forceinline__ size_t scale_index(int g, int n, int G_rows) {
+  return (static_cast<size_t>(n >> 7) * G_rows + g) * TILE_N + (n & 127);
+}
+// Byte holding zero (g, n) in the tile-major nibble array (odd n: high nibble).
+__host__ __device__ __forceinline__ size_t zero_byte(int g, int n, int G_rows) {
+  return (static_cast<size_t>(n >> 7) * G_rows + g) * (TILE_N / 2) + ((n & 127) >> 1);
+}
 
 // Exponent "magic" that turns a 4-bit code c placed in the low mantissa bits
 // into the exact value MAGIC + c: 1024 + c for fp16 (0x6400), 128 + c for
