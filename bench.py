@@ -41,7 +41,16 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
-    ap.add_argument("--tune", action="store_true", help="run tm_tune for every (shape, M) first")
+    ap.add_argument("--no-tune", action="store_true",
+                    help="skip tm_tune (variant selection from measured throughput); use the "
+                         "table in TM_TUNE_CACHE or the built-in rule")
+    ap.add_argument("--warm-replays", type=int, default=0,
+                    help="untimed graph replays before the timed one (0: as many as fit in 1.5 s)")
+    ap.add_argument("--case", type=str, default=None,
+                    help="K,N,M: time one decode-format problem instead of the sweep (for profiling)")
+    ap.add_argument("--variant", type=str, default=None,
+                    help="with --case: kernel:block_m:split_k:dq_warps (default: tuned/auto)")
+    ap.add_argument("--reps", type=int, default=6, help="with --case: launches")
     return ap.parse_args()
 
 
@@ -195,7 +204,7 @@ def run_ours(args, rank: int, world: int):
     del dev_inputs
     torch.cuda.synchronize()
 
-    if args.tune:
+    if not args.no_tune:
         for si in range(len(shapes)):
             binding.tune(packed[(0, si, wl.ms[0])], list(wl.ms))
 
@@ -249,10 +258,15 @@ def run_ours(args, rank: int, world: int):
     sampler.start()
     # graphs replay on the current stream: make it the launch stream
     with torch.cuda.stream(stream):
-        t_end = time.time() + 1.5
-        while time.time() < t_end:
-            graph.replay()
+        if args.warm_replays > 0:
+            for _ in range(args.warm_replays):
+                graph.replay()
             torch.cuda.synchronize()
+        else:
+            t_end = time.time() + 1.5
+            while time.time() < t_end:
+                graph.replay()
+                torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
@@ -467,8 +481,48 @@ def run_reference(args) -> dict:
     }
 
 
+def run_case(args) -> dict:
+    """One problem of the decode format, repeated (a small case for ncu captures)."""
+    import torch
+
+    from w4a16_gemm_gb300 import binding, build, synth
+
+    build.build()
+    K, N, M = (int(x) for x in args.case.split(","))
+    qw, a = synth.random_problem(1, M, K, N)
+    p = binding.to_device(qw)
+    Ws = [binding.pack(p.q, p.scales, p.zeros, qw.group) for _ in range(4)]
+    A = binding.acts_to_device(a, torch.float16)
+    C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    cfg = None
+    if args.variant:
+        k, bm, sk, dq = args.variant.split(":")
+        cfg = dict(kernel=k, block_m=int(bm), split_k=int(sk), dq_warps=int(dq))
+    elif not args.no_tune:
+        binding.tune(Ws[0], [M])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(2):
+        binding.gemm(A, Ws[i % 4], out=C, config=cfg)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(args.reps):
+        binding.gemm(A, Ws[i % 4], out=C, config=cfg)
+    e1.record()
+    torch.cuda.synchronize()
+    binding.poll_error()
+    us = e0.elapsed_time(e1) * 1e3 / args.reps
+    wb = weight_bytes(K, N, 128, False)
+    return {"metric": "W4A16 GEMM weight GB/s (single problem)", "value": round(wb / us / 1e3, 1),
+            "unit": "GB/s", "case": {"K": K, "N": N, "M": M}, "us_per_launch": round(us, 2),
+            "variant": cfg if cfg else binding.select(Ws[0], M),
+            "note": "eager launches, 4 rotated weight copies; for profiling, not the headline"}
+
+
 def main():
     args = parse()
+    if args.case:
+        print(json.dumps(run_case(args)), flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -156,6 +156,16 @@ tm_status tm_select(const tm_packed *W, int M, tm_config *out);
  * receives nM configs. */
 tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *stream, tm_config *best_out);
 
+/* Pipeline geometry of the tcgen05 variant (block_m, dq_warps); host only,
+ * needs no GPU.  *stages: shared-memory stages; *kblocks_per_stage: 64-K
+ * blocks per stage; *tmem_slots: TMEM slots for dequantized 64-K blocks;
+ * *legal: 1 if the variant can run, 0 if it is refused because some of its
+ * mbarrier parity waits could start two phases ahead (the pages give no
+ * pipeline; this is the Blackwell restatement of the overlap of pith.science
+ * review Figure 9). */
+tm_status tm_tc_pipeline(int block_m, int dq_warps, int *stages, int *kblocks_per_stage,
+                         int *tmem_slots, int *legal);
+
 /* Loads/saves the tuned table (JSON lines) from/to a host path. */
 tm_status tm_tune_load(const char *path);
 tm_status tm_tune_save(const char *path);

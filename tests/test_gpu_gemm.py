@@ -28,6 +28,11 @@ def _run(qw, a_bits, config=None):
     return C, W
 
 
+# (block_m, dq_warps) pairs whose pipeline cannot keep every parity wait within
+# one phase (four dequant warpgroups need STAGES % 4 == 0 and 13 / 7 TMEM A slots)
+ILLEGAL = {(16, 16), (64, 16)}
+
+
 def _variants(M):
     out = []
     if M <= 8:
@@ -35,6 +40,8 @@ def _variants(M):
     for bm in (16, 32, 64, 128, 256):
         for sk in (1, 3):
             for dq in (4, 8, 16):
+                if (bm, dq) in ILLEGAL:
+                    continue                      # rejected: see test_illegal_variants
                 if bm >= 128 and dq != 8 and sk == 3:
                     continue
                 out.append(dict(kernel="tc", block_m=bm, split_k=sk, dq_warps=dq))
@@ -66,6 +73,27 @@ def test_small_all_variants(M, K, N, G, dt, sym):
         binding.poll_error()
         r = oracle.max_err_ratio(c_values(C), c_ref, rel=TOL)
         assert r <= 1.0, (cfg, r)
+
+
+def test_repeated_runs_are_identical():
+    """Many launches of the deepest-pipelined variants give bit-identical C
+    (catches pipeline races that only show under some schedules)."""
+    M, K, N = 512, 4096, 2048
+    qw, a = synth.random_problem(23, M, K, N, 128, "bf16")
+    c_ref = oracle.gemm_ref(a[:64], oracle.dequant_bits(qw.q, qw.scales, qw.zeros, 128, "bf16"), "bf16")
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, torch.bfloat16)
+    for cfg in (dict(kernel="tc", block_m=256, split_k=1, dq_warps=16),
+                dict(kernel="tc", block_m=128, split_k=1, dq_warps=16),
+                dict(kernel="tc", block_m=32, split_k=2, dq_warps=16),
+                dict(kernel="tc", block_m=16, split_k=4, dq_warps=8)):
+        first = gemm_poisoned(A, W, config=cfg)
+        torch.cuda.synchronize()
+        assert oracle.max_err_ratio(c_values(first)[:64], c_ref, rel=TOL) <= 1.0, cfg
+        for _ in range(25):
+            C = gemm_poisoned(A, W, config=cfg)
+            torch.cuda.synchronize()
+            assert torch.equal(C.view(torch.int16), first.view(torch.int16)), cfg
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64, 200])
@@ -108,7 +136,7 @@ def test_one_hot_rows_reproduce_dequantized_weight():
     for cfg in [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=4),
                 dict(kernel="tc", block_m=16, split_k=1), dict(kernel="tc", block_m=16, split_k=3),
                 dict(kernel="tc", block_m=128, split_k=1, dq_warps=8),
-                dict(kernel="tc", block_m=32, split_k=5, dq_warps=16)]:
+                dict(kernel="tc", block_m=32, split_k=5, dq_warps=8)]:
         if cfg["kernel"] == "gemv" and len(ks) > 8:
             continue
         C = gemm_poisoned(A, W, config=cfg)
@@ -170,6 +198,35 @@ def test_symmetric_equals_asymmetric_with_zero_eight():
         assert torch.equal(Cs.view(torch.int16), Ca.view(torch.int16))
 
 
+def test_long_k_every_legal_variant():
+    """K = 8192 (128 blocks): many wrap-arounds of every stage and TMEM ring."""
+    M, K, N = 40, 8192, 256
+    qw, a = synth.random_problem(21, M, K, N)
+    c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, 128, "f16"), "f16")
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, torch.float16)
+    for bm in (16, 32, 64, 128, 256):
+        for dq in (4, 8, 16):
+            if (bm, dq) in ILLEGAL:
+                continue
+            for sk in (1, 2):
+                C = gemm_poisoned(A, W, config=dict(kernel="tc", block_m=bm, split_k=sk, dq_warps=dq))
+                torch.cuda.synchronize()
+                binding.poll_error()
+                assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, (bm, dq, sk)
+
+
+def test_illegal_variants_are_rejected():
+    """Variants whose parity waits could run two phases ahead are refused."""
+    qw, a = synth.random_problem(22, 16, 512, 256)
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, torch.float16)
+    for bm, _ in sorted(ILLEGAL):
+        with pytest.raises(binding.TmError) as e:
+            binding.gemm(A, W, config=dict(kernel="tc", block_m=bm, dq_warps=16))
+        assert e.value.status == binding.TM_ERR_UNSUPPORTED
+
+
 def test_m_zero_is_noop_and_argument_errors():
     qw, a = synth.random_problem(9, 4, 256, 256)
     W = packed_from(qw)
@@ -208,8 +265,8 @@ def weight_cache():
 @pytest.mark.parametrize("wl,si,M", FULL, ids=lambda x: str(x))
 def test_full_size_sampled(wl, si, M, weight_cache):
     """Every (workload, shape, M) at full size, in the launch configuration the
-    benchmark times (tm_gemm_w4a16's own selection); sampled rows and columns
-    are checked against the oracle."""
+    benchmark times (the variant tm_tune measures fastest, then tm_gemm_w4a16);
+    sampled rows and columns are checked against the oracle."""
     key = (wl, si)
     if key not in weight_cache:
         weight_cache.clear()
@@ -218,6 +275,7 @@ def test_full_size_sampled(wl, si, M, weight_cache):
     qw, W = weight_cache[key]
     a = synth.activations(wl, si, M)
     A = binding.acts_to_device(a, TORCH_DT[qw.dtype])
+    binding.tune(W, [M])                      # the benchmark's selection procedure
     C = gemm_poisoned(A, W)
     torch.cuda.synchronize()
     binding.poll_error()

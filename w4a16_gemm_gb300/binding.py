@@ -67,6 +67,7 @@ SIGNATURES = [
     ("tm_tune_save", _I, [ctypes.c_char_p]),
     ("tm_poll_error", _I, [_VP]),
     ("tm_selftest_wait_timeout", _I, [_LL, _VP]),
+    ("tm_tc_pipeline", _I, [_I, _I] + [ctypes.POINTER(_I)] * 4),
     ("tm_last_error", ctypes.c_char_p, []),
     ("tm_version", ctypes.c_char_p, []),
 ]
@@ -240,6 +241,14 @@ def poll_status(stream=None) -> int:
 
 def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     _check(lib().tm_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def tc_pipeline(block_m: int, dq_warps: int) -> dict:
+    """Pipeline geometry of a tcgen05 variant (no GPU needed)."""
+    v = [ctypes.c_int() for _ in range(4)]
+    _check(lib().tm_tc_pipeline(int(block_m), int(dq_warps), *[ctypes.byref(x) for x in v]))
+    return {"stages": v[0].value, "kblocks_per_stage": v[1].value, "tmem_slots": v[2].value,
+            "legal": bool(v[3].value)}
 
 
 def version() -> str:

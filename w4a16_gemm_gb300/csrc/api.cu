@@ -88,8 +88,8 @@ static tm_status error_word(int dev, unsigned int **out) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_err_word[dev] == nullptr) {
     unsigned int *p = nullptr;
-    TM_CUDA(cudaMalloc(&p, sizeof(unsigned int)), "cudaMalloc(error word)");
-    TM_CUDA(cudaMemset(p, 0, sizeof(unsigned int)), "cudaMemset(error word)");
+    TM_CUDA(cudaMalloc(&p, TM_ERR_WORDS * sizeof(unsigned int)), "cudaMalloc(error word)");
+    TM_CUDA(cudaMemset(p, 0, TM_ERR_WORDS * sizeof(unsigned int)), "cudaMemset(error word)");
     g_err_word[dev] = p;
   }
   *out = g_err_word[dev];
@@ -271,6 +271,10 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
     if (c->dq_warps == 0) c->dq_warps = 8;
     if (c->dq_warps != 4 && c->dq_warps != 8 && c->dq_warps != 16) {
       if (why) *why = "TC dq_warps must be 4, 8 or 16";
+      return false;
+    }
+    if (!tc_variant_ok(c->block_m, c->dq_warps)) {
+      if (why) *why = "this block_m has too few pipeline stages for that many dequant warps";
       return false;
     }
     if ((M + c->block_m - 1) / c->block_m > 65535) {
@@ -535,6 +539,17 @@ tm_status tm_gemm_w4a16_ex(const void *A, const tm_packed *W, void *C, int M, in
   return run_gemm(A, W, C, M, c, static_cast<cudaStream_t>(stream));
 }
 
+tm_status tm_tc_pipeline(int block_m, int dq_warps, int *stages, int *kblocks_per_stage,
+                         int *tmem_slots, int *legal) {
+  if (stages == nullptr || kblocks_per_stage == nullptr || tmem_slots == nullptr || legal == nullptr)
+    return fail(TM_ERR_INVALID_ARG, "output pointers must not be NULL");
+  if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128 && block_m != 256)
+    return fail(TM_ERR_INVALID_ARG, "block_m must be 16, 32, 64, 128 or 256");
+  tc_pipeline(block_m, stages, kblocks_per_stage, tmem_slots);
+  *legal = tc_variant_ok(block_m, dq_warps) ? 1 : 0;
+  return TM_OK;
+}
+
 tm_status tm_poll_error(void *stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TM_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
@@ -544,10 +559,11 @@ tm_status tm_poll_error(void *stream) {
   unsigned int *err = nullptr;
   s = error_word(dev, &err);
   if (s != TM_OK) return s;
-  unsigned int v = 0;
-  TM_CUDA(cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost), "cudaMemcpy(error word)");
+  unsigned int w[TM_ERR_WORDS] = {};
+  TM_CUDA(cudaMemcpy(w, err, sizeof(w), cudaMemcpyDeviceToHost), "cudaMemcpy(error word)");
+  const unsigned int v = w[0];
   if (v != 0) {
-    TM_CUDA(cudaMemset(err, 0, sizeof(unsigned int)), "cudaMemset(error word)");
+    TM_CUDA(cudaMemset(err, 0, sizeof(w)), "cudaMemset(error word)");
     // a kernel that gave up may have left split-K arrival counters raised
     std::lock_guard<std::mutex> lk(g_mu);
     for (auto &kv : g_ws)
@@ -555,7 +571,10 @@ tm_status tm_poll_error(void *stream) {
         TM_CUDA(cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(unsigned int)),
                 "cudaMemset(counters)");
   }
-  if (v & TM_DEVERR_TIMEOUT) return fail(TM_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (v & TM_DEVERR_TIMEOUT)
+    return fail(TM_ERR_TIMEOUT,
+                "a bounded device wait gave up (site %u, block %u, thread %u, step %u, parity %u)",
+                w[2], w[3], w[4], w[5], w[6]);
   if (v & TM_DEVERR_BAD_CODE) return fail(TM_ERR_INVALID_ARG, "a packed code or zero exceeded 15");
   return TM_OK;
 }

@@ -3,6 +3,9 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "ptx.cuh"
 #include "tmw4_device.cuh"
 
@@ -11,23 +14,49 @@ namespace tmw4 {
 // Eight codes of one word (value e at nibble NIBBLE_POS[e], i.e. word order
 // e7 e5 e3 e1 e6 e4 e2 e0 -- pith.science review, Figures 23/24) become four
 // packed 16-bit pairs {w0,w1}, {w2,w3}, {w4,w5}, {w6,w7} (low half = even
-// element), with w = T(s * (q - z)):
-//   mask 0x000F000F after a shift by 4i isolates the pair (e_2i, e_2i+1);
-//   OR-ing the exponent magic gives MAGIC + q exactly; subtracting the
-//   duplicated (MAGIC + z) is exact; the multiply by the duplicated scale is
-//   the single round-to-nearest-even.
+// element), with w = T(s * (q - z)) rounded once to nearest even.
+//
+// fp16: nibble pairs (e0,e1) and (e4,e5) sit in the low nibble of each
+// half-word (directly, and after one shift by 8); OR-ing 0x6400 gives
+// 1024 + q exactly and subtracting the duplicated 1024 + z is exact.  Pairs
+// (e2,e3) and (e6,e7) sit one nibble higher: OR-ing 0x6400 gives 1024 + 16q
+// exactly, and one fused x * (1/16) - (64 + z) yields q - z exactly (the
+// product is exact, so the single rounding of the FMA is exact too).  The
+// multiply by the scale is the only rounding of w.  bf16 (7 mantissa bits)
+// has no room for the higher nibble, so every pair is shifted down first.
 // zm2 = (MAGIC + z) in both halves, s2 = scale in both halves.
 template <bool BF16>
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zm2, uint32_t s2,
                                              uint32_t (&out)[4]) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162 *>(&zm2);
+    const __nv_bfloat162 s = *reinterpret_cast<const __nv_bfloat162 *>(&s2);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t x = ((w >> (4 * i)) & 0x000F000Fu) | Magic<BF16>::pair;
-    if constexpr (BF16) {
-      out[i] = mul_rn_bf16x2(sub_rn_bf16x2(x, zm2), s2);
-    } else {
-      out[i] = mul_rn_f16x2(sub_rn_f16x2(x, zm2), s2);
+    for (int i = 0; i < 4; ++i) {
+      uint32_t x = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+      __nv_bfloat162 d = __hmul2(__hsub2(*reinterpret_cast<__nv_bfloat162 *>(&x), z), s);
+      out[i] = *reinterpret_cast<uint32_t *>(&d);
     }
+  } else {
+    const __half2 z = *reinterpret_cast<const __half2 *>(&zm2);
+    const __half2 s = *reinterpret_cast<const __half2 *>(&s2);
+    // -(64 + z) = 960 - (1024 + z), exact
+    const __half2 z16 = __hsub2(__float2half2_rn(960.0f), z);
+    const __half2 sixteenth = __float2half2_rn(0.0625f);
+    const uint32_t hi = w >> 8;
+    uint32_t x0 = (w & 0x000F000Fu) | 0x64006400u;
+    uint32_t x1 = (w & 0x00F000F0u) | 0x64006400u;
+    uint32_t x2 = (hi & 0x000F000Fu) | 0x64006400u;
+    uint32_t x3 = (hi & 0x00F000F0u) | 0x64006400u;
+    const __half2 d0 = __hsub2(*reinterpret_cast<__half2 *>(&x0), z);
+    const __half2 d1 = __hfma2(*reinterpret_cast<__half2 *>(&x1), sixteenth, z16);
+    const __half2 d2 = __hsub2(*reinterpret_cast<__half2 *>(&x2), z);
+    const __half2 d3 = __hfma2(*reinterpret_cast<__half2 *>(&x3), sixteenth, z16);
+    __half2 r0 = __hmul2(d0, s), r1 = __hmul2(d1, s), r2 = __hmul2(d2, s), r3 = __hmul2(d3, s);
+    out[0] = *reinterpret_cast<uint32_t *>(&r0);
+    out[1] = *reinterpret_cast<uint32_t *>(&r1);
+    out[2] = *reinterpret_cast<uint32_t *>(&r2);
+    out[3] = *reinterpret_cast<uint32_t *>(&r3);
   }
 }
 

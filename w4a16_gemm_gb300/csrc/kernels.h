@@ -46,6 +46,10 @@ cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, cudaStream_
 size_t tc_smem_bytes(int block_m);
 int tc_stages(int block_m);
 int tc_kblocks_per_stage(int block_m);
+// Pipeline geometry of the tcgen05 kernel for a legal block_m.
+void tc_pipeline(int block_m, int *stages, int *kbs, int *tmem_slots);
+// Whether (block_m, dq_warps) is a legal tcgen05 variant (see tc_gemm.cu).
+bool tc_variant_ok(int block_m, int dq_warps);
 cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                       int dq_warps, cudaStream_t st);
 

@@ -64,10 +64,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  Gives up
 // after `limit_ns` (or as soon as *abort becomes non-zero), records
 // TM_DEVERR_TIMEOUT in the device error word and returns false.  No wait in
-// this library is unbounded.
+// this library is unbounded.  The first wait to give up on the device also
+// records where: err_word[1] = 1, [2] = site, [3] = linear block index,
+// [4] = thread index, [5] = the waiter's stage/step index, [6] = parity.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns, volatile int *abort,
-                                                  unsigned int *err_word) {
+                                                  unsigned int *err_word, unsigned site = 0,
+                                                  unsigned step = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
@@ -77,7 +80,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
       if (abort != nullptr && *abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         if (abort != nullptr) *abort = 1;
-        if (err_word != nullptr) atomicOr(err_word, TM_DEVERR_TIMEOUT);
+        if (err_word != nullptr) {
+          atomicOr(err_word, TM_DEVERR_TIMEOUT);
+          if (atomicCAS(err_word + 1, 0u, 1u) == 0u) {
+            err_word[2] = site;
+            err_word[3] = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+            err_word[4] = threadIdx.x;
+            err_word[5] = step;
+            err_word[6] = parity;
+          }
+        }
         return false;
       }
     }

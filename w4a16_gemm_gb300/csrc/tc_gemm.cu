@@ -49,14 +49,14 @@ constexpr int TMEM_A_COLS = BLOCK_K / 2;   // 32 columns of packed pairs per k-b
 // that one stage (one bulk copy of contiguous tile blocks) amortises the
 // fixed cost of issuing its copies.
 __host__ __device__ constexpr int kbs_for(int block_m) {
-  return block_m <= 32 ? 4 : block_m <= 64 ? 2 : 1;
+  return block_m <= 16 ? 4 : block_m <= 64 ? 2 : 1;
 }
 __host__ __device__ constexpr int a_kb_bytes(int block_m) { return block_m * BLOCK_K * 2; }
 __host__ __device__ constexpr int stage_bytes(int block_m) {
   return kbs_for(block_m) * (a_kb_bytes(block_m) + W_KB_BYTES + SC_GROUP_BYTES + ZP_GROUP_BYTES);
 }
 __host__ __device__ constexpr int stages_for(int block_m) {
-  return block_m <= 16 ? 4 : block_m <= 32 ? 3 : block_m <= 64 ? 4 : block_m <= 128 ? 8 : 5;
+  return block_m <= 64 ? 4 : block_m <= 128 ? 8 : 4;
 }
 // TMEM: D occupies columns [0, max(32, BLOCK_M)); the rest of a 256-column
 // (BLOCK_M <= 128) or 512-column allocation is a ring of k-block A slots.
@@ -64,6 +64,23 @@ __host__ __device__ constexpr int tmem_a_col0(int block_m) { return block_m < 32
 __host__ __device__ constexpr int tmem_cols(int block_m) { return block_m <= 128 ? 256 : 512; }
 __host__ __device__ constexpr int tmem_a_stages(int block_m) {
   return (tmem_cols(block_m) - tmem_a_col0(block_m)) / TMEM_A_COLS;
+}
+// Every mbarrier wait here is a parity wait, which cannot tell phase c from
+// phase c-2: it is correct only if, when a consumer starts waiting for the
+// c-th completion of a barrier, completion c-1 is already known to have
+// happened.  Copies issued in order may land out of order, so a dequant warp
+// may rely only on completions it has observed itself.  With DQ_WG
+// warpgroups taking alternate stages that holds iff
+//   STAGES % DQ_WG == 0    (each shared-memory slot is always consumed by the
+//                           same warpgroup, which saw the slot's previous fill)
+//   TS >= (DQ_WG - 1) * KBS + 1
+//                          (a warp's previous wait on a TMEM slot proves the
+//                           MMAs two uses back retired; MMAs retire in order)
+// A randomized model of this protocol (tests/test_pipeline_protocol.py)
+// checks both conditions.
+__host__ __device__ constexpr bool variant_ok(int block_m, int dq_wg) {
+  return stages_for(block_m) % dq_wg == 0 &&
+         tmem_a_stages(block_m) >= (dq_wg - 1) * kbs_for(block_m) + 1;
 }
 __host__ __device__ constexpr size_t smem_bytes_for(int block_m) {
   return 1024 /* alignment slack */ +
@@ -121,6 +138,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
   static_assert(BLOCK_M % 16 == 0 && BLOCK_M >= 16 && BLOCK_M <= 256, "MMA N");
   static_assert(DQ_WG == 1 || DQ_WG == 2 || DQ_WG == 4, "dequant warpgroups");
   static_assert(TS >= 2, "TMEM A slots");
+  static_assert(variant_ok(BLOCK_M, DQ_WG), "parity waits need at most one phase of lead");
   static_assert(A_KB % 1024 == 0, "swizzle atoms");
 
   extern __shared__ uint8_t smem_raw[];
@@ -187,7 +205,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         const int s = j % STAGES;
         const uint32_t ph = (j / STAGES) & 1;
         if (j >= STAGES &&
-            !mbar_wait_bounded(empty_bar + s, ph ^ 1u, p.limit_ns, abort_flag, p.err))
+            !mbar_wait_bounded(empty_bar + s, ph ^ 1u, p.limit_ns, abort_flag, p.err, SITE_PRODUCER_EMPTY, j))
           break;
         const int kbf = kb0 + j * KBS;
         const int nb = min(KBS, nkb - j * KBS);
@@ -218,7 +236,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
       // drain: every copy issued must have landed before the CTA exits
       for (int s = 0; s < STAGES && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / STAGES) * STAGES;
-        mbar_wait_bounded(full_bar + s, (last / STAGES) & 1, p.limit_ns, nullptr, p.err);
+        mbar_wait_bounded(full_bar + s, (last / STAGES) & 1, p.limit_ns, nullptr, p.err, SITE_DRAIN_TMA, last);
       }
     }
   } else if (warp == 1) {
@@ -227,7 +245,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
       bool any = false, ok = true;
       for (int j = 0; j < nstages && ok; ++j) {
         const int s = j % STAGES;
-        if (!mbar_wait_bounded(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err)) {
+        if (!mbar_wait_bounded(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err, SITE_MMA_FULL, j)) {
           ok = false;
           break;
         }
@@ -235,7 +253,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         for (int b = 0; b < nb; ++b) {
           const int i = j * KBS + b;
           const int t = i % TS;
-          if (!mbar_wait_bounded(afull_bar + t, (i / TS) & 1, p.limit_ns, abort_flag, p.err)) {
+          if (!mbar_wait_bounded(afull_bar + t, (i / TS) & 1, p.limit_ns, abort_flag, p.err, SITE_MMA_AFULL, i)) {
             ok = false;
             break;
           }
@@ -257,7 +275,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         tc_commit(accum_bar);
       } else if (any) {
         tc_commit(drain_bar);
-        mbar_wait_bounded(drain_bar, 0, p.limit_ns, nullptr, p.err);
+        mbar_wait_bounded(drain_bar, 0, p.limit_ns, nullptr, p.err, SITE_DRAIN_MMA, 0);
       }
     }
   } else {
@@ -275,7 +293,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
       // every lane waits (acquire for its own loads); the warp then agrees,
       // so tcgen05.st below is always executed by the whole warp
       const bool got =
-          mbar_wait_bounded(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err);
+          mbar_wait_bounded(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL, j);
       if (!__all_sync(0xFFFFFFFFu, got)) {
         ok = false;
         break;
@@ -289,7 +307,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         const int t = i % TS;
         if (i >= TS) {
           const bool free_slot = mbar_wait_bounded(aempty_bar + t, ((i / TS) & 1) ^ 1u,
-                                                   p.limit_ns, abort_flag, p.err);
+                                                   p.limit_ns, abort_flag, p.err, SITE_DQ_AEMPTY, i);
           if (!__all_sync(0xFFFFFFFFu, free_slot)) {
             ok = false;
             break;
@@ -308,6 +326,10 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         const uint8_t *src = wsrc + s * W_STAGE + b * W_KB_BYTES;
         const uint4 v0 = *reinterpret_cast<const uint4 *>(src);
         const uint4 v1 = *reinterpret_cast<const uint4 *>(src + 1024);
+#ifdef TMW4_TRACE
+        if (p.trace != nullptr && quarter == 2 && lane == 0 && ((v0.x ^ v1.y) == 0x9E3779B9u)) p.trace[8 * 256] = 1;
+        if (quarter == 2 && lane == 0) TMW4_STAMP(8, i);
+#endif
         if (b == nb - 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(empty_bar + s);   // last read of this stage done
@@ -328,11 +350,21 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
             for (int q = 0; q < 4; ++q) d1[4 * q4 + q] = o[q];
           }
         }
+#ifdef TMW4_TRACE
+        if (p.trace != nullptr && quarter == 2 && lane == 0 && ((d0[3] ^ d1[7]) == 0x9E3779B9u)) p.trace[8 * 256 + 1] = 1;
+        if (quarter == 2 && lane == 0) TMW4_STAMP(9, i);
+#endif
         __syncwarp();
         const uint32_t ta = tmem + lane_addr + A_COL0 + t * TMEM_A_COLS;
         tmem_st_16(ta, d0);
         tmem_st_16(ta + 16, d1);
+#ifdef TMW4_TRACE
+        if (quarter == 2 && lane == 0) TMW4_STAMP(10, i);
+#endif
         tmem_wait_st();
+#ifdef TMW4_TRACE
+        if (quarter == 2 && lane == 0) TMW4_STAMP(11, i);
+#endif
         tc_fence_before();
         __syncwarp();
         if (quarter == 2 && lane == 0) TMW4_STAMP(3, i);
@@ -341,7 +373,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && nkb > 0) ok = mbar_wait_bounded(accum_bar, 0, p.limit_ns, abort_flag, p.err);
+    if (ok && nkb > 0) ok = mbar_wait_bounded(accum_bar, 0, p.limit_ns, abort_flag, p.err, SITE_EPI_ACCUM, 0);
     ok = __all_sync(0xFFFFFFFFu, ok);
     if (dw == 0 && lane == 0) TMW4_STAMP(6, 0);
     tc_fence_after();
@@ -420,6 +452,14 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
 size_t tc_smem_bytes(int block_m) { return smem_bytes_for(block_m); }
 int tc_stages(int block_m) { return stages_for(block_m); }
 int tc_kblocks_per_stage(int block_m) { return kbs_for(block_m); }
+void tc_pipeline(int block_m, int *stages, int *kbs, int *tmem_slots) {
+  *stages = stages_for(block_m);
+  *kbs = kbs_for(block_m);
+  *tmem_slots = tmem_a_stages(block_m);
+}
+bool tc_variant_ok(int block_m, int dq_warps) {
+  return (dq_warps == 4 || dq_warps == 8 || dq_warps == 16) && variant_ok(block_m, dq_warps / 4);
+}
 
 template <bool BF16, int BLOCK_M, int DQ_WG>
 static cudaError_t launch_tc_t(const GemmArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
@@ -444,8 +484,12 @@ static cudaError_t launch_tc_bm(const GemmArgs &a, const CUtensorMap &tmap, int 
                                 cudaStream_t st) {
   switch (dq_warps) {
     case 4: return launch_tc_t<BF16, BLOCK_M, 1>(a, tmap, st);
-    case 8: return launch_tc_t<BF16, BLOCK_M, 2>(a, tmap, st);
-    case 16: return launch_tc_t<BF16, BLOCK_M, 4>(a, tmap, st);
+    case 8:
+      if constexpr (variant_ok(BLOCK_M, 2)) return launch_tc_t<BF16, BLOCK_M, 2>(a, tmap, st);
+      return cudaErrorInvalidValue;
+    case 16:
+      if constexpr (variant_ok(BLOCK_M, 4)) return launch_tc_t<BF16, BLOCK_M, 4>(a, tmap, st);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -481,7 +525,7 @@ __global__ void wait_selftest_kernel(unsigned int *err, unsigned long long limit
   __syncthreads();
   if (threadIdx.x == 0) {
     // nothing arrives on `bar`: the wait must give up after limit_ns
-    mbar_wait_bounded(&bar, 0, limit_ns, &abort_flag, err);
+    mbar_wait_bounded(&bar, 0, limit_ns, &abort_flag, err, SITE_SELFTEST, 0);
   }
   __syncthreads();
 }

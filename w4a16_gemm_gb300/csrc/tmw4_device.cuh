@@ -9,6 +9,20 @@ namespace tmw4 {
 // Bits of the per-device error word (read and cleared by tm_poll_error).
 constexpr unsigned int TM_DEVERR_TIMEOUT = 1u;   // a bounded wait gave up
 constexpr unsigned int TM_DEVERR_BAD_CODE = 2u;  // a code byte above 15 was packed
+constexpr int TM_ERR_WORDS = 8;                  // error word + where the first wait gave up
+
+// Wait sites recorded when a bounded wait gives up.
+enum WaitSite : unsigned {
+  SITE_PRODUCER_EMPTY = 1,
+  SITE_MMA_FULL = 2,
+  SITE_MMA_AFULL = 3,
+  SITE_DQ_FULL = 4,
+  SITE_DQ_AEMPTY = 5,
+  SITE_EPI_ACCUM = 6,
+  SITE_DRAIN_TMA = 7,
+  SITE_DRAIN_MMA = 8,
+  SITE_SELFTEST = 9
+};
 
 // Geometry of the packed weight (see include/tmw4.h): 128-column tiles,
 // each tile's 64-K blocks contiguous (4096 bytes = two 2048-byte atoms of
