@@ -5,7 +5,7 @@
 // non-coherent loads (512 contiguous bytes per warp instruction: coalesced,
 // pith.science review, Figure 22), dequantize in registers exactly as the
 // dequant-only kernel does, and accumulate in fp32 against activations held
-// in shared memory.  Partials of the eight warps are summed in a fixed order;
+// in shared memory (mixed-precision fp16/bf16 x fp16/bf16 -> fp32 FMAs).  Partials of the eight warps are summed in a fixed order;
 // with split-K, partials go to the workspace and the last CTA of a strip to
 // arrive sums them in split order, so results do not depend on scheduling.
 #include <cstdint>
@@ -16,16 +16,6 @@
 #include "kernels.h"
 
 namespace tmw4 {
-
-template <bool BF16>
-__device__ __forceinline__ float2 pair_to_float2(uint32_t v) {
-  if constexpr (BF16) {
-    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-  } else {
-    __half2 h = *reinterpret_cast<__half2 *>(&v);
-    return __half22float2(h);
-  }
-}
 
 template <bool BF16>
 __device__ __forceinline__ uint16_t float_to_16(float x) {
@@ -48,32 +38,50 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
 
 constexpr int GEMV_WARPS = 8;
 
+// acc += w.lo * a.lo + w.hi * a.hi with fp32 accumulation, for packed 16-bit
+// pairs w and a.  The mixed-precision FMA multiplies the two 16-bit inputs
+// exactly (at most 22 significant bits) and rounds once into fp32, exactly as
+// converting both to fp32 and using an fp32 FMA would.
+template <bool BF16>
+__device__ __forceinline__ float fma_pair(uint32_t w, uint32_t a, float acc) {
+  float r;
+  if constexpr (BF16) {
+    asm("{\n\t.reg .b16 wl, wh, al, ah;\n\t"
+        "mov.b32 {wl, wh}, %1;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, wl, al, %3;\n\t"
+        "fma.rn.f32.bf16 %0, wh, ah, %0;\n\t}"
+        : "=f"(r) : "r"(w), "r"(a), "f"(acc));
+  } else {
+    asm("{\n\t.reg .f16 wl, wh, al, ah;\n\t"
+        "mov.b32 {wl, wh}, %1;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.f16 %0, wl, al, %3;\n\t"
+        "fma.rn.f32.f16 %0, wh, ah, %0;\n\t}"
+        : "=f"(r) : "r"(w), "r"(a), "f"(acc));
+  }
+  return r;
+}
+
 template <bool BF16, int MT>
 __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
   extern __shared__ float4 smem_f4[];
-  float *smem = reinterpret_cast<float *>(smem_f4);
+  float *red = reinterpret_cast<float *>(smem_f4);          // [GEMV_WARPS][MT][64]
+  uint16_t *As = reinterpret_cast<uint16_t *>(red + GEMV_WARPS * MT * 64);  // [MT][ldA]
   const int na = blockIdx.x, split = blockIdx.y;
   const int KB = p.K / ATOM_K;
   const int kb0 = split * p.kb_per_split;
   const int kb1 = min(KB, kb0 + p.kb_per_split);
   const int ldA = p.kb_per_split * ATOM_K;
-  float *As = smem;                       // [MT][ldA]
-  float *red = smem + MT * ldA;           // [GEMV_WARPS][MT][64]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int M = p.M, N = p.N;
 
-  // activations of this K range -> fp32 shared memory (rows >= M are zero)
+  // activations of this K range -> shared memory, 16 bytes per copy (rows >= M are zero)
   const int klen = (kb1 - kb0) * ATOM_K;
-  for (int idx = tid; idx < MT * (klen / 2); idx += blockDim.x) {
-    const int m = idx / (klen / 2), kk = (idx % (klen / 2)) * 2;
-    float2 f = make_float2(0.f, 0.f);
-    if (m < M) {
-      const uint32_t v = *reinterpret_cast<const uint32_t *>(p.A + static_cast<size_t>(m) * p.K +
-                                                             kb0 * ATOM_K + kk);
-      f = pair_to_float2<BF16>(v);
-    }
-    As[m * ldA + kk] = f.x;
-    As[m * ldA + kk + 1] = f.y;
+  for (int idx = tid; idx < MT * (klen / 8); idx += blockDim.x) {
+    const int m = idx / (klen / 8), kk = (idx % (klen / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M)
+      v = *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * p.K + kb0 * ATOM_K + kk);
+    *reinterpret_cast<uint4 *>(As + m * ldA + kk) = v;
   }
   __syncthreads();
 
@@ -112,27 +120,15 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
       for (int j = 0; j < 4; ++j) {
         uint32_t d[4];
         dequant_word<BF16>(w[j], zmc[col], s2c[col], d);
-        float wf[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = pair_to_float2<BF16>(d[i]);
-          wf[2 * i] = f.x;
-          wf[2 * i + 1] = f.y;
-        }
         const int kloc = (kb - kb0) * ATOM_K + 32 * h + 8 * j;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const float4 a0 = *reinterpret_cast<const float4 *>(As + m * ldA + kloc);
-          const float4 a1 = *reinterpret_cast<const float4 *>(As + m * ldA + kloc + 4);
+          const uint4 av = *reinterpret_cast<const uint4 *>(As + m * ldA + kloc);
           float s = acc[m][ci];
-          s = fmaf(wf[0], a0.x, s);
-          s = fmaf(wf[1], a0.y, s);
-          s = fmaf(wf[2], a0.z, s);
-          s = fmaf(wf[3], a0.w, s);
-          s = fmaf(wf[4], a1.x, s);
-          s = fmaf(wf[5], a1.y, s);
-          s = fmaf(wf[6], a1.z, s);
-          s = fmaf(wf[7], a1.w, s);
+          s = fma_pair<BF16>(d[0], av.x, s);
+          s = fma_pair<BF16>(d[1], av.y, s);
+          s = fma_pair<BF16>(d[2], av.z, s);
+          s = fma_pair<BF16>(d[3], av.w, s);
           acc[m][ci] = s;
         }
       }
@@ -201,8 +197,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
 }
 
 size_t gemv_smem_bytes(int rows_tmpl, int kb_per_split) {
-  return sizeof(float) * (static_cast<size_t>(rows_tmpl) * kb_per_split * ATOM_K +
-                          static_cast<size_t>(GEMV_WARPS) * rows_tmpl * 64);
+  return sizeof(float) * static_cast<size_t>(GEMV_WARPS) * rows_tmpl * 64 +
+         sizeof(uint16_t) * static_cast<size_t>(rows_tmpl) * kb_per_split * ATOM_K;
 }
 
 template <bool BF16, int MT>

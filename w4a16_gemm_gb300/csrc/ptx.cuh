@@ -49,6 +49,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
       : "memory");
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or the hint (ns) runs out, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -73,10 +88,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
                                                   unsigned step = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (((++spins) & 15u) == 0) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    {
       if (abort != nullptr && *abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         if (abort != nullptr) *abort = 1;
@@ -94,6 +108,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
       }
     }
   }
+}
+
+// Warp-wide bounded wait: lane 0 waits (sleeping in hardware), the warp
+// agrees on the outcome, then every lane takes its own acquire with one
+// non-blocking test of the (now completed) phase.  Must be called by all 32
+// lanes.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                               volatile int *abort, unsigned int *err_word,
+                                               unsigned site, unsigned step) {
+  const int lane = threadIdx.x & 31;
+  bool ok = true;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, limit_ns, abort, err_word, site, step);
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  if (ok) (void)mbar_try_wait(bar, parity);
+  return ok;
 }
 
 // --------------------------------------------------------------------- TMA
@@ -173,6 +202,24 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four MMAs over one 64-K block: A columns a_tmem + 0/8/16/24 (16 K each),
+// B descriptors b_desc + 0/2/4/6 (32 bytes further along K each, in 16-byte
+// units of the descriptor's start address).  `first` clears D on the first
+// MMA instead of accumulating.
+__device__ __forceinline__ void tc_mma_ts_kblock(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t first) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.eq.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(first), "r"(a_tmem + 8), "l"(b_desc + 2),
+      "r"(a_tmem + 16), "l"(b_desc + 4), "r"(a_tmem + 24), "l"(b_desc + 6)
       : "memory");
 }
 

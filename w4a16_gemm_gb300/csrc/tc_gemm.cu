@@ -243,6 +243,11 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       bool any = false, ok = true;
+      // descriptor of the B tile (activations) of stage 0, block 0; other
+      // tiles are a constant number of 16-byte units further on
+      const uint64_t desc0 = smem_desc_k128(smem_u32(sA));
+      uint32_t a_slot = tmem + A_COL0;      // TMEM A slot of block i (ring of TS)
+      int t = 0;
       for (int j = 0; j < nstages && ok; ++j) {
         const int s = j % STAGES;
         if (!mbar_wait_bounded(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err, SITE_MMA_FULL, j)) {
@@ -250,24 +255,29 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
           break;
         }
         const int nb = min(KBS, nkb - j * KBS);
+        const uint64_t desc_s = desc0 + static_cast<uint64_t>((s * A_STAGE) >> 4);
         for (int b = 0; b < nb; ++b) {
           const int i = j * KBS + b;
-          const int t = i % TS;
+#ifdef TMW4_TRACE
+          TMW4_STAMP(7, 2 + i);
+#endif
           if (!mbar_wait_bounded(afull_bar + t, (i / TS) & 1, p.limit_ns, abort_flag, p.err, SITE_MMA_AFULL, i)) {
             ok = false;
             break;
           }
           TMW4_STAMP(4, i);
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * A_STAGE + b * A_KB);
-#pragma unroll
-          for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
-            tc_mma_ts(tmem, tmem + A_COL0 + t * TMEM_A_COLS + kk * 8,
-                      smem_desc_k128(a_base + kk * 32), IDESC, (i > 0 || kk > 0) ? 1u : 0u);
-          }
+          tc_mma_ts_kblock(tmem, a_slot, desc_s + static_cast<uint64_t>((b * A_KB) >> 4), IDESC,
+                           i == 0 ? 1u : 0u);
           tc_commit(aempty_bar + t);
           TMW4_STAMP(5, i);
           any = true;
+          if (++t == TS) {
+            t = 0;
+            a_slot = tmem + A_COL0;
+          } else {
+            a_slot += TMEM_A_COLS;
+          }
         }
         if (ok) tc_commit(empty_bar + s);
       }
@@ -290,11 +300,10 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
     bool ok = true;
     for (int j = wg; j < nstages && ok; j += DQ_WG) {
       const int s = j % STAGES;
-      // every lane waits (acquire for its own loads); the warp then agrees,
-      // so tcgen05.st below is always executed by the whole warp
-      const bool got =
-          mbar_wait_bounded(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL, j);
-      if (!__all_sync(0xFFFFFFFFu, got)) {
+      // the warp agrees on the outcome, so tcgen05.st below is always executed
+      // by the whole warp
+      if (!mbar_wait_warp(full_bar + s, (j / STAGES) & 1, p.limit_ns, abort_flag, p.err,
+                          SITE_DQ_FULL, j)) {
         ok = false;
         break;
       }
@@ -305,13 +314,10 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
       for (int b = 0; b < nb; ++b) {
         const int i = j * KBS + b;
         const int t = i % TS;
-        if (i >= TS) {
-          const bool free_slot = mbar_wait_bounded(aempty_bar + t, ((i / TS) & 1) ^ 1u,
-                                                   p.limit_ns, abort_flag, p.err, SITE_DQ_AEMPTY, i);
-          if (!__all_sync(0xFFFFFFFFu, free_slot)) {
-            ok = false;
-            break;
-          }
+        if (i >= TS && !mbar_wait_warp(aempty_bar + t, ((i / TS) & 1) ^ 1u, p.limit_ns,
+                                       abort_flag, p.err, SITE_DQ_AEMPTY, i)) {
+          ok = false;
+          break;
         }
         tc_fence_after();
         if (quarter == 2 && lane == 0) TMW4_STAMP(2, i);
@@ -368,13 +374,17 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         tc_fence_before();
         __syncwarp();
         if (quarter == 2 && lane == 0) TMW4_STAMP(3, i);
+#ifdef TMW4_TRACE
+        if (lane == 0) TMW4_STAMP(12 + quarter, i);
+#endif
         if (lane == 0) mbar_arrive(afull_bar + t);
       }
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && nkb > 0) ok = mbar_wait_bounded(accum_bar, 0, p.limit_ns, abort_flag, p.err, SITE_EPI_ACCUM, 0);
     ok = __all_sync(0xFFFFFFFFu, ok);
+    if (ok && nkb > 0)
+      ok = mbar_wait_warp(accum_bar, 0, p.limit_ns, abort_flag, p.err, SITE_EPI_ACCUM, 0);
     if (dw == 0 && lane == 0) TMW4_STAMP(6, 0);
     tc_fence_after();
     const int n = n0 + r;
