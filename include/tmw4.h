@@ -133,6 +133,27 @@ tm_status tm_gemm_w4a16(const void *A, const tm_packed *W, void *C, int M, int N
 tm_status tm_gemm_w4a16_ex(const void *A, const tm_packed *W, void *C, int M, int N, int K,
                            const tm_config *cfg, void *stream);
 
+/* As tm_gemm_w4a16, for callers that cannot allocate device memory (an
+ * application that owns all GPU memory through its own pool, or a stream
+ * being captured when tm_gemm_w4a16's workspace would have to grow).  The
+ * paper has no counterpart; this is a deployment variant of the same GEMM.
+ *   Allocates nothing: no cudaMalloc/cudaFree and no allocating library
+ *   call.  Split-K partials and arrival counters live in static device
+ *   arrays of the library (8 MiB of partials and 16384 counters, held on
+ *   every GPU that loads the library until the process exits); a shape
+ *   whose selected variant needs more returns TM_ERR_UNSUPPORTED with the
+ *   sizes in tm_last_error().
+ *   The first call on a device looks up the arrays' device addresses
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls share one scratch per device and it keeps the last call's
+ *   contents: calls that overlap on the GPU (different streams, or
+ *   different host threads) race and give wrong results; order them.
+ *   Each call clears the counters it uses with cudaMemsetAsync on `stream`.
+ *   A bounded wait that gives up is recorded in a static device word that
+ *   tm_poll_error does not read; C is then undefined. */
+tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, void *C, int M, int N, int K,
+                                void *stream);
+
 /* Dequant-only: W_out [K][N] (device, handle's dtype) = T(s*(q - z)),
  * bit-exact with a single round-to-nearest-even per element. */
 tm_status tm_dequant_w4(const tm_packed *W, void *W_out, void *stream);

@@ -58,6 +58,7 @@ SIGNATURES = [
     ("tm_pack_w4", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
     ("tm_gemm_w4a16", _I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
     ("tm_gemm_w4a16_ex", _I, [_VP, _VP, _VP, _I, _I, _I, ctypes.POINTER(TmConfig), _VP]),
+    ("tm_gemm_w4a16_noalloc", _I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
     ("tm_dequant_w4", _I, [_VP, _VP, _VP]),
     ("tm_packed_free", _I, [_VP, _VP]),
     ("tm_packed_get", _I, [_VP, ctypes.POINTER(TmPackedInfo)]),

@@ -764,3 +764,111 @@ extern "C" tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *st
   if (p && *p) return tm_tune_save(p);
   return TM_OK;
 }
+
+// ======================================================================
+// GEMM without any device allocation.
+//
+// For callers that cannot allocate device memory: an allocator-less
+// embedding (the host application owns every byte of the GPU through its
+// own pool and forbids cudaMalloc), or a stream that is being captured when
+// the split-K workspace would otherwise have to grow.  The split-K partials,
+// the tile arrival counters and the device error words live in file-scope
+// static __device__ arrays of fixed size, loaded with the library and held
+// by every GPU that loads it until the process exits.  In host code the
+// array names are host-side stand-ins, not device addresses, so their device
+// addresses are fetched once per device with cudaGetSymbolAddress.
+// ======================================================================
+
+static constexpr size_t kStaticWsFloats = static_cast<size_t>(2) << 20;  // 8 MiB of partials
+static constexpr size_t kStaticCounters = 16384;                          // 64 KiB of counters
+
+static __device__ __align__(256) float g_static_ws[kStaticWsFloats];
+static __device__ __align__(256) unsigned int g_static_counters[kStaticCounters];
+static __device__ __align__(256) unsigned int g_static_err[TM_ERR_WORDS];
+
+struct StaticScratch {
+  bool ready = false;
+  float *ws = nullptr;
+  unsigned int *counters = nullptr;
+  unsigned int *err = nullptr;
+};
+static StaticScratch g_static[kMaxDevices];
+
+// Device addresses of the static arrays on device `dev` (which must be
+// current); fetched on the first call on that device.
+static tm_status static_scratch(int dev, StaticScratch **out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  StaticScratch &s = g_static[dev];
+  if (!s.ready) {
+    void *p = nullptr;
+    TM_CUDA(cudaGetSymbolAddress(&p, g_static_ws), "cudaGetSymbolAddress(split-K scratch)");
+    s.ws = static_cast<float *>(p);
+    TM_CUDA(cudaGetSymbolAddress(&p, g_static_counters), "cudaGetSymbolAddress(counters)");
+    s.counters = static_cast<unsigned int *>(p);
+    TM_CUDA(cudaGetSymbolAddress(&p, g_static_err), "cudaGetSymbolAddress(error words)");
+    s.err = static_cast<unsigned int *>(p);
+    s.ready = true;
+  }
+  *out = &s;
+  return TM_OK;
+}
+
+extern "C" tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, void *C, int M, int N,
+                                           int K, void *stream) {
+  tm_status s = check_gemm_args(A, W, C, M, N, K);
+  if (s != TM_OK || M == 0) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  StaticScratch *sc = nullptr;
+  s = static_scratch(W->device, &sc);
+  if (s != TM_OK) return s;
+  const tm_config cfg = select_config(W, M, W->device);
+  const int KB = W->K / 64;
+  GemmArgs a{};
+  a.qw = W->qw;
+  a.scales = W->scales;
+  a.zeros = W->symmetric ? nullptr : W->zeros;
+  a.A = static_cast<const uint16_t *>(A);
+  a.C = static_cast<uint16_t *>(C);
+  a.err = sc->err;
+  a.M = M;
+  a.N = W->N;
+  a.K = W->K;
+  a.group = W->group;
+  const int gran = cfg.kernel == TM_KERNEL_TC ? tc_kblocks_per_stage(cfg.block_m) : 1;
+  int per = (KB + cfg.split_k - 1) / cfg.split_k;
+  per = (per + gran - 1) / gran * gran;
+  a.kb_per_split = per;
+  a.splits = (KB + per - 1) / per;
+  a.limit_ns = wait_limit_ns();
+  const bool bf16 = W->dtype == TM_BF16;
+  if (a.splits > 1) {
+    const size_t ws_floats = static_cast<size_t>(a.splits) * M * W->N;
+    const size_t tiles = cfg.kernel == TM_KERNEL_GEMV
+                             ? static_cast<size_t>(W->N / 64)
+                             : static_cast<size_t>(W->N / 128) * ((M + cfg.block_m - 1) / cfg.block_m);
+    if (ws_floats > kStaticWsFloats || tiles > kStaticCounters)
+      return fail(TM_ERR_UNSUPPORTED,
+                  "tm_gemm_w4a16_noalloc: this shape needs %zu bytes of split-K scratch and %zu "
+                  "counters; the static scratch holds %zu bytes and %zu counters",
+                  ws_floats * sizeof(float), tiles, kStaticWsFloats * sizeof(float),
+                  kStaticCounters);
+    // the counters must start at zero (a kernel that gave up may have left
+    // some raised); clearing is stream-ordered and allocates nothing
+    TM_CUDA(cudaMemsetAsync(sc->counters, 0, tiles * sizeof(unsigned int), st),
+            "cudaMemsetAsync(counters)");
+    a.ws = sc->ws;
+    a.counters = sc->counters;
+  }
+  cudaError_t e;
+  if (cfg.kernel == TM_KERNEL_GEMV) {
+    e = launch_gemv(a, bf16, gemv_rows_tmpl(M), st);
+  } else {
+    CUtensorMap map;
+    s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_kblocks_per_stage(cfg.block_m), &map,
+                       &a.act_map_3d);
+    if (s != TM_OK) return s;
+    e = launch_tc(a, map, bf16, cfg.block_m, cfg.dq_warps, st);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "tm_gemm_w4a16_noalloc launch");
+  return TM_OK;
+}
