@@ -48,13 +48,16 @@ typedef enum { TM_F16 = 0, TM_BF16 = 1 } tm_dtype;
 
 /* Kernel families (tm_config.kernel). */
 enum {
-  TM_KERNEL_AUTO = 0, /* pick from the tuned table, else the built-in rule */
-  TM_KERNEL_GEMV = 1, /* CUDA-core split-K GEMV, M <= 8                    */
-  TM_KERNEL_TC = 2    /* tcgen05/TMEM/TMA kernel, any M                     */
+  TM_KERNEL_AUTO = 0,     /* pick from the tuned table, else the built-in rule */
+  TM_KERNEL_GEMV = 1,     /* CUDA-core split-K GEMV, M <= 8                    */
+  TM_KERNEL_TC = 2,       /* tcgen05/TMEM kernel, weights staged by TMA        */
+  TM_KERNEL_TC_DECODE = 3 /* tcgen05/TMEM kernel for small M (block_m 16..64),
+                             weights streamed from HBM straight into registers */
 };
 
-/* A kernel variant: family, rows of A per CTA tile (TC: 16..256, a
- * multiple of 16; GEMV: ignored) and the number of K splits (>= 1). */
+/* A kernel variant: family, rows of A per CTA tile (TC: 16, 32, 64, 128 or
+ * 256; TC_DECODE: 16, 32 or 64; GEMV: ignored) and the number of K splits
+ * (>= 1). */
 typedef struct {
   int32_t kernel;
   int32_t block_m;

@@ -45,6 +45,10 @@ def _variants(M):
                 if bm >= 128 and dq != 8 and sk == 3:
                     continue
                 out.append(dict(kernel="tc", block_m=bm, split_k=sk, dq_warps=dq))
+    for bm in (16, 32, 64):
+        for sk in (1, 3):
+            for dq in (4, 8, 16):
+                out.append(dict(kernel="tc_decode", block_m=bm, split_k=sk, dq_warps=dq))
     return out
 
 
@@ -214,6 +218,14 @@ def test_long_k_every_legal_variant():
                 torch.cuda.synchronize()
                 binding.poll_error()
                 assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, (bm, dq, sk)
+    for bm in (16, 32, 64):
+        for dq in (4, 8, 16):
+            for sk in (1, 2):
+                cfg = dict(kernel="tc_decode", block_m=bm, split_k=sk, dq_warps=dq)
+                C = gemm_poisoned(A, W, config=cfg)
+                torch.cuda.synchronize()
+                binding.poll_error()
+                assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, cfg
 
 
 def test_illegal_variants_are_rejected():
@@ -224,6 +236,10 @@ def test_illegal_variants_are_rejected():
     for bm, _ in sorted(ILLEGAL):
         with pytest.raises(binding.TmError) as e:
             binding.gemm(A, W, config=dict(kernel="tc", block_m=bm, dq_warps=16))
+        assert e.value.status == binding.TM_ERR_UNSUPPORTED
+    for bm, dq in ((128, 8), (16, 2), (48, 8)):
+        with pytest.raises(binding.TmError) as e:
+            binding.gemm(A, W, config=dict(kernel="tc_decode", block_m=bm, dq_warps=dq))
         assert e.value.status == binding.TM_ERR_UNSUPPORTED
 
 

@@ -283,6 +283,22 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
     }
     return true;
   }
+  if (c->kernel == TM_KERNEL_TC_DECODE) {
+    if (c->block_m != 16 && c->block_m != 32 && c->block_m != 64) {
+      if (why) *why = "TC_DECODE block_m must be 16, 32 or 64";
+      return false;
+    }
+    if (c->dq_warps == 0) c->dq_warps = 8;
+    if (!tc_decode_ok(c->block_m, c->dq_warps)) {
+      if (why) *why = "TC_DECODE dq_warps must be 4, 8 or 16";
+      return false;
+    }
+    if ((M + c->block_m - 1) / c->block_m > 65535) {
+      if (why) *why = "too many row tiles";
+      return false;
+    }
+    return true;
+  }
   if (why) *why = "unknown kernel family";
   return false;
 }
@@ -374,6 +390,12 @@ static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, con
   cudaError_t e;
   if (cfg.kernel == TM_KERNEL_GEMV) {
     e = launch_gemv(a, bf16, gemv_rows_tmpl(M), st);
+  } else if (cfg.kernel == TM_KERNEL_TC_DECODE) {
+    CUtensorMap map;
+    s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_decode_kblocks_per_stage(), &map,
+                       &a.act_map_3d);
+    if (s != TM_OK) return s;
+    e = launch_tc_decode(a, map, bf16, cfg.block_m, cfg.dq_warps, st);
   } else {
     CUtensorMap map;
     s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_kblocks_per_stage(cfg.block_m), &map,
@@ -671,6 +693,17 @@ static std::vector<tm_config> candidates(const tm_packed *W, int M) {
       if (normalize_config(W, M, &c, nullptr)) out.push_back(c);
     }
   }
+  for (int bm : {16, 32, 64}) {
+    if (bm > 16 && bm / 2 >= M) continue;
+    const int tiles = (W->N / 128) * ((M + bm - 1) / bm);
+    for (int s : splits) {
+      if (s > KB || (s > 1 && tiles * s > 8 * 152)) continue;
+      for (int dq : {4, 8, 16}) {
+        tm_config c{TM_KERNEL_TC_DECODE, bm, s, dq};
+        if (normalize_config(W, M, &c, nullptr)) out.push_back(c);
+      }
+    }
+  }
   const int bms[] = {16, 32, 64, 128, 256};
   for (int bm : bms) {
     if (bm > 16 && bm / 2 >= M) continue;        // at most one mostly empty tile size
@@ -862,6 +895,12 @@ extern "C" tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, vo
   cudaError_t e;
   if (cfg.kernel == TM_KERNEL_GEMV) {
     e = launch_gemv(a, bf16, gemv_rows_tmpl(M), st);
+  } else if (cfg.kernel == TM_KERNEL_TC_DECODE) {
+    CUtensorMap map;
+    s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_decode_kblocks_per_stage(), &map,
+                       &a.act_map_3d);
+    if (s != TM_OK) return s;
+    e = launch_tc_decode(a, map, bf16, cfg.block_m, cfg.dq_warps, st);
   } else {
     CUtensorMap map;
     s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_kblocks_per_stage(cfg.block_m), &map,

@@ -53,6 +53,14 @@ bool tc_variant_ok(int block_m, int dq_warps);
 cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                       int dq_warps, cudaStream_t st);
 
+// tcgen05 decode kernel (weights streamed into registers, not shared
+// memory): block_m in {16,32,64}, dq_warps in {4,8,16}.
+bool tc_decode_ok(int block_m, int dq_warps);
+int tc_decode_slots(int block_m, int dq_warps);
+int tc_decode_kblocks_per_stage();   // 64-K blocks per activation box
+cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
+                             int dq_warps, cudaStream_t st);
+
 // Bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t st);
 

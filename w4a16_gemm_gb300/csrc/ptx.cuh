@@ -85,10 +85,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns, volatile int *abort,
                                                   unsigned int *err_word, unsigned site = 0,
-                                                  unsigned step = 0) {
+                                                  unsigned step = 0,
+                                                  unsigned long long *spin = nullptr) {
+#ifdef TMW4_TRACE
+  // debug builds: spin[0] += calls, spin[1] += polls of the barrier
+  if (spin != nullptr) atomicAdd(spin, 1ull);
+#else
+  (void)spin;
+#endif
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
+#ifdef TMW4_TRACE
+    if (spin != nullptr) atomicAdd(spin + 1, 1ull);
+#endif
     if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
     {
       if (abort != nullptr && *abort) return false;
@@ -116,10 +126,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 // lanes.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                                volatile int *abort, unsigned int *err_word,
-                                               unsigned site, unsigned step) {
+                                               unsigned site, unsigned step,
+                                               unsigned long long *spin = nullptr) {
   const int lane = threadIdx.x & 31;
   bool ok = true;
-  if (lane == 0) ok = mbar_wait_bounded(bar, parity, limit_ns, abort, err_word, site, step);
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, limit_ns, abort, err_word, site, step, spin);
   ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
   if (ok) (void)mbar_try_wait(bar, parity);
   return ok;

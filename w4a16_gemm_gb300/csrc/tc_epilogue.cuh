@@ -1,0 +1,104 @@
+// tc_epilogue.cuh -- the output stage shared by the tcgen05 kernels: read the
+// fp32 accumulator from TMEM, round once to the 16-bit output type, or write
+// split-K partials and let the last CTA of the tile sum them in split order.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace tmw4 {
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t f32_to_16(float x) {
+  if constexpr (BF16) {
+    __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&b);
+  } else {
+    __half h = __float2half_rn(x);
+    return *reinterpret_cast<uint16_t *>(&h);
+  }
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Called by all DQ_WG * 128 epilogue threads of the CTA.  Thread (wg, lane
+// quarter, lane) owns weight column n = n0 + r with r = 32 * quarter + lane
+// (TMEM lane r); D's columns are the rows m0.. of C.  The result is the sum,
+// in a fixed order, of `nacc` accumulators `acc_stride` TMEM columns apart
+// (nacc = 0: this CTA had no K blocks, the result is zero).  `ok` must be
+// warp-uniform.
+template <bool BF16, int BLOCK_M, int DQ_WG>
+__device__ __forceinline__ void tc_epilogue(const GemmArgs &p, uint32_t d_addr, int wg, int dw,
+                                            int lane, int r, int n0, int m0, int split, bool ok,
+                                            int nacc, uint32_t acc_stride, int *last_flag) {
+  constexpr int DQ_THREADS = 128 * DQ_WG;
+  const int N = p.N, M = p.M;
+  const int n = n0 + r;
+  const bool direct = (p.splits == 1);
+  if (ok) {
+    // warpgroups take alternate 16-column chunks of D
+    for (int c0 = wg * 16; c0 < BLOCK_M; c0 += 16 * DQ_WG) {
+      if (m0 + c0 >= M) break;  // warp-uniform
+      float x16[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x16[j] = 0.f;
+      for (int a = 0; a < nacc; ++a) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld_16(d_addr + a * acc_stride + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x16[j] = a == 0 ? __uint_as_float(v[j]) : x16[j] + __uint_as_float(v[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = m0 + c0 + j;
+        if (m < M) {
+          const float x = x16[j];
+          if (direct)
+            p.C[static_cast<size_t>(m) * N + n] = f32_to_16<BF16>(x);
+          else
+            p.ws[(static_cast<size_t>(split) * M + m) * N + n] = x;
+        }
+      }
+    }
+  }
+  if (direct) return;
+  __threadfence();
+  named_bar_sync(1, DQ_THREADS);
+  unsigned int *ctr = p.counters + (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x);
+  if (dw == 0 && lane == 0) {
+    const unsigned prev = atomicAdd(ctr, 1u);
+    *last_flag = (prev == static_cast<unsigned>(p.splits - 1));
+  }
+  named_bar_sync(1, DQ_THREADS);
+  if (!*last_flag) return;
+  __threadfence();
+  // fixed split order per element; 8 independent loads in flight
+  const size_t split_stride = static_cast<size_t>(M) * N;
+  for (int c = wg; c < BLOCK_M; c += DQ_WG) {
+    const int m = m0 + c;
+    if (m >= M) break;
+    const float *src = p.ws + static_cast<size_t>(m) * N + n;
+    float acc = 0.f;
+    int sp = 0;
+    for (; sp + 8 <= p.splits; sp += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (sp + j) * split_stride);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc += v[j];
+    }
+    for (; sp < p.splits; ++sp) acc += __ldcg(src + sp * split_stride);
+    p.C[static_cast<size_t>(m) * N + n] = f32_to_16<BF16>(acc);
+  }
+  if (dw == 0 && lane == 0) *ctr = 0u;
+}
+
+}  // namespace tmw4

@@ -33,6 +33,7 @@
 #include "dequant.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tc_epilogue.cuh"
 
 namespace tmw4 {
 
@@ -88,35 +89,8 @@ __host__ __device__ constexpr size_t smem_bytes_for(int block_m) {
          512 /* barriers and flags */;
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint16_t f32_to_16(float x) {
-  if constexpr (BF16) {
-    __nv_bfloat16 b = __float2bfloat16_rn(x);
-    return *reinterpret_cast<uint16_t *>(&b);
-  } else {
-    __half h = __float2half_rn(x);
-    return *reinterpret_cast<uint16_t *>(&h);
-  }
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 }  // namespace
 
-#ifdef TMW4_TRACE
-#define TMW4_STAMP(slot, idx)                                                              \
-  do {                                                                                     \
-    if (p.trace != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&     \
-        (idx) < 256)                                                                       \
-      p.trace[(slot) * 256 + (idx)] = clock64();                                           \
-  } while (0)
-#else
-#define TMW4_STAMP(slot, idx) \
-  do {                        \
-  } while (0)
-#endif
 
 // DQ_WG dequant warpgroups; warpgroup g dequantizes the shared-memory stages
 // j with j % DQ_WG == g, so DQ_WG stages are in flight in the ALUs at once.
@@ -387,66 +361,8 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
       ok = mbar_wait_warp(accum_bar, 0, p.limit_ns, abort_flag, p.err, SITE_EPI_ACCUM, 0);
     if (dw == 0 && lane == 0) TMW4_STAMP(6, 0);
     tc_fence_after();
-    const int n = n0 + r;
-    const bool direct = (p.splits == 1);
-    if (ok) {
-      // columns of D are rows m of C; warpgroups take alternate 16-column chunks
-      for (int c0 = wg * 16; c0 < BLOCK_M; c0 += 16 * DQ_WG) {
-        if (m0 + c0 >= M) break;  // warp-uniform
-        uint32_t v[16];
-        __syncwarp();
-        if (nkb > 0) {
-          tmem_ld_16(tmem + lane_addr + c0, v);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = m0 + c0 + j;
-          if (m < M) {
-            const float x = __uint_as_float(v[j]);
-            if (direct)
-              p.C[static_cast<size_t>(m) * N + n] = f32_to_16<BF16>(x);
-            else
-              p.ws[(static_cast<size_t>(split) * M + m) * N + n] = x;
-          }
-        }
-      }
-    }
-    if (!direct) {
-      __threadfence();
-      named_bar_sync(1, DQ_THREADS);
-      unsigned int *ctr = p.counters + (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x);
-      if (dw == 0 && lane == 0) {
-        const unsigned prev = atomicAdd(ctr, 1u);
-        *last_flag = (prev == static_cast<unsigned>(p.splits - 1));
-      }
-      named_bar_sync(1, DQ_THREADS);
-      if (*last_flag) {
-        __threadfence();
-        // fixed split order per element; 8 independent loads in flight
-        const size_t split_stride = static_cast<size_t>(M) * N;
-        for (int c = wg; c < BLOCK_M; c += DQ_WG) {
-          const int m = m0 + c;
-          if (m >= M) break;
-          const float *src = p.ws + static_cast<size_t>(m) * N + n;
-          float acc = 0.f;
-          int sp = 0;
-          for (; sp + 8 <= p.splits; sp += 8) {
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (sp + j) * split_stride);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc += v[j];
-          }
-          for (; sp < p.splits; ++sp) acc += __ldcg(src + sp * split_stride);
-          p.C[static_cast<size_t>(m) * N + n] = f32_to_16<BF16>(acc);
-        }
-        if (dw == 0 && lane == 0) *ctr = 0u;
-      }
-    }
+    tc_epilogue<BF16, BLOCK_M, DQ_WG>(p, tmem + lane_addr, wg, dw, lane, r, n0, m0, split, ok,
+                                      nkb > 0 ? 1 : 0, 0u, last_flag);
   }
 
   tc_fence_before();

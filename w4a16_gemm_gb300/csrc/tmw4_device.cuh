@@ -60,3 +60,18 @@ struct Magic {
 };
 
 }  // namespace tmw4
+
+// Debug timeline: with TMW4_TRACE defined, kernels record clock64() stamps of
+// pipeline events of CTA (0,0,0) into GemmArgs::trace[slot * 256 + idx].
+#ifdef TMW4_TRACE
+#define TMW4_STAMP(slot, idx)                                                              \
+  do {                                                                                     \
+    if (p.trace != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&     \
+        (idx) < 256)                                                                       \
+      p.trace[(slot) * 256 + (idx)] = clock64();                                           \
+  } while (0)
+#else
+#define TMW4_STAMP(slot, idx) \
+  do {                        \
+  } while (0)
+#endif
