@@ -290,9 +290,10 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
     }
     if (c->dq_warps == 0) c->dq_warps = 8;
     if (!tc_decode_ok(c->block_m, c->dq_warps)) {
-      if (why) *why = "TC_DECODE dq_warps must be 4, 8 or 16";
+      if (why) *why = "TC_DECODE dq_warps must be 4, 8 or 12 (12 only with block_m <= 32)";
       return false;
     }
+    c->split_k = 1;   // stream-K: the grid divides the work itself
     if ((M + c->block_m - 1) / c->block_m > 65535) {
       if (why) *why = "too many row tiles";
       return false;
@@ -344,15 +345,59 @@ extern "C" tm_status tm_debug_set_trace(void *p) {
   g_trace = static_cast<long long *>(p);
   return TM_OK;
 }
+static __global__ void debug_marker_kernel(long long *out, int idx) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (threadIdx.x == 0) out[idx] = static_cast<long long>(t);
+}
+// debug builds only: a one-thread kernel that records %globaltimer at out[idx]
+extern "C" tm_status tm_debug_marker(void *out, int idx, void *stream) {
+  debug_marker_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<long long *>(out), idx);
+  return cudaGetLastError() == cudaSuccess ? TM_OK : TM_ERR_CUDA;
+}
 #endif
 
 // ------------------------------------------------------------ GEMM launch
+// K split and scratch of a launch: GEMV and TC split K evenly (TC on stage
+// boundaries; trailing splits that would be empty are dropped); TC_DECODE
+// divides (tile, stage) units over a persistent grid and needs partial slots
+// only where the grid cuts a tile.
+static void plan_work(const tm_packed *W, int M, const tm_config &cfg, GemmArgs *a, int *dec_grid,
+                      size_t *ws_floats, size_t *n_counters) {
+  const int KB = W->K / 64;
+  *ws_floats = 0;
+  *n_counters = 0;
+  if (cfg.kernel == TM_KERNEL_TC_DECODE) {
+    long long tiles = 0;
+    int slots = 1;
+    tc_decode_plan(M, W->N, W->K, cfg.block_m, sm_count(W->device), dec_grid, &tiles, &slots);
+    a->kb_per_split = KB;
+    a->splits = 1;
+    a->ws_slots = slots;
+    if (slots > 1) {
+      *ws_floats = static_cast<size_t>(tiles) * slots * 128 * cfg.block_m;
+      *n_counters = static_cast<size_t>(tiles);
+    }
+    return;
+  }
+  const int gran = cfg.kernel == TM_KERNEL_TC ? tc_kblocks_per_stage(cfg.block_m) : 1;
+  int per = (KB + cfg.split_k - 1) / cfg.split_k;
+  per = (per + gran - 1) / gran * gran;
+  a->kb_per_split = per;
+  a->splits = (KB + per - 1) / per;
+  if (a->splits > 1) {
+    *ws_floats = static_cast<size_t>(a->splits) * M * W->N;
+    *n_counters = cfg.kernel == TM_KERNEL_GEMV
+                      ? static_cast<size_t>(W->N / 64)
+                      : static_cast<size_t>(W->N / 128) * ((M + cfg.block_m - 1) / cfg.block_m);
+  }
+}
+
 static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, const tm_config &cfg,
                           cudaStream_t st) {
   unsigned int *err = nullptr;
   tm_status s = error_word(W->device, &err);
   if (s != TM_OK) return s;
-  const int KB = W->K / 64;
   GemmArgs a{};
   a.qw = W->qw;
   a.scales = W->scales;
@@ -364,25 +409,17 @@ static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, con
   a.N = W->N;
   a.K = W->K;
   a.group = W->group;
-  // the TC kernel moves whole stages of `gran` 64-K blocks: split on stage
-  // boundaries; trailing splits that would be empty are dropped
-  const int gran = cfg.kernel == TM_KERNEL_TC ? tc_kblocks_per_stage(cfg.block_m) : 1;
-  int per = (KB + cfg.split_k - 1) / cfg.split_k;
-  per = (per + gran - 1) / gran * gran;
-  a.kb_per_split = per;
-  a.splits = (KB + per - 1) / per;
+  int dec_grid = 0;
+  size_t ws_floats = 0, n_counters = 0;
+  plan_work(W, M, cfg, &a, &dec_grid, &ws_floats, &n_counters);
   a.limit_ns = wait_limit_ns();
 #ifdef TMW4_TRACE
   a.trace = g_trace;
 #endif
   const bool bf16 = W->dtype == TM_BF16;
-  if (a.splits > 1) {
+  if (ws_floats > 0) {
     Workspace *ws = nullptr;
-    const size_t ws_bytes = sizeof(float) * static_cast<size_t>(a.splits) * M * W->N;
-    const size_t tiles = cfg.kernel == TM_KERNEL_GEMV
-                             ? static_cast<size_t>(W->N / 64)
-                             : static_cast<size_t>(W->N / 128) * ((M + cfg.block_m - 1) / cfg.block_m);
-    s = get_workspace(W->device, st, ws_bytes, tiles, &ws);
+    s = get_workspace(W->device, st, sizeof(float) * ws_floats, n_counters, &ws);
     if (s != TM_OK) return s;
     a.ws = ws->ws;
     a.counters = ws->counters;
@@ -395,7 +432,7 @@ static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, con
     s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_decode_kblocks_per_stage(), &map,
                        &a.act_map_3d);
     if (s != TM_OK) return s;
-    e = launch_tc_decode(a, map, bf16, cfg.block_m, cfg.dq_warps, st);
+    e = launch_tc_decode(a, map, bf16, cfg.block_m, cfg.dq_warps, dec_grid, st);
   } else {
     CUtensorMap map;
     s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_kblocks_per_stage(cfg.block_m), &map,
@@ -696,12 +733,10 @@ static std::vector<tm_config> candidates(const tm_packed *W, int M) {
   for (int bm : {16, 32, 64}) {
     if (bm > 16 && bm / 2 >= M) continue;
     const int tiles = (W->N / 128) * ((M + bm - 1) / bm);
-    for (int s : splits) {
-      if (s > KB || (s > 1 && tiles * s > 8 * 152)) continue;
-      for (int dq : {4, 8, 16}) {
-        tm_config c{TM_KERNEL_TC_DECODE, bm, s, dq};
-        if (normalize_config(W, M, &c, nullptr)) out.push_back(c);
-      }
+    (void)tiles;
+    for (int dq : {4, 8, 12}) {
+      tm_config c{TM_KERNEL_TC_DECODE, bm, 1, dq};
+      if (normalize_config(W, M, &c, nullptr)) out.push_back(c);
     }
   }
   const int bms[] = {16, 32, 64, 128, 256};
@@ -855,7 +890,6 @@ extern "C" tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, vo
   s = static_scratch(W->device, &sc);
   if (s != TM_OK) return s;
   const tm_config cfg = select_config(W, M, W->device);
-  const int KB = W->K / 64;
   GemmArgs a{};
   a.qw = W->qw;
   a.scales = W->scales;
@@ -867,18 +901,12 @@ extern "C" tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, vo
   a.N = W->N;
   a.K = W->K;
   a.group = W->group;
-  const int gran = cfg.kernel == TM_KERNEL_TC ? tc_kblocks_per_stage(cfg.block_m) : 1;
-  int per = (KB + cfg.split_k - 1) / cfg.split_k;
-  per = (per + gran - 1) / gran * gran;
-  a.kb_per_split = per;
-  a.splits = (KB + per - 1) / per;
+  int dec_grid = 0;
+  size_t ws_floats = 0, tiles = 0;
+  plan_work(W, M, cfg, &a, &dec_grid, &ws_floats, &tiles);
   a.limit_ns = wait_limit_ns();
   const bool bf16 = W->dtype == TM_BF16;
-  if (a.splits > 1) {
-    const size_t ws_floats = static_cast<size_t>(a.splits) * M * W->N;
-    const size_t tiles = cfg.kernel == TM_KERNEL_GEMV
-                             ? static_cast<size_t>(W->N / 64)
-                             : static_cast<size_t>(W->N / 128) * ((M + cfg.block_m - 1) / cfg.block_m);
+  if (ws_floats > 0) {
     if (ws_floats > kStaticWsFloats || tiles > kStaticCounters)
       return fail(TM_ERR_UNSUPPORTED,
                   "tm_gemm_w4a16_noalloc: this shape needs %zu bytes of split-K scratch and %zu "
@@ -900,7 +928,7 @@ extern "C" tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, vo
     s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_decode_kblocks_per_stage(), &map,
                        &a.act_map_3d);
     if (s != TM_OK) return s;
-    e = launch_tc_decode(a, map, bf16, cfg.block_m, cfg.dq_warps, st);
+    e = launch_tc_decode(a, map, bf16, cfg.block_m, cfg.dq_warps, dec_grid, st);
   } else {
     CUtensorMap map;
     s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_kblocks_per_stage(cfg.block_m), &map,

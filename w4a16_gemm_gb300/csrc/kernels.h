@@ -32,6 +32,7 @@ struct GemmArgs {
   int splits;
   int kb_per_split;  // 64-wide K blocks per split (a multiple of the TC stage's k-blocks)
   int act_map_3d;    // TC: the activation tensor map is 3-D (64 x M x K/64)
+  int ws_slots;      // TC_DECODE: fp32 partial slots per tile in ws (stream-K contributors)
   unsigned long long limit_ns;
   // Debug builds compiled with -DTMW4_TRACE record per-stage SM cycle
   // stamps of CTA (0,0,0) here ([8][256] slots); nullptr otherwise.
@@ -53,13 +54,16 @@ bool tc_variant_ok(int block_m, int dq_warps);
 cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                       int dq_warps, cudaStream_t st);
 
-// tcgen05 decode kernel (weights streamed into registers, not shared
-// memory): block_m in {16,32,64}, dq_warps in {4,8,16}.
+// tcgen05 decode kernel: persistent, stream-K; block_m in {16,32,64},
+// dq_warps in {4,8,12} (see tc_decode.cu).  tc_decode_plan gives the grid,
+// the tile count (split-K counters) and the partial slots per tile.
 bool tc_decode_ok(int block_m, int dq_warps);
 int tc_decode_slots(int block_m, int dq_warps);
 int tc_decode_kblocks_per_stage();   // 64-K blocks per activation box
+void tc_decode_plan(int M, int N, int K, int block_m, int sms, int *grid, long long *tiles,
+                    int *ws_slots);
 cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
-                             int dq_warps, cudaStream_t st);
+                             int dq_warps, int grid, cudaStream_t st);
 
 // Bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t st);

@@ -136,6 +136,20 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, u
   return ok;
 }
 
+// Warp-wide bounded wait in which every lane polls the barrier itself: one
+// poll and one vote when the phase is already complete (the common case in
+// a pipeline that runs ahead), the bounded loop otherwise.  The result is
+// warp-uniform.
+__device__ __forceinline__ bool mbar_wait_all(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int *abort, unsigned int *err_word,
+                                              unsigned site, unsigned step,
+                                              unsigned long long *spin = nullptr) {
+  const bool done = mbar_try_wait(bar, parity);
+  if (__all_sync(0xFFFFFFFFu, done)) return true;
+  const bool ok = done || mbar_wait_bounded(bar, parity, limit_ns, abort, err_word, site, step, spin);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
                                              uint64_t *bar) {

@@ -1,14 +1,13 @@
-// tc_decode.cu -- W4A16 GEMM for small row counts (decode) on the tcgen05
-// tensor cores.
+// tc_decode.cu -- W4A16 GEMM for small row counts (decode): a persistent,
+// stream-K tcgen05 kernel.
 //
 // With few rows of activations there is little work per weight byte, so the
-// kernel must keep HBM busy rather than the tensor pipe.  Three measured
-// GB300 costs shape it:
+// kernel must keep HBM busy rather than the tensor pipe.  Measured GB300 costs
+// shape it:
 //   * one thread can issue a 64-K block (4 MMAs of M=128, N<=64, K=16 plus
 //     a commit) only every ~250-400 cycles, whatever N is, while issuers in
 //     different warps proceed in parallel.  Each dequant warpgroup therefore
-//     has its own MMA-issuing warp and its own fp32 accumulator in TMEM; the
-//     epilogue adds the accumulators in a fixed order;
+//     has its own MMA-issuing warp and its own fp32 accumulators in TMEM;
 //   * a bulk copy costs its issuing thread hundreds of cycles whatever its
 //     size, so weights move in stages of WKB = 4 packed blocks (16 KB, one
 //     copy, plus one copy each for the stage's scales and zeros) and
@@ -16,8 +15,15 @@
 //   * per-thread 128-bit global loads of the weights crowd the SM's
 //     memory-instruction queue that tcgen05 and mbarrier instructions also
 //     use, so weights go through shared memory, and a weight stage is
-//     released as soon as its dequant warps have read it, whatever the MMAs
-//     are doing.
+//     released as soon as its dequant warps have read it;
+//   * a weight stage takes ~1.5-2 us from copy issue to arrival under load,
+//     so each warpgroup keeps several stages in flight: one CTA per SM with a
+//     deep ring;
+//   * with one CTA per SM, whole-tile CTAs leave SMs idle (e.g. 224 tiles on
+//     152 SMs), so the work is split stream-K style: the (tile, 16 KB stage)
+//     units of the problem are divided evenly over a persistent grid, a CTA
+//     runs its units in order, and a tile cut between CTAs is finished by the
+//     last one to arrive, which adds the fp32 partials in a fixed order.
 // The packed block is already in the order the consumer needs (the pages'
 // fragment-order repack, "Efficient Mixed-Precision Large Language Model
 // Inference with TurboMind", pith.science review, Figures 6/7): the thread that
@@ -27,17 +33,23 @@
 //   warp 0          weight producer (stage ring of WST)
 //   warp 1          TMEM allocator; activation producer
 //   warps 2..       one MMA-issuing warp per dequant warpgroup
-//   then            DQ_WG dequant warpgroups; stage j goes to warpgroup
-//                   j % DQ_WG: read each block, release the stage after its
-//                   last block, dequantize exactly (w = T(s*(q-z))),
-//                   tcgen05.st into one of the warpgroup's TMEM A slots; then
-//                   the epilogue
+//   next 4 warps    epilogue warpgroup: per tile segment, waits for the
+//                   accumulators, adds them, writes C or an fp32 partial
+//   then            DQ_WG dequant warpgroups; the CTA's j-th stage goes to
+//                   warpgroup j % DQ_WG, which dequantizes exactly
+//                   (w = T(s*(q-z))) two blocks at a time into its TMEM A slots
+//
+// Each warpgroup has two accumulators and alternates between them from one
+// tile segment to the next, so the MMAs of a segment overlap the epilogue of
+// the previous one.
 //
 // Parity waits stay at most one phase ahead (no aliasing) because every ring
 // slot always serves the same warpgroup (WST % DQ_WG == 0 for the weight
-// ring; private activation stages and TMEM slots per warpgroup), whose
-// waiters have seen the slot's previous phase; copies may land out of order
-// across slots.
+// ring; private activation stages, TMEM slots and accumulators per
+// warpgroup), whose waiters have seen the slot's previous phase, and because
+// one thread's tcgen05 commits complete in issue order; copies may land out
+// of order across slots.
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 
@@ -48,8 +60,9 @@
 
 namespace tmw4 {
 
-// Debug builds count barrier polls per wait site into the trace buffer.
-#ifdef TMW4_TRACE
+// Debug builds with TMW4_SPIN_COUNT count barrier polls per wait site into
+// the trace buffer (global atomics: they slow the kernel down).
+#if defined(TMW4_TRACE) && defined(TMW4_SPIN_COUNT)
 #define TMW4_SPIN(site)                                                                       \
   (p.trace != nullptr ? reinterpret_cast<unsigned long long *>(p.trace + 15 * 256) + 2 * (site) \
                       : nullptr)
@@ -63,54 +76,102 @@ constexpr int DBLOCK_N = 128;
 constexpr int DBLOCK_K = 64;
 constexpr int DSLOT_COLS = DBLOCK_K / 2;   // 32 TMEM columns of packed pairs per block
 constexpr int WKB = 4;                     // 64-K blocks per weight / activation stage
-constexpr int WST = 4;                     // weight ring depth (divisible by 1, 2, 4)
 constexpr int MAX_G = WKB;                 // groups a stage can touch (group >= 64)
 constexpr int W_SC_OFF = WKB * BLOCK_BYTES;                       // scales of the stage's groups
 constexpr int W_ZP_OFF = W_SC_OFF + MAX_G * 2 * DBLOCK_N;         // packed zeros
 constexpr int W_STAGE_BYTES = W_ZP_OFF + MAX_G * (DBLOCK_N / 2);  // 17664, a multiple of 16
+constexpr int TMEM_COLS = 512;             // one CTA per SM
+constexpr long long SMEM_BUDGET = 220 * 1024;
 
-// TMEM: DQ_WG accumulators of dec_dcols columns, then DQ_WG * TSW A slots.
-// Up to two warpgroups share 256 columns so that two CTAs fit on an SM.
-__host__ __device__ constexpr int dec_tmem_cols(int dq_wg) { return dq_wg <= 2 ? 256 : 512; }
 __host__ __device__ constexpr int dec_dcols(int block_m) { return block_m < 32 ? 32 : block_m; }
-// TMEM A slots per warpgroup
+// TMEM columns per warpgroup: two accumulators, then the A slots (at most 8)
+__host__ __device__ constexpr int dec_wg_cols(int dq_wg) { return (TMEM_COLS / dq_wg) / 32 * 32; }
+__host__ __device__ constexpr int dec_tsw_fit(int block_m, int dq_wg) {
+  return (dec_wg_cols(dq_wg) - 2 * dec_dcols(block_m)) / DSLOT_COLS;
+}
+// a power of two (ring indices are masks and shifts), at most 8
 __host__ __device__ constexpr int dec_tsw(int block_m, int dq_wg) {
-  return (dec_tmem_cols(dq_wg) / dq_wg - dec_dcols(block_m)) / DSLOT_COLS;
+  return dec_tsw_fit(block_m, dq_wg) >= 8   ? 8
+         : dec_tsw_fit(block_m, dq_wg) >= 4 ? 4
+         : dec_tsw_fit(block_m, dq_wg) >= 2 ? 2
+                                            : 1;
 }
-// activation stages (WKB tiles each) per warpgroup: double-buffered when the
-// tiles are small, single otherwise, so that two CTAs fit on an SM
+__host__ __device__ constexpr long long dec_a_stage(int block_m) {
+  return static_cast<long long>(WKB) * block_m * DBLOCK_K * 2;
+}
+// activation stages per warpgroup: double-buffered when it leaves room for a
+// weight ring of six stages
 __host__ __device__ constexpr int dec_asw(int block_m, int dq_wg) {
-  return block_m * dq_wg <= 32 ? 2 : 1;
+  return 2 * dq_wg * dec_a_stage(block_m) + 6 * W_STAGE_BYTES <= SMEM_BUDGET ? 2 : 1;
 }
-__host__ __device__ constexpr int dec_threads(int dq_wg) { return 64 + 32 * dq_wg + 128 * dq_wg; }
-__host__ __device__ constexpr int dec_a_bytes(int block_m) { return block_m * DBLOCK_K * 2; }
-__host__ __device__ constexpr size_t dec_smem_bytes(int block_m, int dq_wg) {
-  return 1024 +
-         static_cast<size_t>(dq_wg * dec_asw(block_m, dq_wg)) * WKB * dec_a_bytes(block_m) +
-         static_cast<size_t>(WST) * W_STAGE_BYTES + 1024;
+// weight ring depth: the deepest multiple of dq_wg (at most 12) that fits
+__host__ __device__ constexpr int dec_wst_fit(int block_m, int dq_wg) {
+  return static_cast<int>(
+      ((SMEM_BUDGET - dq_wg * dec_asw(block_m, dq_wg) * dec_a_stage(block_m)) / W_STAGE_BYTES) /
+      dq_wg * dq_wg);
 }
+__host__ __device__ constexpr int dec_wst(int block_m, int dq_wg) {
+  return dec_wst_fit(block_m, dq_wg) > 12 ? 12 / dq_wg * dq_wg : dec_wst_fit(block_m, dq_wg);
+}
+__host__ __device__ constexpr int dec_threads(int dq_wg) { return 64 + 32 * dq_wg + 128 + 128 * dq_wg; }
+__host__ __device__ constexpr long long dec_smem_bytes(int block_m, int dq_wg) {
+  return 1024 + dq_wg * dec_asw(block_m, dq_wg) * dec_a_stage(block_m) +
+         static_cast<long long>(dec_wst(block_m, dq_wg)) * W_STAGE_BYTES + 1024;
+}
+
+// Stream-K partition: CTA c owns units [unit_begin(c), unit_begin(c + 1)).
+__host__ __device__ __forceinline__ long long unit_begin(long long c, long long U, long long G) {
+  return c * U / G;
+}
+// The CTA whose range holds unit u.
+__host__ __device__ __forceinline__ int cta_of_unit(long long u, long long U, long long G) {
+  long long c = u * G / U;
+  while (c + 1 < G && unit_begin(c + 1, U, G) <= u) ++c;
+  while (c > 0 && unit_begin(c, U, G) > u) --c;
+  return static_cast<int>(c);
+}
+
+// Position of a unit: tile t (= mt * NT + nt) and stage s of that tile.
+// Loops step it forward instead of dividing a 64-bit unit index: a 64-bit
+// division by a runtime value costs a few hundred cycles per loop trip.
+struct UnitPos {
+  int t, s, mt, nt;
+  __device__ __forceinline__ void step(int n, int S, int NT) {
+    s += n;
+    while (s >= S) {
+      s -= S;
+      ++t;
+      if (++nt == NT) {
+        nt = 0;
+        ++mt;
+      }
+    }
+  }
+};
 
 }  // namespace
 
 template <bool BF16, int BLOCK_M, int DQ_WG>
-__global__ void __launch_bounds__(dec_threads(DQ_WG), DQ_WG <= 2 ? 2 : 1)
+__global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
   constexpr int TSW = dec_tsw(BLOCK_M, DQ_WG);
   constexpr int TSLOTS = DQ_WG * TSW;
   constexpr int ASW = dec_asw(BLOCK_M, DQ_WG);
   constexpr int ASTAGES = DQ_WG * ASW;
-  constexpr int TCOLS = dec_tmem_cols(DQ_WG);
-  constexpr int A_KB = dec_a_bytes(BLOCK_M);
-  constexpr int A_STAGE = WKB * A_KB;
+  constexpr int WST = dec_wst(BLOCK_M, DQ_WG);
+  constexpr int A_KB = BLOCK_M * DBLOCK_K * 2;
+  constexpr int A_STAGE = static_cast<int>(dec_a_stage(BLOCK_M));
   constexpr int DCOLS = dec_dcols(BLOCK_M);
-  constexpr int A_COL0 = DQ_WG * DCOLS;
-  constexpr int FIRST_DQ_WARP = 2 + DQ_WG;
+  constexpr int WG_COLS = dec_wg_cols(DQ_WG);
+  constexpr int ISSUE_WARP0 = 2;
+  constexpr int EPI_WARP0 = 2 + DQ_WG;
+  constexpr int DQ_WARP0 = EPI_WARP0 + 4;
   constexpr uint32_t IDESC = idesc_f16(BF16 ? 1u : 0u, 128u, static_cast<uint32_t>(BLOCK_M));
   static_assert(BLOCK_M == 16 || BLOCK_M == 32 || BLOCK_M == 64, "decode tiles");
-  static_assert(TSW >= 2, "each warpgroup needs two TMEM A slots to overlap dequant and MMA");
-  static_assert(A_COL0 + TSLOTS * DSLOT_COLS <= TCOLS, "TMEM budget");
-  static_assert(WST % DQ_WG == 0, "weight ring: a stage must always go to the same warpgroup");
+  static_assert(TSW >= 2, "a warpgroup needs two TMEM A slots (one block pair)");
+  static_assert(WST >= 2 * DQ_WG && WST % DQ_WG == 0, "weight ring");
   static_assert(A_KB % 1024 == 0, "swizzle atoms");
+  static_assert(dec_smem_bytes(BLOCK_M, DQ_WG) <= 227 * 1024, "shared memory");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -123,26 +184,36 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), DQ_WG <= 2 ? 2 : 1)
   uint64_t *aempty_bar = afull_bar + ASTAGES;           // MMAs reading it retired
   uint64_t *tfull_bar = aempty_bar + ASTAGES;           // dequantized block in TMEM
   uint64_t *kfree_bar = tfull_bar + TSLOTS;             // MMAs of the slot's block retired
-  uint64_t *accum_bar = kfree_bar + TSLOTS;             // every issuer's MMAs retired
-  uint64_t *drain_bar = accum_bar + 1;                  // [DQ_WG] abort path
+  uint64_t *accfull_bar = kfree_bar + TSLOTS;           // [DQ_WG][2] segment's MMAs retired
+  uint64_t *accempty_bar = accfull_bar + 2 * DQ_WG;     // [DQ_WG][2] epilogue has read it
+  uint64_t *drain_bar = accempty_bar + 2 * DQ_WG;       // [DQ_WG] abort path
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + DQ_WG);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   int *last_flag = reinterpret_cast<int *>(tmem_holder + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = blockIdx.x;
-  const int n0 = nt * DBLOCK_N;
-  const int m0 = blockIdx.y * BLOCK_M;
-  const int split = blockIdx.z;
   const int KB = p.K / DBLOCK_K;
+  const int S = (KB + WKB - 1) / WKB;                   // stages per tile
+  const int NT = p.N / DBLOCK_N;
+  const long long T = static_cast<long long>(NT) * ((p.M + BLOCK_M - 1) / BLOCK_M);
+  const long long U = T * S;
+  const long long G = gridDim.x;
+  const long long u0 = unit_begin(blockIdx.x, U, G);
+  const int nloc = static_cast<int>(unit_begin(blockIdx.x + 1, U, G) - u0);
   const int G_rows = p.K / p.group;
-  const int kb0 = split * p.kb_per_split;
-  const int nkb = max(0, min(KB, kb0 + p.kb_per_split) - kb0);
-  const int nst = (nkb + WKB - 1) / WKB;                // stages of this CTA
-  const int nacc = min(DQ_WG, nst);                     // warpgroups that own a stage
+  const int gshift = p.group == 128 ? 1 : 0;            // 64-K blocks per group: 1 << gshift
+  UnitPos pos0;                                         // this CTA's first unit
+  pos0.t = static_cast<int>(u0 / S);
+  pos0.s = static_cast<int>(u0 - static_cast<long long>(pos0.t) * S);
+  pos0.mt = pos0.t / NT;
+  pos0.nt = pos0.t - pos0.mt * NT;
 
   if (threadIdx.x == 0) {
     TMW4_STAMP(7, 1);
+#ifdef TMW4_TRACE
+    if (p.trace != nullptr && blockIdx.x < 256)
+      p.trace[13 * 256 + blockIdx.x] = static_cast<long long>(globaltimer_ns());
+#endif
     for (int s = 0; s < WST; ++s) {
       mbar_init(wfull_bar + s, 1);
       mbar_init(wempty_bar + s, 4);
@@ -155,7 +226,10 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), DQ_WG <= 2 ? 2 : 1)
       mbar_init(tfull_bar + s, 4);
       mbar_init(kfree_bar + s, 1);
     }
-    mbar_init(accum_bar, nacc > 0 ? nacc : 1);
+    for (int s = 0; s < 2 * DQ_WG; ++s) {
+      mbar_init(accfull_bar + s, 1);
+      mbar_init(accempty_bar + s, 4);
+    }
     for (int g = 0; g < DQ_WG; ++g) mbar_init(drain_bar + g, 1);
     *abort_flag = 0;
     *last_flag = 0;
@@ -163,7 +237,7 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), DQ_WG <= 2 ? 2 : 1)
     prefetch_tensormap(&tmap_a);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, TCOLS);
+    tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -176,15 +250,17 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), DQ_WG <= 2 ? 2 : 1)
     // --------------------------------------------------- weight producer
     if (lane == 0) {
       int issued = 0;
-      for (int j = 0; j < nst; ++j) {
+      UnitPos pos = pos0;
+      for (int j = 0; j < nloc; ++j, pos.step(1, S, NT)) {
         const int s = j % WST;
         if (j >= WST && !mbar_wait_bounded(wempty_bar + s, ((j / WST) & 1) ^ 1u, p.limit_ns,
                                            abort_flag, p.err, SITE_PRODUCER_EMPTY, j, TMW4_SPIN(0)))
           break;
-        const int kbf = kb0 + j * WKB;
-        const int nb = min(WKB, nkb - j * WKB);
-        const int gf = (kbf * DBLOCK_K) / p.group;
-        const int ng = ((kbf + nb) * DBLOCK_K - 1) / p.group - gf + 1;
+        const int nt = pos.nt;
+        const int kbf = pos.s * WKB;
+        const int nb = min(WKB, KB - kbf);
+        const int gf = kbf >> gshift;
+        const int ng = ((kbf + nb - 1) >> gshift) - gf + 1;
         uint8_t *st = sW + s * W_STAGE_BYTES;
         const uint32_t tx = nb * BLOCK_BYTES + ng * 2 * DBLOCK_N +
                             (p.zeros != nullptr ? ng * (DBLOCK_N / 2) : 0);
@@ -211,25 +287,28 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), DQ_WG <= 2 ? 2 : 1)
     // ----------------------------------------------- activation producer
     if (lane == 0) {
       int issued = 0;
-      for (int j = 0; j < nst; ++j) {
+      UnitPos pos = pos0;
+      for (int j = 0; j < nloc; ++j, pos.step(1, S, NT)) {
         const int cs = j / DQ_WG;                        // j is stage cs of warpgroup j % DQ_WG
         const int s = (j % DQ_WG) * ASW + cs % ASW;
         if (cs >= ASW && !mbar_wait_bounded(aempty_bar + s, ((cs / ASW) & 1) ^ 1u, p.limit_ns,
                                             abort_flag, p.err, SITE_PRODUCER_EMPTY, j, TMW4_SPIN(1)))
           break;
-        const int kbf = kb0 + j * WKB;
-        const int nb = min(WKB, nkb - j * WKB);
+        const int mt = pos.mt;
+        const int kbf = pos.s * WKB;
+        const int nb = min(WKB, KB - kbf);
         uint8_t *dst = sA + s * A_STAGE;
         if (p.act_map_3d) {
           // a box of WKB tiles; tiles past the end of K are zero-filled and
           // still counted by the transaction
           mbar_arrive_expect_tx(afull_bar + s, A_STAGE);
-          tma_load_3d(dst, &tmap_a, 0, m0, kbf, afull_bar + s);
+          tma_load_3d(dst, &tmap_a, 0, mt * BLOCK_M, kbf, afull_bar + s);
         } else {
           mbar_arrive_expect_tx(afull_bar + s, nb * A_KB);
           for (int b = 0; b < nb; ++b)
-            tma_load_2d(dst + b * A_KB, &tmap_a, (kbf + b) * DBLOCK_K, m0, afull_bar + s);
+            tma_load_2d(dst + b * A_KB, &tmap_a, (kbf + b) * DBLOCK_K, mt * BLOCK_M, afull_bar + s);
         }
+        TMW4_STAMP(1, j);
         issued = j + 1;
       }
       for (int j = max(0, issued - ASTAGES); j < issued; ++j) {
@@ -238,189 +317,379 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), DQ_WG <= 2 ? 2 : 1)
                           nullptr, p.err, SITE_DRAIN_TMA, j);
       }
     }
-  } else if (warp < FIRST_DQ_WARP) {
-    // ---------------------------------- MMA issue for warpgroup warp - 2
-    const int wg = warp - 2;
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------ MMA issue for warpgroup warp - ISSUE_WARP0
+    const int wg = warp - ISSUE_WARP0;
     if (lane == 0) {
       bool ok = true, any = false;
-      const uint32_t d_tmem = tmem + wg * DCOLS;
+      const uint32_t wg_tmem = tmem + wg * WG_COLS;
       const uint64_t desc0 = smem_desc_k128(smem_u32(sA));
-      int c = 0;                                         // this warpgroup's block counter
-      for (int j = wg, cs = 0; j < nst && ok; j += DQ_WG, ++cs) {
+      unsigned c = 0;        // this warpgroup's block counter (TMEM slot ring)
+      int e = -1;       // this warpgroup's segment counter (accumulator ring)
+      int t_cur = -1;
+      bool first = true;
+      UnitPos pos = pos0;
+      pos.step(wg, S, NT);
+      for (int j = wg, cs = 0; j < nloc && ok; j += DQ_WG, ++cs) {
+        const int t = pos.t;
+        if (t != t_cur) {
+          // first stage of a new tile segment for this warpgroup
+          t_cur = t;
+          ++e;
+          first = true;
+          if (e >= 2 && !mbar_wait_bounded(accempty_bar + wg * 2 + (e & 1), ((e >> 1) & 1) ^ 1u,
+                                           p.limit_ns, abort_flag, p.err, SITE_MMA_FULL, j,
+                                           TMW4_SPIN(2))) {
+            ok = false;
+            break;
+          }
+        }
+        const uint32_t d_tmem = wg_tmem + (e & 1) * DCOLS;
         const int as = wg * ASW + cs % ASW;
         if (!mbar_wait_bounded(afull_bar + as, (cs / ASW) & 1, p.limit_ns, abort_flag, p.err,
                                SITE_MMA_FULL, j, TMW4_SPIN(2))) {
           ok = false;
           break;
         }
-        const int nb = min(WKB, nkb - j * WKB);
+        const int nb = min(WKB, KB - pos.s * WKB);
         for (int b = 0; b < nb; ++b, ++c) {
-          const int s = wg * TSW + c % TSW;
-          const int i = j * WKB + b;
-          TMW4_STAMP(8, i);
-          if (!mbar_wait_bounded(tfull_bar + s, (c / TSW) & 1, p.limit_ns, abort_flag, p.err,
-                                 SITE_MMA_AFULL, i, TMW4_SPIN(3))) {
+          const unsigned s = c & (TSW - 1);
+          TMW4_STAMP(8, j * WKB + b);
+          if (!mbar_wait_bounded(tfull_bar + wg * TSW + s, (c / TSW) & 1u, p.limit_ns, abort_flag,
+                                 p.err, SITE_MMA_AFULL, j * WKB + b, TMW4_SPIN(3))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          TMW4_STAMP(4, i);
-          tc_mma_ts_kblock(d_tmem, tmem + A_COL0 + s * DSLOT_COLS,
+          TMW4_STAMP(4, j * WKB + b);
+          tc_mma_ts_kblock(d_tmem, wg_tmem + 2 * DCOLS + s * DSLOT_COLS,
                            desc0 + static_cast<uint64_t>((as * A_STAGE + b * A_KB) >> 4), IDESC,
-                           c == 0 ? 1u : 0u);
+                           first ? 1u : 0u);
+          first = false;
           any = true;
-          TMW4_STAMP(9, i);
-          tc_commit(kfree_bar + s);
-          TMW4_STAMP(5, i);
+          tc_commit(kfree_bar + wg * TSW + s);
+          TMW4_STAMP(5, j * WKB + b);
         }
-        if (ok) tc_commit(aempty_bar + as);
+        if (!ok) break;
+        tc_commit(aempty_bar + as);
+        // last stage of this segment for this warpgroup: hand the accumulator over
+        pos.step(DQ_WG, S, NT);
+        if (j + DQ_WG >= nloc || pos.t != t) tc_commit(accfull_bar + wg * 2 + (e & 1));
       }
-      if (ok && any) {
-        tc_commit(accum_bar);
-      } else if (any) {
+      if (!ok && any) {
         tc_commit(drain_bar + wg);
         mbar_wait_bounded(drain_bar + wg, 0, p.limit_ns, nullptr, p.err, SITE_DRAIN_MMA, wg);
       }
     }
+  } else if (warp < DQ_WARP0) {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                 // weight column within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const int M = p.M, N = p.N;
+    int e_of[DQ_WG];                                   // per warpgroup: segments seen so far
+#pragma unroll
+    for (int w = 0; w < DQ_WG; ++w) e_of[w] = -1;
+    bool ok = true;
+    int jseg = 0;                                      // first local stage of the segment
+    UnitPos pos = pos0;
+    while (jseg < nloc && ok) {
+      const int t = pos.t;
+      const int s_begin = pos.s;                         // first stage of the tile in this CTA
+      const int jend = min(nloc, jseg + (S - s_begin));
+      const int mt = pos.mt, nt = pos.nt;
+      const int m0 = mt * BLOCK_M, n = nt * DBLOCK_N + r;
+      // the warpgroups with a stage in this segment, in a fixed order
+      const int nwg = min(jend - jseg, DQ_WG);
+      if (quarter == 0 && lane == 0) TMW4_STAMP(6, jseg);
+      float acc[BLOCK_M];
+#pragma unroll
+      for (int x = 0; x < BLOCK_M; ++x) acc[x] = 0.f;
+      for (int q = 0; q < nwg && ok; ++q) {
+        const int w = (jseg + q) % DQ_WG;
+        int e = 0;
+#pragma unroll
+        for (int ww = 0; ww < DQ_WG; ++ww)
+          if (ww == w) e = ++e_of[ww];
+        ok = mbar_wait_warp(accfull_bar + w * 2 + (e & 1), (e >> 1) & 1, p.limit_ns, abort_flag,
+                            p.err, SITE_EPI_ACCUM, jseg, TMW4_SPIN(6));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a_addr = tmem + lane_addr + w * WG_COLS + (e & 1) * DCOLS;
+#pragma unroll
+        for (int c0 = 0; c0 < BLOCK_M; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_16(a_addr + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) acc[c0 + x] += __uint_as_float(v[x]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accempty_bar + w * 2 + (e & 1));
+      }
+      if (!ok) break;
+      if (quarter == 0 && lane == 0) TMW4_STAMP(10, jseg);
+      const bool whole = s_begin == 0 && jend - jseg == S;
+      if (whole) {
+#pragma unroll
+        for (int x = 0; x < BLOCK_M; ++x)
+          if (m0 + x < M) p.C[static_cast<size_t>(m0 + x) * N + n] = f32_to_16<BF16>(acc[x]);
+      } else {
+        // partial of contributor (this CTA) of tile t; the last to arrive sums
+        const int c_first = cta_of_unit(static_cast<long long>(t) * S, U, G);
+        const int c_last = cta_of_unit(static_cast<long long>(t + 1) * S - 1, U, G);
+        const int ncontrib = c_last - c_first + 1;
+        const int idx = static_cast<int>(blockIdx.x) - c_first;
+        float *slot_base = p.ws + static_cast<size_t>(t) * p.ws_slots * (DBLOCK_N * BLOCK_M);
+        float *mine = slot_base + static_cast<size_t>(idx) * (DBLOCK_N * BLOCK_M);
+        // slot layout [column r][row x]: a thread's BLOCK_M values are
+        // contiguous, so it writes and later reads them as 16-byte vectors
+        float4 *mine4 = reinterpret_cast<float4 *>(mine + r * BLOCK_M);
+#pragma unroll
+        for (int x = 0; x < BLOCK_M; x += 4)
+          mine4[x / 4] = make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (quarter == 0 && lane == 0) {
+          const unsigned prev = atomicAdd(p.counters + t, 1u);
+          *last_flag = (prev == static_cast<unsigned>(ncontrib - 1));
+        }
+        named_bar_sync(1, 128);
+        if (*last_flag) {
+          __threadfence();
+          // contributors in a fixed order; the loads of several contributors
+          // are independent and in flight together
+          float sum[BLOCK_M];
+#pragma unroll
+          for (int x = 0; x < BLOCK_M; ++x) sum[x] = 0.f;
+#pragma unroll 4
+          for (int q = 0; q < ncontrib; ++q) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                slot_base + static_cast<size_t>(q) * (DBLOCK_N * BLOCK_M) + r * BLOCK_M);
+#pragma unroll
+            for (int x = 0; x < BLOCK_M; x += 4) {
+              const float4 v4 = __ldcg(src + x / 4);
+              sum[x] += v4.x;
+              sum[x + 1] += v4.y;
+              sum[x + 2] += v4.z;
+              sum[x + 3] += v4.w;
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < BLOCK_M; ++x)
+            if (m0 + x < M) p.C[static_cast<size_t>(m0 + x) * N + n] = f32_to_16<BF16>(sum[x]);
+          if (quarter == 0 && lane == 0) p.counters[t] = 0u;
+        }
+        named_bar_sync(1, 128);   // last_flag is reused by the next segment
+      }
+      if (quarter == 0 && lane == 0) TMW4_STAMP(11, jseg);
+      pos.step(jend - jseg, S, NT);
+      jseg = jend;
+    }
   } else {
-    // ------------------------------------------------- dequant + epilogue
-    const int dw = warp - FIRST_DQ_WARP;
+    // ------------------------------------------------------------ dequant
+    const int dw = warp - DQ_WARP0;
     const int wg = dw >> 2;
     const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;            // weight column within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t slot0 = tmem + lane_addr + wg * WG_COLS + 2 * DCOLS;
+    uint64_t *const my_tfull = tfull_bar + wg * TSW;
+    uint64_t *const my_kfree = kfree_bar + wg * TSW;
     const int w_off = (r >> 6) * ATOM_BYTES + (r & 63) * 16;
     const int zshift = (r & 1) * 4;
+    const bool has_zeros = p.zeros != nullptr;
     bool ok = true;
-    int c = 0;
-    for (int j = wg; j < nst && ok; j += DQ_WG) {
+    unsigned c = 0;                               // this warpgroup's block counter
+    UnitPos pos = pos0;
+    pos.step(wg, S, NT);
+    // reads block b of a stage: its two 16-byte words, scale and zero
+    auto read_block = [&](const uint8_t *st, int b, int kbf, int gf, uint4 &v0, uint4 &v1,
+                          uint32_t &s2, uint32_t &zm2) {
+      const uint8_t *src = st + b * BLOCK_BYTES + w_off;
+      v0 = *reinterpret_cast<const uint4 *>(src);
+      v1 = *reinterpret_cast<const uint4 *>(src + 1024);
+      const int gi = ((kbf + b) >> gshift) - gf;
+      s2 = dup16(reinterpret_cast<const uint16_t *>(st + W_SC_OFF)[gi * DBLOCK_N + r]);
+      const uint32_t z =
+          has_zeros ? (static_cast<uint32_t>(st[W_ZP_OFF + gi * (DBLOCK_N / 2) + (r >> 1)]) >> zshift) & 0xFu
+                    : 8u;
+      zm2 = zero_magic2<BF16>(z);
+    };
+    // dequantizes one block into TMEM slot `slot` (stores not yet waited)
+    auto put_block = [&](const uint4 &v0, const uint4 &v1, uint32_t s2, uint32_t zm2, unsigned slot) {
+      uint32_t d0[16], d1[16];
+      const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+      const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t o[4];
+        dequant_word<BF16>(w0[q4], zm2, s2, o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d0[4 * q4 + q] = o[q];
+        dequant_word<BF16>(w1[q4], zm2, s2, o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d1[4 * q4 + q] = o[q];
+      }
+      const uint32_t ta = slot0 + slot * DSLOT_COLS;
+      tmem_st_16(ta, d0);
+      tmem_st_16(ta + 16, d1);
+    };
+    // before writing block `cl`'s slot: the MMAs of block cl - TSW retired
+    // (one thread issues the warpgroup's MMAs, so its commits complete in
+    // order and this also covers every earlier block)
+    auto slot_free = [&](unsigned cl, int step) -> bool {
+      if (cl < static_cast<unsigned>(TSW)) return true;
+      return mbar_wait_all(my_kfree + (cl & (TSW - 1)), ((cl / TSW) & 1u) ^ 1u, p.limit_ns,
+                           abort_flag, p.err, SITE_DQ_AEMPTY, step, TMW4_SPIN(5));
+    };
+    // after the stores of blocks [c0, c0 + n): hand them to the MMA issuer
+    auto publish = [&](unsigned c0, int n) {
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        for (int h = 0; h < n; ++h) mbar_arrive(my_tfull + ((c0 + h) & (TSW - 1)));
+      }
+    };
+    for (int j = wg; j < nloc && ok; j += DQ_WG, pos.step(DQ_WG, S, NT)) {
       const int ws = j % WST;
-      if (!mbar_wait_warp(wfull_bar + ws, (j / WST) & 1, p.limit_ns, abort_flag, p.err,
-                          SITE_DQ_FULL, j, TMW4_SPIN(4))) {
+      if (!mbar_wait_all(wfull_bar + ws, (j / WST) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL,
+                         j, TMW4_SPIN(4))) {
         ok = false;
         break;
       }
       const uint8_t *st = sW + ws * W_STAGE_BYTES;
-      const int kbf = kb0 + j * WKB;
-      const int nb = min(WKB, nkb - j * WKB);
-      const int gf = (kbf * DBLOCK_K) / p.group;
-      for (int b = 0; b < nb; ++b, ++c) {
-        const int i = j * WKB + b;
-        const int ts = wg * TSW + c % TSW;
-        if (quarter == 2 && lane == 0) TMW4_STAMP(12, i);
-        const uint4 v0 = *reinterpret_cast<const uint4 *>(st + b * BLOCK_BYTES + w_off);
-        const uint4 v1 = *reinterpret_cast<const uint4 *>(st + b * BLOCK_BYTES + w_off + 1024);
-        const int gi = ((kbf + b) * DBLOCK_K) / p.group - gf;
-        const uint16_t sc = reinterpret_cast<const uint16_t *>(st + W_SC_OFF)[gi * DBLOCK_N + r];
-        const uint32_t z =
-            p.zeros != nullptr
-                ? (static_cast<uint32_t>(st[W_ZP_OFF + gi * (DBLOCK_N / 2) + (r >> 1)]) >> zshift) & 0xFu
-                : 8u;
-        if (b == nb - 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(wempty_bar + ws);   // this warp is done with the stage
-        }
-        if (c >= TSW && !mbar_wait_warp(kfree_bar + ts, ((c / TSW) & 1) ^ 1u, p.limit_ns,
-                                        abort_flag, p.err, SITE_DQ_AEMPTY, i, TMW4_SPIN(5))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (quarter == 2 && lane == 0) TMW4_STAMP(2, i);
-        const uint32_t s2 = dup16(sc), zm2 = zero_magic2<BF16>(z);
-        uint32_t d0[16], d1[16];
-        {
-          const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-          const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+      const int kbf = pos.s * WKB;
+      const int nb = min(WKB, KB - kbf);
+      const int gf = kbf >> gshift;
+      if (nb == WKB) {
+        // a full stage: read all four blocks, release the stage, then two pairs
+        uint4 v[WKB][2];
+        uint32_t s2[WKB], zm2[WKB];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t o[4];
-            dequant_word<BF16>(w0[q4], zm2, s2, o);
+        for (int b = 0; b < WKB; ++b) read_block(st, b, kbf, gf, v[b][0], v[b][1], s2[b], zm2[b]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(wempty_bar + ws);
+        if (wg == 0 && quarter == 2 && lane == 0) TMW4_STAMP(12, j * WKB);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) d0[4 * q4 + q] = o[q];
-            dequant_word<BF16>(w1[q4], zm2, s2, o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) d1[4 * q4 + q] = o[q];
+        for (int pr = 0; pr < WKB / 2; ++pr) {
+          if (!slot_free(c + 2 * pr + 1, j * WKB + 2 * pr)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          put_block(v[2 * pr][0], v[2 * pr][1], s2[2 * pr], zm2[2 * pr], (c + 2 * pr) & (TSW - 1));
+          put_block(v[2 * pr + 1][0], v[2 * pr + 1][1], s2[2 * pr + 1], zm2[2 * pr + 1],
+                    (c + 2 * pr + 1) & (TSW - 1));
+          publish(c + 2 * pr, 2);
         }
-        __syncwarp();
-        const uint32_t ta = tmem + lane_addr + A_COL0 + ts * DSLOT_COLS;
-        tmem_st_16(ta, d0);
-        tmem_st_16(ta + 16, d1);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tfull_bar + ts);
-        if (quarter == 2 && lane == 0) TMW4_STAMP(3, i);
+        if (wg == 0 && quarter == 2 && lane == 0) TMW4_STAMP(3, j * WKB);
+        c += WKB;
+      } else {
+        // the ragged last stage of a tile: one block at a time
+        for (int b = 0; b < nb; ++b) {
+          uint4 v0, v1;
+          uint32_t s2, zm2;
+          read_block(st, b, kbf, gf, v0, v1, s2, zm2);
+          if (b == nb - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wempty_bar + ws);
+          }
+          if (!slot_free(c, j * WKB + b)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          put_block(v0, v1, s2, zm2, c & (TSW - 1));
+          publish(c, 1);
+          ++c;
+        }
       }
     }
-    ok = __all_sync(0xFFFFFFFFu, ok);
-    if (ok && nkb > 0)
-      ok = mbar_wait_warp(accum_bar, 0, p.limit_ns, abort_flag, p.err, SITE_EPI_ACCUM, 0, TMW4_SPIN(6));
-    tc_fence_after();
-    if (dw == 0 && lane == 0) TMW4_STAMP(6, 0);
-    tc_epilogue<BF16, BLOCK_M, DQ_WG>(p, tmem + lane_addr, wg, dw, lane, r, n0, m0, split, ok, nacc,
-                                      static_cast<uint32_t>(DCOLS), last_flag);
-    if (dw == 0 && lane == 0) TMW4_STAMP(6, 1);
   }
-
   tc_fence_before();
   __syncthreads();
+#ifdef TMW4_TRACE
+  if (threadIdx.x == 0 && p.trace != nullptr && blockIdx.x < 256)
+    p.trace[14 * 256 + blockIdx.x] = static_cast<long long>(globaltimer_ns());
+#endif
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, TCOLS);
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 bool tc_decode_ok(int block_m, int dq_warps) {
   if (block_m != 16 && block_m != 32 && block_m != 64) return false;
-  if (dq_warps != 4 && dq_warps != 8 && dq_warps != 16) return false;
+  if (dq_warps != 4 && dq_warps != 8 && dq_warps != 12) return false;
   const int wg = dq_warps / 4;
-  return dec_tsw(block_m, wg) >= 2 && WST % wg == 0;
+  return dec_tsw(block_m, wg) >= 2 && dec_wst(block_m, wg) >= 2 * wg;
 }
 
 int tc_decode_slots(int block_m, int dq_warps) { return dec_tsw(block_m, dq_warps / 4); }
 
 int tc_decode_kblocks_per_stage() { return WKB; }
 
+void tc_decode_plan(int M, int N, int K, int block_m, int sms, int *grid, long long *tiles,
+                    int *ws_slots) {
+  const long long KB = K / DBLOCK_K;
+  const long long S = (KB + WKB - 1) / WKB;
+  const long long T = static_cast<long long>(N / DBLOCK_N) * ((M + block_m - 1) / block_m);
+  const long long U = T * S;
+  const long long G = std::max<long long>(1, std::min<long long>(sms, U));
+  // contributors of a tile: the CTAs whose ranges meet its S units
+  int maxc = 1;
+  for (long long t = 0; t < T; ++t) {
+    const int c = cta_of_unit((t + 1) * S - 1, U, G) - cta_of_unit(t * S, U, G) + 1;
+    if (c > maxc) maxc = c;
+  }
+  *grid = static_cast<int>(G);
+  *tiles = T;
+  *ws_slots = maxc;
+}
+
 template <bool BF16, int BLOCK_M, int DQ_WG>
-static cudaError_t launch_dec_t(const GemmArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
+static cudaError_t launch_dec_t(const GemmArgs &a, const CUtensorMap &tmap, int grid, cudaStream_t st) {
   auto kern = tc_decode_kernel<BF16, BLOCK_M, DQ_WG>;
-  const size_t smem = dec_smem_bytes(BLOCK_M, DQ_WG);
+  const int smem = static_cast<int>(dec_smem_bytes(BLOCK_M, DQ_WG));
   static int attr_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (attr_device != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
-  dim3 grid(a.N / DBLOCK_N, (a.M + BLOCK_M - 1) / BLOCK_M, a.splits);
   kern<<<grid, dec_threads(DQ_WG), smem, st>>>(tmap, a);
   return cudaGetLastError();
 }
 
 template <bool BF16, int BLOCK_M>
-static cudaError_t launch_dec_bm(const GemmArgs &a, const CUtensorMap &tmap, int dq, cudaStream_t st) {
+static cudaError_t launch_dec_bm(const GemmArgs &a, const CUtensorMap &tmap, int dq, int grid,
+                                 cudaStream_t st) {
   switch (dq) {
-    case 4: return launch_dec_t<BF16, BLOCK_M, 1>(a, tmap, st);
-    case 8: return launch_dec_t<BF16, BLOCK_M, 2>(a, tmap, st);
-    case 16: return launch_dec_t<BF16, BLOCK_M, 4>(a, tmap, st);
+    case 4: return launch_dec_t<BF16, BLOCK_M, 1>(a, tmap, grid, st);
+    case 8: return launch_dec_t<BF16, BLOCK_M, 2>(a, tmap, grid, st);
+    case 12:
+      if constexpr (dec_tsw(BLOCK_M, 3) >= 2) return launch_dec_t<BF16, BLOCK_M, 3>(a, tmap, grid, st);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
-                             int dq_warps, cudaStream_t st) {
+                             int dq_warps, int grid, cudaStream_t st) {
   switch (block_m) {
-    case 16: return bf16 ? launch_dec_bm<true, 16>(a, tmap_a, dq_warps, st)
-                         : launch_dec_bm<false, 16>(a, tmap_a, dq_warps, st);
-    case 32: return bf16 ? launch_dec_bm<true, 32>(a, tmap_a, dq_warps, st)
-                         : launch_dec_bm<false, 32>(a, tmap_a, dq_warps, st);
-    case 64: return bf16 ? launch_dec_bm<true, 64>(a, tmap_a, dq_warps, st)
-                         : launch_dec_bm<false, 64>(a, tmap_a, dq_warps, st);
+    case 16: return bf16 ? launch_dec_bm<true, 16>(a, tmap_a, dq_warps, grid, st)
+                         : launch_dec_bm<false, 16>(a, tmap_a, dq_warps, grid, st);
+    case 32: return bf16 ? launch_dec_bm<true, 32>(a, tmap_a, dq_warps, grid, st)
+                         : launch_dec_bm<false, 32>(a, tmap_a, dq_warps, grid, st);
+    case 64: return bf16 ? launch_dec_bm<true, 64>(a, tmap_a, dq_warps, grid, st)
+                         : launch_dec_bm<false, 64>(a, tmap_a, dq_warps, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
