@@ -213,6 +213,8 @@ def run_ours(args, rank: int, world: int):
     def variant_name(v):
         if v["kernel"] == "gemv":
             return f"gemv_kernel<f16,{v['block_m']}>"
+        if v["kernel"] == "tc_decode":
+            return f"tc_decode_kernel<f16,{v['block_m']},{v['dq_warps']}>"
         return f"tc_gemm_kernel<f16,{v['block_m']},{v['dq_warps']}>"
 
     stream = torch.cuda.Stream(device=dev)

@@ -31,7 +31,7 @@ def _run(qw, a_bits, config=None):
 # (block_m, dq_warps) pairs whose pipeline cannot keep every parity wait within
 # one phase (four dequant warpgroups need STAGES % 4 == 0 and 13 / 7 TMEM A slots)
 ILLEGAL = {(16, 16), (64, 16)}
-DECODE_ILLEGAL = {(64, 12)}        # three warpgroups leave too few TMEM columns at block_m 64
+DECODE_ILLEGAL = {(64, 12), (64, 16)}   # 3-4 warpgroups leave too few TMEM columns at block_m 64
 
 
 def _variants(M):
@@ -47,7 +47,7 @@ def _variants(M):
                     continue
                 out.append(dict(kernel="tc", block_m=bm, split_k=sk, dq_warps=dq))
     for bm in (16, 32, 64):
-        for dq in (4, 8, 12):
+        for dq in (4, 8, 12, 16):
             if (bm, dq) in DECODE_ILLEGAL:
                 continue
             out.append(dict(kernel="tc_decode", block_m=bm, dq_warps=dq))
@@ -223,7 +223,7 @@ def test_long_k_every_legal_variant():
                 binding.poll_error()
                 assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, (bm, dq, sk)
     for bm in (16, 32, 64):
-        for dq in (4, 8, 12):
+        for dq in (4, 8, 12, 16):
             if (bm, dq) in DECODE_ILLEGAL:
                 continue
             cfg = dict(kernel="tc_decode", block_m=bm, dq_warps=dq)
@@ -242,7 +242,7 @@ def test_illegal_variants_are_rejected():
         with pytest.raises(binding.TmError) as e:
             binding.gemm(A, W, config=dict(kernel="tc", block_m=bm, dq_warps=16))
         assert e.value.status == binding.TM_ERR_UNSUPPORTED
-    for bm, dq in ((128, 8), (16, 2), (48, 8), (16, 16), (64, 12)):
+    for bm, dq in ((128, 8), (16, 2), (48, 8), (16, 20), (64, 12), (64, 16)):
         with pytest.raises(binding.TmError) as e:
             binding.gemm(A, W, config=dict(kernel="tc_decode", block_m=bm, dq_warps=dq))
         assert e.value.status == binding.TM_ERR_UNSUPPORTED

@@ -290,7 +290,7 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
     }
     if (c->dq_warps == 0) c->dq_warps = 8;
     if (!tc_decode_ok(c->block_m, c->dq_warps)) {
-      if (why) *why = "TC_DECODE dq_warps must be 4, 8 or 12 (12 only with block_m <= 32)";
+      if (why) *why = "TC_DECODE dq_warps must be 4, 8, 12 or 16 (12 and 16 only with block_m <= 32)";
       return false;
     }
     c->split_k = 1;   // stream-K: the grid divides the work itself
@@ -734,7 +734,7 @@ static std::vector<tm_config> candidates(const tm_packed *W, int M) {
     if (bm > 16 && bm / 2 >= M) continue;
     const int tiles = (W->N / 128) * ((M + bm - 1) / bm);
     (void)tiles;
-    for (int dq : {4, 8, 12}) {
+    for (int dq : {4, 8, 12, 16}) {
       tm_config c{TM_KERNEL_TC_DECODE, bm, 1, dq};
       if (normalize_config(W, M, &c, nullptr)) out.push_back(c);
     }

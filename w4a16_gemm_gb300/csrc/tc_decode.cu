@@ -565,24 +565,26 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
       const int nb = min(WKB, KB - kbf);
       const int gf = kbf >> gshift;
       if (nb == WKB) {
-        // a full stage: read all four blocks, release the stage, then two pairs
-        uint4 v[WKB][2];
-        uint32_t s2[WKB], zm2[WKB];
-#pragma unroll
-        for (int b = 0; b < WKB; ++b) read_block(st, b, kbf, gf, v[b][0], v[b][1], s2[b], zm2[b]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(wempty_bar + ws);
-        if (wg == 0 && quarter == 2 && lane == 0) TMW4_STAMP(12, j * WKB);
+        // a full stage, two blocks at a time; the stage is released as soon
+        // as its last block is in registers
 #pragma unroll
         for (int pr = 0; pr < WKB / 2; ++pr) {
+          uint4 v[2][2];
+          uint32_t s2[2], zm2[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            read_block(st, 2 * pr + h, kbf, gf, v[h][0], v[h][1], s2[h], zm2[h]);
+          if (pr == WKB / 2 - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wempty_bar + ws);
+          }
           if (!slot_free(c + 2 * pr + 1, j * WKB + 2 * pr)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          put_block(v[2 * pr][0], v[2 * pr][1], s2[2 * pr], zm2[2 * pr], (c + 2 * pr) & (TSW - 1));
-          put_block(v[2 * pr + 1][0], v[2 * pr + 1][1], s2[2 * pr + 1], zm2[2 * pr + 1],
-                    (c + 2 * pr + 1) & (TSW - 1));
+          put_block(v[0][0], v[0][1], s2[0], zm2[0], (c + 2 * pr) & (TSW - 1));
+          put_block(v[1][0], v[1][1], s2[1], zm2[1], (c + 2 * pr + 1) & (TSW - 1));
           publish(c + 2 * pr, 2);
         }
         if (wg == 0 && quarter == 2 && lane == 0) TMW4_STAMP(3, j * WKB);
@@ -609,6 +611,21 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
       }
     }
   }
+#ifdef TMW4_TRACE
+  // per-role finishing time of every CTA (slot by role, index 128 + CTA % 128)
+  if (p.trace != nullptr && lane == 0) {
+    const int role_slot = warp == 0 ? 6 : warp == 1 ? 10 : warp == ISSUE_WARP0 ? 12
+                        : warp == EPI_WARP0 ? 11 : warp == DQ_WARP0 ? 7 : -1;
+    if (role_slot >= 0)
+      p.trace[role_slot * 256 + 128 + (blockIdx.x & 127)] = static_cast<long long>(globaltimer_ns());
+  }
+#endif
+  // Lanes of the single-thread roles (producers, MMA issuer) leave their
+  // branch at different times than the rest of their warp; reconverge
+  // each warp first, because a CTA barrier counts a warp as arrived as soon
+  // as any of its lanes reach it, and TMEM may only be freed once every
+  // role, those lanes included, is done with it.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
 #ifdef TMW4_TRACE
@@ -618,13 +635,21 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
+#ifdef TMW4_TRACE
+    if (lane == 0 && p.trace != nullptr && blockIdx.x < 256)
+      p.trace[5 * 256 + 128 + (blockIdx.x & 127)] = static_cast<long long>(globaltimer_ns());
+#endif
     tmem_dealloc(tmem, TMEM_COLS);
+#ifdef TMW4_TRACE
+    if (lane == 0 && p.trace != nullptr && blockIdx.x < 256)
+      p.trace[9 * 256 + blockIdx.x] = static_cast<long long>(globaltimer_ns());
+#endif
   }
 }
 
 bool tc_decode_ok(int block_m, int dq_warps) {
   if (block_m != 16 && block_m != 32 && block_m != 64) return false;
-  if (dq_warps != 4 && dq_warps != 8 && dq_warps != 12) return false;
+  if (dq_warps != 4 && dq_warps != 8 && dq_warps != 12 && dq_warps != 16) return false;
   const int wg = dq_warps / 4;
   return dec_tsw(block_m, wg) >= 2 && dec_wst(block_m, wg) >= 2 * wg;
 }
@@ -676,6 +701,9 @@ static cudaError_t launch_dec_bm(const GemmArgs &a, const CUtensorMap &tmap, int
     case 8: return launch_dec_t<BF16, BLOCK_M, 2>(a, tmap, grid, st);
     case 12:
       if constexpr (dec_tsw(BLOCK_M, 3) >= 2) return launch_dec_t<BF16, BLOCK_M, 3>(a, tmap, grid, st);
+      return cudaErrorInvalidValue;
+    case 16:
+      if constexpr (dec_tsw(BLOCK_M, 4) >= 2) return launch_dec_t<BF16, BLOCK_M, 4>(a, tmap, grid, st);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }

@@ -365,6 +365,12 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
                                       nkb > 0 ? 1 : 0, 0u, last_flag);
   }
 
+  // Lanes of the single-thread roles (producers, MMA issuer) leave their
+  // branch at different times than the rest of their warp; reconverge
+  // each warp first, because a CTA barrier counts a warp as arrived as soon
+  // as any of its lanes reach it, and TMEM may only be freed once every
+  // role, those lanes included, is done with it.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) TMW4_STAMP(6, 1);
