@@ -150,6 +150,16 @@ __device__ __forceinline__ bool mbar_wait_all(uint64_t *bar, uint32_t parity, ui
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// Device-scope atomic add with acquire-release semantics; returns the old value.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
                                              uint64_t *bar) {

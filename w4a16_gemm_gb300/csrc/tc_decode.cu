@@ -352,6 +352,29 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
           break;
         }
         const int nb = min(WKB, KB - pos.s * WKB);
+        if (nb == WKB) {
+          // a full stage arrives in pairs: one wait (the pair's second block
+          // is published after its first) and one fence per eight MMAs
+#pragma unroll
+          for (int b = 0; b < WKB; b += 2, c += 2) {
+            const unsigned s0 = c & (TSW - 1), s1 = (c + 1) & (TSW - 1);
+            if (!mbar_wait_bounded(tfull_bar + wg * TSW + s1, ((c + 1) / TSW) & 1u, p.limit_ns,
+                                   abort_flag, p.err, SITE_MMA_AFULL, j * WKB + b, TMW4_SPIN(3))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t bdesc = desc0 + static_cast<uint64_t>((as * A_STAGE + b * A_KB) >> 4);
+            tc_mma_ts_kblock(d_tmem, wg_tmem + 2 * DCOLS + s0 * DSLOT_COLS, bdesc, IDESC,
+                             first ? 1u : 0u);
+            tc_commit(kfree_bar + wg * TSW + s0);
+            tc_mma_ts_kblock(d_tmem, wg_tmem + 2 * DCOLS + s1 * DSLOT_COLS,
+                             bdesc + static_cast<uint64_t>(A_KB >> 4), IDESC, 0u);
+            tc_commit(kfree_bar + wg * TSW + s1);
+            first = false;
+            any = true;
+          }
+        } else
         for (int b = 0; b < nb; ++b, ++c) {
           const unsigned s = c & (TSW - 1);
           TMW4_STAMP(8, j * WKB + b);
@@ -449,17 +472,19 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
 #pragma unroll
         for (int x = 0; x < BLOCK_M; x += 4)
           mine4[x / 4] = make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
-        __threadfence();
+        // the barrier orders the warpgroup's partial writes before one
+        // thread's release-acquire arrival on the tile counter (cumulative
+        // release); the second barrier passes the acquire on to all 128
+        // threads, so no separate fences are needed
         named_bar_sync(1, 128);
         if (quarter == 0 && lane == 0) {
-          const unsigned prev = atomicAdd(p.counters + t, 1u);
+          const unsigned prev = atomic_add_acq_rel_gpu(p.counters + t, 1u);
           *last_flag = (prev == static_cast<unsigned>(ncontrib - 1));
         }
         named_bar_sync(1, 128);
         if (*last_flag) {
-          __threadfence();
-          // contributors in a fixed order; the loads of several contributors
-          // are independent and in flight together
+          // contributors in a fixed order (this CTA's own values from
+          // registers); the loads of several contributors are in flight together
           float sum[BLOCK_M];
 #pragma unroll
           for (int x = 0; x < BLOCK_M; ++x) sum[x] = 0.f;
@@ -469,7 +494,11 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
                 slot_base + static_cast<size_t>(q) * (DBLOCK_N * BLOCK_M) + r * BLOCK_M);
 #pragma unroll
             for (int x = 0; x < BLOCK_M; x += 4) {
-              const float4 v4 = __ldcg(src + x / 4);
+              float4 v4;
+              if (q == idx)
+                v4 = make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
+              else
+                v4 = __ldcg(src + x / 4);
               sum[x] += v4.x;
               sum[x + 1] += v4.y;
               sum[x + 2] += v4.z;
