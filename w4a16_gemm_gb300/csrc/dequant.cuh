@@ -63,11 +63,11 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zm2, uint32_t 
 // (MAGIC + z) duplicated into both 16-bit halves.
 template <bool BF16>
 __device__ __forceinline__ uint32_t zero_magic2(uint32_t z) {
-  const uint32_t h = Magic<BF16>::one + z;
-  return h | (h << 16);
+  // one integer multiply-add (FMA pipe) instead of three logic ops
+  return z * 0x00010001u + Magic<BF16>::pair;
 }
 
-__device__ __forceinline__ uint32_t dup16(uint32_t h) { return (h & 0xFFFFu) | (h << 16); }
+__device__ __forceinline__ uint32_t dup16(uint32_t h) { return (h & 0xFFFFu) * 0x00010001u; }
 
 // Zero point of column n in group g from the tile-major nibble array; 8 for
 // the symmetric format (zeros == nullptr).

@@ -534,17 +534,29 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
     UnitPos pos = pos0;
     pos.step(wg, S, NT);
     // reads block b of a stage: its two 16-byte words, scale and zero
+    // shared-memory offsets of this thread's scale and zero byte for the
+    // group of block b of a full stage (stages start on a multiple of 4
+    // blocks, so the group index within the stage is b >> gshift)
+    int sc_off[WKB], zp_off[WKB];
+#pragma unroll
+    for (int b = 0; b < WKB; ++b) {
+      sc_off[b] = W_SC_OFF + ((b >> gshift) * DBLOCK_N + r) * 2;
+      zp_off[b] = W_ZP_OFF + (b >> gshift) * (DBLOCK_N / 2) + (r >> 1);
+    }
+    auto read_scale_zero = [&](const uint8_t *st, int soff, int zoff, uint32_t &s2, uint32_t &zm2) {
+      s2 = dup16(*reinterpret_cast<const uint16_t *>(st + soff));
+      const uint32_t z =
+          has_zeros ? (static_cast<uint32_t>(st[zoff]) >> zshift) & 0xFu : 8u;
+      zm2 = zero_magic2<BF16>(z);
+    };
     auto read_block = [&](const uint8_t *st, int b, int kbf, int gf, uint4 &v0, uint4 &v1,
                           uint32_t &s2, uint32_t &zm2) {
       const uint8_t *src = st + b * BLOCK_BYTES + w_off;
       v0 = *reinterpret_cast<const uint4 *>(src);
       v1 = *reinterpret_cast<const uint4 *>(src + 1024);
       const int gi = ((kbf + b) >> gshift) - gf;
-      s2 = dup16(reinterpret_cast<const uint16_t *>(st + W_SC_OFF)[gi * DBLOCK_N + r]);
-      const uint32_t z =
-          has_zeros ? (static_cast<uint32_t>(st[W_ZP_OFF + gi * (DBLOCK_N / 2) + (r >> 1)]) >> zshift) & 0xFu
-                    : 8u;
-      zm2 = zero_magic2<BF16>(z);
+      read_scale_zero(st, W_SC_OFF + (gi * DBLOCK_N + r) * 2, W_ZP_OFF + gi * (DBLOCK_N / 2) + (r >> 1),
+                      s2, zm2);
     };
     // dequantizes one block into TMEM slot `slot` (stores not yet waited)
     auto put_block = [&](const uint4 &v0, const uint4 &v1, uint32_t s2, uint32_t zm2, unsigned slot) {
@@ -601,8 +613,12 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
           uint4 v[2][2];
           uint32_t s2[2], zm2[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            read_block(st, 2 * pr + h, kbf, gf, v[h][0], v[h][1], s2[h], zm2[h]);
+          for (int h = 0; h < 2; ++h) {
+            const uint8_t *src = st + (2 * pr + h) * BLOCK_BYTES + w_off;
+            v[h][0] = *reinterpret_cast<const uint4 *>(src);
+            v[h][1] = *reinterpret_cast<const uint4 *>(src + 1024);
+            read_scale_zero(st, sc_off[2 * pr + h], zp_off[2 * pr + h], s2[h], zm2[h]);
+          }
           if (pr == WKB / 2 - 1) {
             __syncwarp();
             if (lane == 0) mbar_arrive(wempty_bar + ws);
