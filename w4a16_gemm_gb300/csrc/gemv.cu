@@ -93,25 +93,36 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
 
   const int nA = na * ATOM_N + lane, nB = nA + 32;
   const int G_rows = p.K / p.group;
-  // register double buffer: the next atom's four 128-bit loads (and its
-  // scales) are in flight while the current atom is dequantized
+  // register double buffer: the next atom's four 128-bit loads and its raw
+  // scale and zero bytes are in flight while the current atom is
+  // dequantized; nothing consumes a loaded value before its atom's turn, so
+  // no load stalls the warp early
   uint4 cur[4], nxt[4];
-  uint32_t s2c[2], zmc[2], s2n[2], zmn[2];
-  auto fetch = [&](int kb, uint4 (&c)[4], uint32_t (&s2)[2], uint32_t (&zm2)[2]) {
+  uint16_t sc_c[2], sc_n[2];
+  uint8_t zb_c[2], zb_n[2];
+  const bool has_zeros = p.zeros != nullptr;
+  auto fetch = [&](int kb, uint4 (&c)[4], uint16_t (&sc)[2], uint8_t (&zb)[2]) {
     const uint4 *atom = reinterpret_cast<const uint4 *>(p.qw + atom_offset(kb, na, KB));
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = ldg_stream(atom + lane + 32 * i);
     const int g = (kb * ATOM_K) / p.group;
-    s2[0] = dup16(__ldg(p.scales + scale_index(g, nA, G_rows)));
-    s2[1] = dup16(__ldg(p.scales + scale_index(g, nB, G_rows)));
-    zm2[0] = zero_magic2<BF16>(zero_of(p.zeros, g, nA, G_rows));
-    zm2[1] = zero_magic2<BF16>(zero_of(p.zeros, g, nB, G_rows));
+    sc[0] = __ldg(p.scales + scale_index(g, nA, G_rows));
+    sc[1] = __ldg(p.scales + scale_index(g, nB, G_rows));
+    zb[0] = has_zeros ? __ldg(p.zeros + zero_byte(g, nA, G_rows)) : static_cast<uint8_t>(0x88u);
+    zb[1] = has_zeros ? __ldg(p.zeros + zero_byte(g, nB, G_rows)) : static_cast<uint8_t>(0x88u);
   };
+  const int zsh = (lane & 1) * 4;   // nA and nB = nA + 32 have the same parity
   int kb = kb0 + warp;
-  if (kb < kb1) fetch(kb, cur, s2c, zmc);
+  if (kb < kb1) fetch(kb, cur, sc_c, zb_c);
   for (; kb < kb1; kb += GEMV_WARPS) {
     const int kbn = kb + GEMV_WARPS;
-    if (kbn < kb1) fetch(kbn, nxt, s2n, zmn);
+    if (kbn < kb1) fetch(kbn, nxt, sc_n, zb_n);
+    uint32_t s2c[2], zmc[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      s2c[i] = dup16(sc_c[i]);
+      zmc[i] = zero_magic2<BF16>((static_cast<uint32_t>(zb_c[i]) >> zsh) & 0xFu);
+    }
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
       const int col = ci & 1, h = ci >> 1;
@@ -135,10 +146,11 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
-    s2c[0] = s2n[0];
-    s2c[1] = s2n[1];
-    zmc[0] = zmn[0];
-    zmc[1] = zmn[1];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      sc_c[i] = sc_n[i];
+      zb_c[i] = zb_n[i];
+    }
   }
   // per-warp partials -> shared memory, then a fixed-order sum over warps
 #pragma unroll
