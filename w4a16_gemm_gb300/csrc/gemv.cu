@@ -186,22 +186,34 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
     const int idx = tid + 256 * i, m = idx / 64, n = na * ATOM_N + idx % 64;
     if (idx < MT * 64 && m < M) p.ws[(static_cast<size_t>(split) * M + m) * N + n] = sum[i];
   }
-  __threadfence();
+  // the barrier orders the CTA's partial writes before one thread's
+  // release-acquire arrival on the strip counter (cumulative release); the
+  // second barrier passes the acquire on to the whole CTA
   __syncthreads();
   if (tid == 0) {
-    const unsigned prev = atomicAdd(p.counters + na, 1u);
+    const unsigned prev = atomic_add_acq_rel_gpu(p.counters + na, 1u);
     s_last = (prev == static_cast<unsigned>(p.splits - 1));
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 #pragma unroll
   for (int i = 0; i < PER_THREAD; ++i) {
     const int idx = tid + 256 * i, m = idx / 64, n = na * ATOM_N + idx % 64;
     if (idx < MT * 64 && m < M) {
+      // fixed split order (this CTA's own partial from registers); eight
+      // independent loads in flight
+      const float *src = p.ws + static_cast<size_t>(m) * N + n;
+      const size_t stride = static_cast<size_t>(M) * N;
       float t = 0.f;
-      for (int s = 0; s < p.splits; ++s)
-        t += __ldcg(p.ws + (static_cast<size_t>(s) * M + m) * N + n);
+      int s0 = 0;
+      for (; s0 + 8 <= p.splits; s0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = s0 + j == split ? sum[i] : __ldcg(src + (s0 + j) * stride);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) t += v[j];
+      }
+      for (; s0 < p.splits; ++s0) t += s0 == split ? sum[i] : __ldcg(src + s0 * stride);
       p.C[static_cast<size_t>(m) * N + n] = float_to_16<BF16>(t);
     }
   }

@@ -70,16 +70,17 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs &p, uint32_t d_addr, 
     }
   }
   if (direct) return;
-  __threadfence();
+  // the barrier orders every epilogue thread's partial writes before one
+  // thread's release-acquire arrival on the tile counter (cumulative
+  // release); the second barrier passes the acquire on to all of them
   named_bar_sync(1, DQ_THREADS);
   unsigned int *ctr = p.counters + (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x);
   if (dw == 0 && lane == 0) {
-    const unsigned prev = atomicAdd(ctr, 1u);
+    const unsigned prev = atomic_add_acq_rel_gpu(ctr, 1u);
     *last_flag = (prev == static_cast<unsigned>(p.splits - 1));
   }
   named_bar_sync(1, DQ_THREADS);
   if (!*last_flag) return;
-  __threadfence();
   // fixed split order per element; 8 independent loads in flight
   const size_t split_stride = static_cast<size_t>(M) * N;
   for (int c = wg; c < BLOCK_M; c += DQ_WG) {
