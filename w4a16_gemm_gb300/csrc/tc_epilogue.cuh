@@ -32,11 +32,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // (TMEM lane r); D's columns are the rows m0.. of C.  The result is the sum,
 // in a fixed order, of `nacc` accumulators `acc_stride` TMEM columns apart
 // (nacc = 0: this CTA had no K blocks, the result is zero).  `ok` must be
-// warp-uniform.
+// warp-uniform.  With `stage` (free shared memory, 4 KB per warpgroup), the
+// direct path goes through shared memory so that C is written in 16-byte
+// pieces of whole rows instead of one 2-byte value per thread and row.
 template <bool BF16, int BLOCK_M, int DQ_WG>
 __device__ __forceinline__ void tc_epilogue(const GemmArgs &p, uint32_t d_addr, int wg, int dw,
                                             int lane, int r, int n0, int m0, int split, bool ok,
-                                            int nacc, uint32_t acc_stride, int *last_flag) {
+                                            int nacc, uint32_t acc_stride, int *last_flag,
+                                            uint8_t *stage = nullptr) {
   constexpr int DQ_THREADS = 128 * DQ_WG;
   const int N = p.N, M = p.M;
   const int n = n0 + r;
@@ -55,6 +58,24 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs &p, uint32_t d_addr, 
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) x16[j] = a == 0 ? __uint_as_float(v[j]) : x16[j] + __uint_as_float(v[j]);
+      }
+      if (direct && stage != nullptr) {
+        // [16 rows][128 columns] of 16-bit values; thread r writes column r,
+        // then each thread copies two 16-byte pieces of whole rows to C
+        uint16_t *T = reinterpret_cast<uint16_t *>(stage + wg * 4096);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) T[j * 128 + r] = f32_to_16<BF16>(x16[j]);
+        named_bar_sync(2 + wg, 128);
+#pragma unroll
+        for (int q = r; q < 256; q += 128) {
+          const int row = q >> 4, col = (q & 15) * 8;
+          const int m = m0 + c0 + row;
+          if (m < M)
+            *reinterpret_cast<uint4 *>(p.C + static_cast<size_t>(m) * N + n0 + col) =
+                *reinterpret_cast<const uint4 *>(T + row * 128 + col);
+        }
+        named_bar_sync(2 + wg, 128);
+        continue;
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {

@@ -361,8 +361,9 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
       ok = mbar_wait_warp(accum_bar, 0, p.limit_ns, abort_flag, p.err, SITE_EPI_ACCUM, 0);
     if (dw == 0 && lane == 0) TMW4_STAMP(6, 0);
     tc_fence_after();
+    // the stage ring is idle once every MMA has retired: reuse it to stage C
     tc_epilogue<BF16, BLOCK_M, DQ_WG>(p, tmem + lane_addr, wg, dw, lane, r, n0, m0, split, ok,
-                                      nkb > 0 ? 1 : 0, 0u, last_flag);
+                                      nkb > 0 ? 1 : 0, 0u, last_flag, smem);
   }
 
   // Lanes of the single-thread roles (producers, MMA issuer) leave their
