@@ -190,6 +190,25 @@ tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *stream, tm_co
 tm_status tm_tc_pipeline(int block_m, int dq_warps, int *stages, int *kblocks_per_stage,
                          int *tmem_slots, int *legal);
 
+/* Pipeline geometry of the TM_KERNEL_TC_DECODE kernel for (block_m,
+ * dq_warps): the depth of its weight-stage ring (stages of four 64-K blocks;
+ * a multiple of the warpgroup count, so a slot always feeds one
+ * warpgroup), the activation stages and TMEM operand slots each warpgroup
+ * owns, and whether the variant is accepted.  Host-only; for tests and
+ * tools.  Returns TM_ERR_INVALID_ARG on NULL outputs. */
+tm_status tm_tc_decode_pipeline(int block_m, int dq_warps, int *weight_stages,
+                                int *act_stages_per_wg, int *tmem_slots_per_wg, int *legal);
+
+/* Stream-K plan of the TM_KERNEL_TC_DECODE kernel for an M x N x K GEMM on a
+ * GPU with `sm_count` SMs: the persistent grid (CTAs), the number of output
+ * tiles (128 weight columns x block_m rows) and the fp32 partial slots per
+ * tile that the split fix-up needs (1: no tile is cut between CTAs, no
+ * scratch).  CTA c owns the (tile, 256-K stage) units [c*U/grid,
+ * (c+1)*U/grid) of the U = tiles * ceil(K/256) units.  Host-only.
+ * Returns TM_ERR_INVALID_ARG for sizes the GEMM would reject. */
+tm_status tm_decode_plan(int M, int N, int K, int block_m, int sm_count, int *grid,
+                         long long *tiles, int *partial_slots);
+
 /* Loads/saves the tuned table (JSON lines) from/to a host path. */
 tm_status tm_tune_load(const char *path);
 tm_status tm_tune_save(const char *path);

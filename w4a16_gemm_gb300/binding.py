@@ -69,6 +69,9 @@ SIGNATURES = [
     ("tm_poll_error", _I, [_VP]),
     ("tm_selftest_wait_timeout", _I, [_LL, _VP]),
     ("tm_tc_pipeline", _I, [_I, _I] + [ctypes.POINTER(_I)] * 4),
+    ("tm_tc_decode_pipeline", _I, [_I, _I] + [ctypes.POINTER(_I)] * 4),
+    ("tm_decode_plan", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_LL),
+                            ctypes.POINTER(_I)]),
     ("tm_last_error", ctypes.c_char_p, []),
     ("tm_version", ctypes.c_char_p, []),
 ]
@@ -251,6 +254,23 @@ def tc_pipeline(block_m: int, dq_warps: int) -> dict:
     _check(lib().tm_tc_pipeline(int(block_m), int(dq_warps), *[ctypes.byref(x) for x in v]))
     return {"stages": v[0].value, "kblocks_per_stage": v[1].value, "tmem_slots": v[2].value,
             "legal": bool(v[3].value)}
+
+
+def tc_decode_pipeline(block_m: int, dq_warps: int) -> dict:
+    """Pipeline geometry of a tcgen05 decode variant (no GPU needed)."""
+    v = [ctypes.c_int() for _ in range(4)]
+    _check(lib().tm_tc_decode_pipeline(int(block_m), int(dq_warps), *[ctypes.byref(x) for x in v]))
+    return {"weight_stages": v[0].value, "act_stages_per_wg": v[1].value,
+            "tmem_slots_per_wg": v[2].value, "legal": bool(v[3].value)}
+
+
+def decode_plan(M: int, N: int, K: int, block_m: int, sm_count: int) -> dict:
+    """Stream-K plan of the tcgen05 decode kernel (no GPU needed)."""
+    g, p = ctypes.c_int(), ctypes.c_int()
+    t = ctypes.c_longlong()
+    _check(lib().tm_decode_plan(int(M), int(N), int(K), int(block_m), int(sm_count),
+                                ctypes.byref(g), ctypes.byref(t), ctypes.byref(p)))
+    return {"grid": g.value, "tiles": t.value, "partial_slots": p.value}
 
 
 def version() -> str:

@@ -467,6 +467,33 @@ static tm_status check_gemm_args(const void *A, const tm_packed *W, const void *
 }
 
 // ================================================================ C ABI
+extern "C" tm_status tm_tc_decode_pipeline(int block_m, int dq_warps, int *weight_stages,
+                                           int *act_stages_per_wg, int *tmem_slots_per_wg,
+                                           int *legal) {
+  if (weight_stages == nullptr || act_stages_per_wg == nullptr || tmem_slots_per_wg == nullptr ||
+      legal == nullptr)
+    return fail(TM_ERR_INVALID_ARG, "output pointers must not be NULL");
+  *legal = tc_decode_ok(block_m, dq_warps) ? 1 : 0;
+  if (block_m != 16 && block_m != 32 && block_m != 64)
+    return fail(TM_ERR_INVALID_ARG, "block_m must be 16, 32 or 64");
+  if (dq_warps != 4 && dq_warps != 8 && dq_warps != 12 && dq_warps != 16)
+    return fail(TM_ERR_INVALID_ARG, "dq_warps must be 4, 8, 12 or 16");
+  tc_decode_pipeline(block_m, dq_warps, weight_stages, act_stages_per_wg, tmem_slots_per_wg);
+  return TM_OK;
+}
+
+extern "C" tm_status tm_decode_plan(int M, int N, int K, int block_m, int sm_count, int *grid,
+                                    long long *tiles, int *partial_slots) {
+  if (grid == nullptr || tiles == nullptr || partial_slots == nullptr)
+    return fail(TM_ERR_INVALID_ARG, "output pointers must not be NULL");
+  if (M <= 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 64 != 0 || sm_count <= 0)
+    return fail(TM_ERR_INVALID_ARG, "need M, N, K, sm_count > 0, N %% 128 == 0, K %% 64 == 0");
+  if (block_m != 16 && block_m != 32 && block_m != 64)
+    return fail(TM_ERR_INVALID_ARG, "block_m must be 16, 32 or 64");
+  tc_decode_plan(M, N, K, block_m, sm_count, grid, tiles, partial_slots);
+  return TM_OK;
+}
+
 extern "C" {
 
 const char *tm_version(void) { return "tmw4 0.1 (sm_103a)"; }

@@ -60,6 +60,8 @@ cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, i
 bool tc_decode_ok(int block_m, int dq_warps);
 int tc_decode_slots(int block_m, int dq_warps);
 int tc_decode_kblocks_per_stage();   // 64-K blocks per activation box
+void tc_decode_pipeline(int block_m, int dq_warps, int *weight_stages, int *act_stages_per_wg,
+                        int *tmem_slots_per_wg);
 void tc_decode_plan(int M, int N, int K, int block_m, int sms, int *grid, long long *tiles,
                     int *ws_slots);
 cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,

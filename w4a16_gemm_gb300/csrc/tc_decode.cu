@@ -703,6 +703,14 @@ int tc_decode_slots(int block_m, int dq_warps) { return dec_tsw(block_m, dq_warp
 
 int tc_decode_kblocks_per_stage() { return WKB; }
 
+void tc_decode_pipeline(int block_m, int dq_warps, int *weight_stages, int *act_stages_per_wg,
+                        int *tmem_slots_per_wg) {
+  const int wg = dq_warps / 4;
+  *weight_stages = wg > 0 ? dec_wst(block_m, wg) : 0;
+  *act_stages_per_wg = wg > 0 ? dec_asw(block_m, wg) : 0;
+  *tmem_slots_per_wg = wg > 0 ? dec_tsw(block_m, wg) : 0;
+}
+
 void tc_decode_plan(int M, int N, int K, int block_m, int sms, int *grid, long long *tiles,
                     int *ws_slots) {
   const long long KB = K / DBLOCK_K;
