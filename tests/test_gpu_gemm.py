@@ -30,7 +30,7 @@ def _run(qw, a_bits, config=None):
 
 # (block_m, dq_warps) pairs whose pipeline cannot keep every parity wait within
 # one phase (four dequant warpgroups need STAGES % 4 == 0 and 13 / 7 TMEM A slots)
-ILLEGAL = {(16, 16), (64, 16)}
+ILLEGAL = {(16, 16), (64, 16), (256, 16)}
 DECODE_ILLEGAL = {(64, 12), (64, 16)}   # 3-4 warpgroups leave too few TMEM columns at block_m 64
 
 

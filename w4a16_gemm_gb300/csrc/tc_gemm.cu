@@ -56,8 +56,10 @@ __host__ __device__ constexpr int a_kb_bytes(int block_m) { return block_m * BLO
 __host__ __device__ constexpr int stage_bytes(int block_m) {
   return kbs_for(block_m) * (a_kb_bytes(block_m) + W_KB_BYTES + SC_GROUP_BYTES + ZP_GROUP_BYTES);
 }
+// A copy takes ~1500 cycles to land under prefill load, so the ring must be
+// deep enough to cover it: 256-row tiles take the six stages that fit.
 __host__ __device__ constexpr int stages_for(int block_m) {
-  return block_m <= 64 ? 4 : block_m <= 128 ? 8 : 4;
+  return block_m <= 64 ? 4 : block_m <= 128 ? 8 : 6;
 }
 // TMEM: D occupies columns [0, max(32, BLOCK_M)); the rest of a 256-column
 // (BLOCK_M <= 128) or 512-column allocation is a ring of k-block A slots.
