@@ -296,3 +296,11 @@ def test_decode_model_catches_a_ring_too_small_for_a_pair():
     failures = [simulate_decode(4, 2, 1, 2, [(t // 3, WKB) for t in range(12)], seed=s)
                 for s in range(10)]
     assert any(f is not None for f in failures)
+
+
+def test_decode_model_catches_a_weight_ring_shared_across_warpgroups():
+    # 5 weight slots over 2 warpgroups: a warp may poll a slot whose previous
+    # phase belonged to the other warpgroup and take phase c - 2 for c
+    rnd = random.Random(3)
+    failures = [simulate_decode(5, 2, 4, 2, _stage_list(rnd), seed=s) for s in range(200)]
+    assert any(f is not None and "weight slot" in f for f in failures)
