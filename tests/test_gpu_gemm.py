@@ -92,7 +92,7 @@ def test_repeated_runs_are_identical():
     W = packed_from(qw)
     A = binding.acts_to_device(a, torch.bfloat16)
     for cfg in (dict(kernel="tc", block_m=256, split_k=1, dq_warps=4),
-                dict(kernel="tc", block_m=128, split_k=1, dq_warps=16),
+                dict(kernel="tc", block_m=128, split_k=1, dq_warps=8),
                 dict(kernel="tc", block_m=32, split_k=2, dq_warps=16),
                 dict(kernel="tc", block_m=16, split_k=4, dq_warps=8)):
         first = gemm_poisoned(A, W, config=cfg)
