@@ -214,27 +214,26 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
     if (p.trace != nullptr && blockIdx.x < 256)
       p.trace[13 * 256 + blockIdx.x] = static_cast<long long>(globaltimer_ns());
 #endif
-    for (int s = 0; s < WST; ++s) {
-      mbar_init(wfull_bar + s, 1);
-      mbar_init(wempty_bar + s, 4);
-    }
-    for (int s = 0; s < ASTAGES; ++s) {
-      mbar_init(afull_bar + s, 1);
-      mbar_init(aempty_bar + s, 1);
-    }
-    for (int s = 0; s < TSLOTS; ++s) {
-      mbar_init(tfull_bar + s, 4);
-      mbar_init(kfree_bar + s, 1);
-    }
-    for (int s = 0; s < 2 * DQ_WG; ++s) {
-      mbar_init(accfull_bar + s, 1);
-      mbar_init(accempty_bar + s, 4);
-    }
-    for (int g = 0; g < DQ_WG; ++g) mbar_init(drain_bar + g, 1);
     *abort_flag = 0;
     *last_flag = 0;
-    fence_mbar_init();
     prefetch_tensormap(&tmap_a);
+  }
+  {
+    // one barrier per thread: the barriers are contiguous, in the order
+    // wfull, wempty, afull, aempty, tfull, kfree, accfull, accempty, drain
+    constexpr int NBAR = 2 * WST + 2 * ASTAGES + 2 * TSLOTS + 4 * DQ_WG + DQ_WG;
+    static_assert(NBAR <= 64 + 32 * DQ_WG + 128 + 128 * DQ_WG, "one thread per barrier");
+    const int b = threadIdx.x;
+    if (b < NBAR) {
+      int cnt = 1;
+      if (b >= WST && b < 2 * WST) cnt = 4;                                   // wempty
+      const int t0 = 2 * WST + 2 * ASTAGES;
+      if (b >= t0 && b < t0 + TSLOTS) cnt = 4;                                 // tfull
+      const int e0 = t0 + 2 * TSLOTS + 2 * DQ_WG;
+      if (b >= e0 && b < e0 + 2 * DQ_WG) cnt = 4;                              // accempty
+      mbar_init(wfull_bar + b, cnt);
+      fence_mbar_init();
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, TMEM_COLS);

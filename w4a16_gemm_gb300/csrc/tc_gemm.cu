@@ -110,7 +110,6 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
   constexpr int A_COL0 = tmem_a_col0(BLOCK_M);
   constexpr int TS = tmem_a_stages(BLOCK_M);
   constexpr uint32_t IDESC = idesc_f16(BF16 ? 1u : 0u, 128u, static_cast<uint32_t>(BLOCK_M));
-  constexpr int DQ_THREADS = 128 * DQ_WG;
   static_assert(BLOCK_M % 16 == 0 && BLOCK_M >= 16 && BLOCK_M <= 256, "MMA N");
   static_assert(DQ_WG == 1 || DQ_WG == 2 || DQ_WG == 4, "dequant warpgroups");
   static_assert(TS >= 2, "TMEM A slots");
@@ -144,24 +143,26 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
   const int kb0 = split * p.kb_per_split;
   const int nkb = max(0, min(KB, kb0 + p.kb_per_split) - kb0);
   const int nstages = (nkb + KBS - 1) / KBS;
-  const int N = p.N, M = p.M;
 
   if (threadIdx.x == 0) {
     TMW4_STAMP(7, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar + s, 1);
-      mbar_init(empty_bar + s, 1 + 4);   // MMA commit + the 4 warps of one warpgroup
-    }
-    for (int t = 0; t < TS; ++t) {
-      mbar_init(afull_bar + t, 4);
-      mbar_init(aempty_bar + t, 1);
-    }
-    mbar_init(accum_bar, 1);
-    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     *last_flag = 0;
-    fence_mbar_init();
     prefetch_tensormap(&tmap_a);
+  }
+  {
+    // one barrier per thread; the barriers are contiguous, in the order
+    // full, empty, afull, aempty, accum, drain
+    constexpr int NBAR = 2 * STAGES + 2 * TS + 2;
+    static_assert(NBAR <= 64 + 128 * DQ_WG, "one thread per barrier");
+    const int b = threadIdx.x;
+    if (b < NBAR) {
+      int cnt = 1;
+      if (b >= STAGES && b < 2 * STAGES) cnt = 1 + 4;   // MMA commit + the 4 warps of one warpgroup
+      if (b >= 2 * STAGES && b < 2 * STAGES + TS) cnt = 4;
+      mbar_init(full_bar + b, cnt);
+      fence_mbar_init();
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, TMEM_COLS);
