@@ -24,6 +24,14 @@
  *   - Conditions found on the device (a code byte above 15, a bounded wait
  *     that gave up) are recorded in a per-device error word and reported by
  *     tm_poll_error().
+ *   - GEMM kernels are launched with programmatic stream serialization
+ *     (programmatic dependent launch): a GEMM may start while the previous
+ *     kernel in the stream is finishing and stream its packed weights at
+ *     once, but it reads A and writes C (and its split-K scratch) only after
+ *     that kernel has completed and its writes are visible.  Stream order is
+ *     therefore kept for A and C; the packed weight must not be modified by
+ *     the previous kernel.  Setting the environment variable TM_PDL=0
+ *     before the first GEMM launches every kernel plainly.
  */
 #ifndef TMW4_H
 #define TMW4_H

@@ -73,6 +73,16 @@ static unsigned long long wait_limit_ns() {
   return v;
 }
 
+// GEMM launches overlap the previous kernel in the stream (programmatic
+// dependent launch) unless TM_PDL=0.
+static bool pdl_enabled() {
+  static const bool v = [] {
+    const char *e = getenv("TM_PDL");
+    return !(e != nullptr && e[0] == '0' && e[1] == '\0');
+  }();
+  return v;
+}
+
 // --------------------------------------------------- per-device state
 static std::mutex g_mu;
 static constexpr int kMaxDevices = 64;
@@ -413,6 +423,7 @@ static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, con
   size_t ws_floats = 0, n_counters = 0;
   plan_work(W, M, cfg, &a, &dec_grid, &ws_floats, &n_counters);
   a.limit_ns = wait_limit_ns();
+  a.pdl = pdl_enabled() ? 1 : 0;
 #ifdef TMW4_TRACE
   a.trace = g_trace;
 #endif
@@ -932,6 +943,7 @@ extern "C" tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, vo
   size_t ws_floats = 0, tiles = 0;
   plan_work(W, M, cfg, &a, &dec_grid, &ws_floats, &tiles);
   a.limit_ns = wait_limit_ns();
+  a.pdl = pdl_enabled() ? 1 : 0;
   const bool bf16 = W->dtype == TM_BF16;
   if (ws_floats > 0) {
     if (ws_floats > kStaticWsFloats || tiles > kStaticCounters)

@@ -74,17 +74,6 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int M = p.M, N = p.N;
 
-  // activations of this K range -> shared memory, 16 bytes per copy (rows >= M are zero)
-  const int klen = (kb1 - kb0) * ATOM_K;
-  for (int idx = tid; idx < MT * (klen / 8); idx += blockDim.x) {
-    const int m = idx / (klen / 8), kk = (idx % (klen / 8)) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (m < M)
-      v = *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * p.K + kb0 * ATOM_K + kk);
-    *reinterpret_cast<uint4 *>(As + m * ldA + kk) = v;
-  }
-  __syncthreads();
-
   float acc[MT][4];
 #pragma unroll
   for (int m = 0; m < MT; ++m)
@@ -113,7 +102,23 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
   };
   const int zsh = (lane & 1) * 4;   // nA and nB = nA + 32 have the same parity
   int kb = kb0 + warp;
+  // the packed weights do not depend on earlier kernels in the stream: the
+  // first atom's loads go out before waiting for them
   if (kb < kb1) fetch(kb, cur, sc_c, zb_c);
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // activations of this K range -> shared memory, 16 bytes per copy (rows >= M are zero)
+  const int klen = (kb1 - kb0) * ATOM_K;
+  for (int idx = tid; idx < MT * (klen / 8); idx += blockDim.x) {
+    const int m = idx / (klen / 8), kk = (idx % (klen / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M)
+      v = *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * p.K + kb0 * ATOM_K + kk);
+    *reinterpret_cast<uint4 *>(As + m * ldA + kk) = v;
+  }
+  __syncthreads();
+
   for (; kb < kb1; kb += GEMV_WARPS) {
     const int kbn = kb + GEMV_WARPS;
     if (kbn < kb1) fetch(kbn, nxt, sc_n, zb_n);
@@ -242,8 +247,7 @@ static cudaError_t launch_gemv_t(const GemmArgs &a, cudaStream_t st) {
     attr_device = dev;
   }
   dim3 grid(a.N / ATOM_N, a.splits);
-  gemv_kernel<BF16, MT><<<grid, 256, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(gemv_kernel<BF16, MT>, grid, dim3(256), smem, st, a.pdl != 0, a);
 }
 
 cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, cudaStream_t st) {

@@ -34,10 +34,33 @@ struct GemmArgs {
   int act_map_3d;    // TC: the activation tensor map is 3-D (64 x M x K/64)
   int ws_slots;      // TC_DECODE: fp32 partial slots per tile in ws (stream-K contributors)
   unsigned long long limit_ns;
+  // Host side only: launch with programmatic stream serialization, so the
+  // kernel's prologue and weight loads overlap the previous kernel's tail.
+  // Every GEMM kernel calls pdl_wait() before it reads A or touches C, the
+  // split-K workspace or its counters.
+  int pdl;
   // Debug builds compiled with -DTMW4_TRACE record per-stage SM cycle
   // stamps of CTA (0,0,0) here ([8][256] slots); nullptr otherwise.
   long long *trace;
 };
+
+// Launch kern<<<grid, block, smem, st>>>(args...), with programmatic stream
+// serialization when pdl is set (see GemmArgs::pdl).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // GEMV (CUDA cores): rows_tmpl in {1,2,4,8} >= M.  Shared memory bytes:
 size_t gemv_smem_bytes(int rows_tmpl, int kb_per_split);

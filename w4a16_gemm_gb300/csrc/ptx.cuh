@@ -188,6 +188,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const CUtensorMap *m
       : "memory");
 }
 
+// Programmatic dependent launch (griddepcontrol, sm_90 and later).  A kernel
+// launched with programmatic stream serialization may start while the
+// previous kernel in the stream is still running.  pdl_wait() blocks the
+// calling thread until every kernel this launch depends on has completed and
+// its memory writes are visible; it returns at once for a plain launch.
+// pdl_launch_dependents() lets the next such launch in the stream start
+// early (the next kernel still waits for this one before reading its output).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -244,6 +244,10 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   if (threadIdx.x == 0) TMW4_STAMP(7, 0);
+  // Only the activation producer and the epilogue touch memory that an
+  // earlier kernel in the stream may write (A; C, the partials and the
+  // counters): they call pdl_wait() first.  The weight stream starts at once.
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // --------------------------------------------------- weight producer
@@ -285,6 +289,7 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
   } else if (warp == 1) {
     // ----------------------------------------------- activation producer
     if (lane == 0) {
+      pdl_wait();
       int issued = 0;
       UnitPos pos = pos0;
       for (int j = 0; j < nloc; ++j, pos.step(1, S, NT)) {
@@ -405,6 +410,7 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
     }
   } else if (warp < DQ_WARP0) {
     // -------------------------------------------------------------- epilogue
+    pdl_wait();
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                 // weight column within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
@@ -741,8 +747,8 @@ static cudaError_t launch_dec_t(const GemmArgs &a, const CUtensorMap &tmap, int 
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
-  kern<<<grid, dec_threads(DQ_WG), smem, st>>>(tmap, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(dec_threads(DQ_WG)), static_cast<size_t>(smem), st,
+                       a.pdl != 0, tmap, a);
 }
 
 template <bool BF16, int BLOCK_M>

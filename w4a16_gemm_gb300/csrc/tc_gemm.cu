@@ -173,6 +173,10 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   if (threadIdx.x == 0) TMW4_STAMP(7, 0);
+  // the prologue above overlaps the previous kernel in the stream; nothing
+  // below runs before it has completed
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -411,8 +415,7 @@ static cudaError_t launch_tc_t(const GemmArgs &a, const CUtensorMap &tmap, cudaS
     attr_device = dev;
   }
   dim3 grid(a.N / BLOCK_N, (a.M + BLOCK_M - 1) / BLOCK_M, a.splits);
-  kern<<<grid, 64 + 128 * DQ_WG, smem, st>>>(tmap, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(64 + 128 * DQ_WG), smem, st, a.pdl != 0, tmap, a);
 }
 
 template <bool BF16, int BLOCK_M>
