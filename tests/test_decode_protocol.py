@@ -174,8 +174,9 @@ def simulate_decode(WST, ASW, TSW, DQ, stages, seed, max_steps=400_000):
                     accfull[w][buf].arrive()
             groups = [(0, 2), (2, 2)] if nb == WKB else [(b, 1) for b in range(nb)]
             for gi, (b0, cnt) in enumerate(groups):
-                cl = c + cnt - 1
-                yield from wait(tfull[w][cl % TSW], (cl // TSW) & 1)
+                for h in range(cnt):                # every block of the group
+                    cl = c + h
+                    yield from wait(tfull[w][cl % TSW], (cl // TSW) & 1)
                 for h in range(cnt):
                     slot = (c + h) % TSW
                     if any(tmem[w][slot][q] != (j, b0 + h) for q in range(4)):
@@ -196,11 +197,10 @@ def simulate_decode(WST, ASW, TSW, DQ, stages, seed, max_steps=400_000):
             for gi, (b0, cnt) in enumerate(groups):
                 if smem_w[s] != j:
                     errors.append(f"warp {w}.{q}: weight slot {s} holds {smem_w[s]}, wanted {j}")
-                if gi == len(groups) - 1:
-                    wempty[s].arrive()          # last read of the stage
-                cl = c + cnt - 1                # the later block's slot free covers both
-                if cl >= TSW:
-                    yield from wait(kfree[w][cl % TSW], ((cl // TSW) & 1) ^ 1)
+                for h in range(cnt):            # every slot of the group is free
+                    cl = c + h
+                    if cl >= TSW:
+                        yield from wait(kfree[w][cl % TSW], ((cl // TSW) & 1) ^ 1)
                 yield
                 for h in range(cnt):
                     tmem[w][(c + h) % TSW][q] = None      # tcgen05.st in flight
@@ -209,6 +209,10 @@ def simulate_decode(WST, ASW, TSW, DQ, stages, seed, max_steps=400_000):
                     tmem[w][(c + h) % TSW][q] = (j, b0 + h)
                 for h in range(cnt):
                     tfull[w][(c + h) % TSW].arrive()
+                if gi == len(groups) - 1:
+                    if smem_w[s] != j:
+                        errors.append(f"warp {w}.{q}: weight slot {s} overwritten while in use")
+                    wempty[s].arrive()          # the stage's data has been used
                 c += cnt
 
     def epilogue():

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
       v = *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * p.K + kb0 * ATOM_K + kk);
     *reinterpret_cast<uint4 *>(As + m * ldA + kk) = v;
   }
+  __syncwarp();   // a CTA barrier counts a warp as arrived once any lane reaches it
   __syncthreads();
 
   for (; kb < kb1; kb += GEMV_WARPS) {
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
     const unsigned prev = atomic_add_acq_rel_gpu(p.counters + na, 1u);
     s_last = (prev == static_cast<unsigned>(p.splits - 1));
   }
+  __syncwarp();   // lane 0 of warp 0 must be out of its branch before the barrier
   __syncthreads();
   if (!s_last) return;
 #pragma unroll
@@ -247,7 +249,7 @@ static cudaError_t launch_gemv_t(const GemmArgs &a, cudaStream_t st) {
     attr_device = dev;
   }
   dim3 grid(a.N / ATOM_N, a.splits);
-  return launch_kernel(gemv_kernel<BF16, MT>, grid, dim3(256), smem, st, a.pdl != 0, a);
+  return launch_kernel(gemv_kernel<BF16, MT>, grid, dim3(256), smem, st, a.pdl != 0, 1u, a);
 }
 
 cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, cudaStream_t st) {

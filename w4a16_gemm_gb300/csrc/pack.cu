@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
       for (int b = 0; b < 4; ++b) tile[row][col + 4 * i + b] = (w[i] >> (8 * b)) & 0xFu;
     }
   }
+  __syncwarp();   // rejoin lanes that took the error branch before the CTA barrier
   __syncthreads();
   uint32_t *out = reinterpret_cast<uint32_t *>(qw + atom_offset(kb, na, K / ATOM_K));
 #pragma unroll

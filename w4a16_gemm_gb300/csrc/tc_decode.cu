@@ -14,8 +14,8 @@
 //     activations in 4-block boxes of a 3-D tensor map;
 //   * per-thread 128-bit global loads of the weights crowd the SM's
 //     memory-instruction queue that tcgen05 and mbarrier instructions also
-//     use, so weights go through shared memory, and a weight stage is
-//     released as soon as its dequant warps have read it;
+//     use, so weights go through shared memory; a weight stage is released
+//     once its dequant warps have used its data;
 //   * a weight stage takes ~1.5-2 us from copy issue to arrival under load,
 //     so each warpgroup keeps several stages in flight: one CTA per SM with a
 //     deep ring;
@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
+  __syncwarp();   // threads that initialised a barrier rejoin their warp first
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -357,12 +358,14 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
         }
         const int nb = min(WKB, KB - pos.s * WKB);
         if (nb == WKB) {
-          // a full stage arrives in pairs: one wait (the pair's second block
-          // is published after its first) and one fence per eight MMAs
+          // a full stage arrives in pairs: two waits (each a single try_wait
+          // once the pair is published) and one fence per eight MMAs
 #pragma unroll
           for (int b = 0; b < WKB; b += 2, c += 2) {
             const unsigned s0 = c & (TSW - 1), s1 = (c + 1) & (TSW - 1);
-            if (!mbar_wait_bounded(tfull_bar + wg * TSW + s1, ((c + 1) / TSW) & 1u, p.limit_ns,
+            if (!mbar_wait_bounded(tfull_bar + wg * TSW + s0, (c / TSW) & 1u, p.limit_ns,
+                                   abort_flag, p.err, SITE_MMA_AFULL, j * WKB + b, TMW4_SPIN(3)) ||
+                !mbar_wait_bounded(tfull_bar + wg * TSW + s1, ((c + 1) / TSW) & 1u, p.limit_ns,
                                    abort_flag, p.err, SITE_MMA_AFULL, j * WKB + b, TMW4_SPIN(3))) {
               ok = false;
               break;
@@ -582,13 +585,23 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
       tmem_st_16(ta, d0);
       tmem_st_16(ta + 16, d1);
     };
-    // before writing block `cl`'s slot: the MMAs of block cl - TSW retired
-    // (one thread issues the warpgroup's MMAs, so its commits complete in
-    // order and this also covers every earlier block)
+    // before writing block `cl`'s slot: the MMAs of block cl - TSW retired.
+    // One thread issues the warpgroup's MMAs and its commits complete in
+    // order, so waiting for the later block of a pair would cover the earlier
+    // one; both are waited for all the same (one try_wait when done), which
+    // keeps every slot reuse explicit.
     auto slot_free = [&](unsigned cl, int step) -> bool {
       if (cl < static_cast<unsigned>(TSW)) return true;
       return mbar_wait_all(my_kfree + (cl & (TSW - 1)), ((cl / TSW) & 1u) ^ 1u, p.limit_ns,
                            abort_flag, p.err, SITE_DQ_AEMPTY, step, TMW4_SPIN(5));
+    };
+    // the weight stage `ws` is no longer read by this warp: order its shared-
+    // memory reads before the copy that will refill it (generic to async
+    // proxy), then arrive on the stage's empty barrier
+    auto release_stage = [&](int ws_) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(wempty_bar + ws_);
     };
     // after the stores of blocks [c0, c0 + n): hand them to the MMA issuer
     auto publish = [&](unsigned c0, int n) {
@@ -611,8 +624,8 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
       const int nb = min(WKB, KB - kbf);
       const int gf = kbf >> gshift;
       if (nb == WKB) {
-        // a full stage, two blocks at a time; the stage is released as soon
-        // as its last block is in registers
+        // a full stage, two blocks at a time; the stage is released once its
+        // last pair has been dequantized
 #pragma unroll
         for (int pr = 0; pr < WKB / 2; ++pr) {
           uint4 v[2][2];
@@ -624,11 +637,8 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
             v[h][1] = *reinterpret_cast<const uint4 *>(src + 1024);
             read_scale_zero(st, sc_off[2 * pr + h], zp_off[2 * pr + h], s2[h], zm2[h]);
           }
-          if (pr == WKB / 2 - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(wempty_bar + ws);
-          }
-          if (!slot_free(c + 2 * pr + 1, j * WKB + 2 * pr)) {
+          if (!slot_free(c + 2 * pr, j * WKB + 2 * pr) ||
+              !slot_free(c + 2 * pr + 1, j * WKB + 2 * pr)) {
             ok = false;
             break;
           }
@@ -636,6 +646,7 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
           put_block(v[0][0], v[0][1], s2[0], zm2[0], (c + 2 * pr) & (TSW - 1));
           put_block(v[1][0], v[1][1], s2[1], zm2[1], (c + 2 * pr + 1) & (TSW - 1));
           publish(c + 2 * pr, 2);
+          if (pr == WKB / 2 - 1) release_stage(ws);
         }
         if (wg == 0 && quarter == 2 && lane == 0) TMW4_STAMP(3, j * WKB);
         c += WKB;
@@ -645,10 +656,6 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
           uint4 v0, v1;
           uint32_t s2, zm2;
           read_block(st, b, kbf, gf, v0, v1, s2, zm2);
-          if (b == nb - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(wempty_bar + ws);
-          }
           if (!slot_free(c, j * WKB + b)) {
             ok = false;
             break;
@@ -656,6 +663,7 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
           tc_fence_after();
           put_block(v0, v1, s2, zm2, c & (TSW - 1));
           publish(c, 1);
+          if (b == nb - 1) release_stage(ws);
           ++c;
         }
       }
@@ -748,7 +756,7 @@ static cudaError_t launch_dec_t(const GemmArgs &a, const CUtensorMap &tmap, int 
     attr_device = dev;
   }
   return launch_kernel(kern, dim3(grid), dim3(dec_threads(DQ_WG)), static_cast<size_t>(smem), st,
-                       a.pdl != 0, tmap, a);
+                       a.pdl != 0, 1u, tmap, a);
 }
 
 template <bool BF16, int BLOCK_M>

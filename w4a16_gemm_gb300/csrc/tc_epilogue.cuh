@@ -23,7 +23,12 @@ __device__ __forceinline__ uint16_t f32_to_16(float x) {
   }
 }
 
+// bar.sync counts a whole warp as arrived as soon as any of its threads
+// executes it.  A thread still inside a lane-0 branch (the counter atomic
+// just before the fix-up barriers) would then miss the barrier and arrive at
+// the next one instead, so every warp reconverges first.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 

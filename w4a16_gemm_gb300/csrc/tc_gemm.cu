@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
+  __syncwarp();   // threads that initialised a barrier rejoin their warp first
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -415,7 +416,7 @@ static cudaError_t launch_tc_t(const GemmArgs &a, const CUtensorMap &tmap, cudaS
     attr_device = dev;
   }
   dim3 grid(a.N / BLOCK_N, (a.M + BLOCK_M - 1) / BLOCK_M, a.splits);
-  return launch_kernel(kern, grid, dim3(64 + 128 * DQ_WG), smem, st, a.pdl != 0, tmap, a);
+  return launch_kernel(kern, grid, dim3(64 + 128 * DQ_WG), smem, st, a.pdl != 0, 1u, tmap, a);
 }
 
 template <bool BF16, int BLOCK_M>
@@ -461,11 +462,13 @@ __global__ void wait_selftest_kernel(unsigned int *err, unsigned long long limit
     abort_flag = 0;
     fence_mbar_init();
   }
+  __syncwarp();
   __syncthreads();
   if (threadIdx.x == 0) {
     // nothing arrives on `bar`: the wait must give up after limit_ns
     mbar_wait_bounded(&bar, 0, limit_ns, &abort_flag, err, SITE_SELFTEST, 0);
   }
+  __syncwarp();
   __syncthreads();
 }
 
