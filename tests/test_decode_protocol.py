@@ -174,9 +174,8 @@ def simulate_decode(WST, ASW, TSW, DQ, stages, seed, max_steps=400_000):
                     accfull[w][buf].arrive()
             groups = [(0, 2), (2, 2)] if nb == WKB else [(b, 1) for b in range(nb)]
             for gi, (b0, cnt) in enumerate(groups):
-                for h in range(cnt):                # every block of the group
-                    cl = c + h
-                    yield from wait(tfull[w][cl % TSW], (cl // TSW) & 1)
+                cl = c + cnt - 1                    # the group's last block covers it
+                yield from wait(tfull[w][cl % TSW], (cl // TSW) & 1)
                 for h in range(cnt):
                     slot = (c + h) % TSW
                     if any(tmem[w][slot][q] != (j, b0 + h) for q in range(4)):
@@ -197,10 +196,9 @@ def simulate_decode(WST, ASW, TSW, DQ, stages, seed, max_steps=400_000):
             for gi, (b0, cnt) in enumerate(groups):
                 if smem_w[s] != j:
                     errors.append(f"warp {w}.{q}: weight slot {s} holds {smem_w[s]}, wanted {j}")
-                for h in range(cnt):            # every slot of the group is free
-                    cl = c + h
-                    if cl >= TSW:
-                        yield from wait(kfree[w][cl % TSW], ((cl // TSW) & 1) ^ 1)
+                cl = c + cnt - 1                # the later block's slot free covers both
+                if cl >= TSW:
+                    yield from wait(kfree[w][cl % TSW], ((cl // TSW) & 1) ^ 1)
                 yield
                 for h in range(cnt):
                     tmem[w][(c + h) % TSW][q] = None      # tcgen05.st in flight

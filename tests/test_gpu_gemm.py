@@ -305,3 +305,36 @@ def test_full_size_sampled(wl, si, M, weight_cache):
     c_ref = oracle_sampled(qw, a, rows, cols)
     r = oracle.max_err_ratio(c_values(C, rows, cols), c_ref, rel=TOL)
     assert r <= 1.0, r
+
+
+def test_alternating_problems_decode_kernel():
+    """Stale-data races hide when one problem is repeated: a slot read too early
+    returns the previous launch's identical data.  Two weights of one shape
+    (the second is the first with its tiles rotated by one) alternate, every
+    launch is compared bit for bit with the first launch of its problem, and
+    those first launches are checked against the oracle.  The shape and M
+    give every CTA a cut tile followed by whole tiles, where a failure showed."""
+    M, G = 32, 64
+    qw = synth.weight("sym_g64", 0)
+    a = synth.activations("sym_g64", 0, M)
+    roll = lambda x: np.ascontiguousarray(np.roll(x, 128, axis=1))
+    qw2 = synth.QuantWeight(roll(qw.q), roll(qw.scales), None, qw.group, qw.dtype)
+    A = binding.acts_to_device(a, torch.float16)
+    Ws = [packed_from(qw), packed_from(qw2)]
+    cols = sample_indices(qw.N, 160, seed=5)
+    rows = np.arange(M)
+    refs = [oracle_sampled(q, a, rows, cols) for q in (qw, qw2)]
+    for cfg in (dict(kernel="tc_decode", block_m=64, dq_warps=4),
+                dict(kernel="tc_decode", block_m=32, dq_warps=8),
+                dict(kernel="tc_decode", block_m=16, dq_warps=8)):
+        first = []
+        for i in range(2):
+            C = gemm_poisoned(A, Ws[i], config=cfg)
+            torch.cuda.synchronize()
+            assert oracle.max_err_ratio(c_values(C, rows, cols), refs[i], rel=TOL) <= 1.0, (cfg, i)
+            first.append(C.view(torch.int16).clone())
+        for r in range(40):
+            C = gemm_poisoned(A, Ws[r % 2], config=cfg)
+            torch.cuda.synchronize()
+            assert torch.equal(C.view(torch.int16), first[r % 2]), (cfg, r)
+        binding.poll_error()

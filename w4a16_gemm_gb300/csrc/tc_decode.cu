@@ -358,14 +358,12 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
         }
         const int nb = min(WKB, KB - pos.s * WKB);
         if (nb == WKB) {
-          // a full stage arrives in pairs: two waits (each a single try_wait
-          // once the pair is published) and one fence per eight MMAs
+          // a full stage arrives in pairs: one wait (the pair's second block
+          // is published after its first) and one fence per eight MMAs
 #pragma unroll
           for (int b = 0; b < WKB; b += 2, c += 2) {
             const unsigned s0 = c & (TSW - 1), s1 = (c + 1) & (TSW - 1);
-            if (!mbar_wait_bounded(tfull_bar + wg * TSW + s0, (c / TSW) & 1u, p.limit_ns,
-                                   abort_flag, p.err, SITE_MMA_AFULL, j * WKB + b, TMW4_SPIN(3)) ||
-                !mbar_wait_bounded(tfull_bar + wg * TSW + s1, ((c + 1) / TSW) & 1u, p.limit_ns,
+            if (!mbar_wait_bounded(tfull_bar + wg * TSW + s1, ((c + 1) / TSW) & 1u, p.limit_ns,
                                    abort_flag, p.err, SITE_MMA_AFULL, j * WKB + b, TMW4_SPIN(3))) {
               ok = false;
               break;
@@ -585,19 +583,20 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
       tmem_st_16(ta, d0);
       tmem_st_16(ta + 16, d1);
     };
-    // before writing block `cl`'s slot: the MMAs of block cl - TSW retired.
-    // One thread issues the warpgroup's MMAs and its commits complete in
-    // order, so waiting for the later block of a pair would cover the earlier
-    // one; both are waited for all the same (one try_wait when done), which
-    // keeps every slot reuse explicit.
+    // before writing block `cl`'s slot: the MMAs of block cl - TSW retired
+    // (one thread issues the warpgroup's MMAs, so its commits complete in
+    // order and this also covers every earlier block)
     auto slot_free = [&](unsigned cl, int step) -> bool {
       if (cl < static_cast<unsigned>(TSW)) return true;
       return mbar_wait_all(my_kfree + (cl & (TSW - 1)), ((cl / TSW) & 1u) ^ 1u, p.limit_ns,
                            abort_flag, p.err, SITE_DQ_AEMPTY, step, TMW4_SPIN(5));
     };
-    // the weight stage `ws` is no longer read by this warp: order its shared-
-    // memory reads before the copy that will refill it (generic to async
-    // proxy), then arrive on the stage's empty barrier
+    // the weight stage `ws` is no longer needed by this warp: its data has
+    // been dequantized and stored, and a generic-to-async proxy fence orders
+    // the warp's shared-memory reads of it before the bulk copy that will
+    // refill it; then arrive on the stage's empty barrier.  (Releasing the
+    // stage as soon as its last block was in registers, without the fence,
+    // let a refill corrupt a warp's weights now and then.)
     auto release_stage = [&](int ws_) {
       fence_proxy_async_smem();
       __syncwarp();
@@ -637,8 +636,7 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
             v[h][1] = *reinterpret_cast<const uint4 *>(src + 1024);
             read_scale_zero(st, sc_off[2 * pr + h], zp_off[2 * pr + h], s2[h], zm2[h]);
           }
-          if (!slot_free(c + 2 * pr, j * WKB + 2 * pr) ||
-              !slot_free(c + 2 * pr + 1, j * WKB + 2 * pr)) {
+          if (!slot_free(c + 2 * pr + 1, j * WKB + 2 * pr)) {
             ok = false;
             break;
           }
