@@ -3,8 +3,8 @@
  *
  * The library implements the mixed-precision GEMM pipeline of the TurboMind
  * engine ("Efficient Mixed-Precision Large Language Model Inference with
- * TurboMind", arXiv 2508.15601; abstract: a GEMM pipeline made of "offline
- * weight packing" and "online acceleration"):
+ * TurboMind", arXiv 2508.15601; abstract: a GEMM pipeline in two parts, an
+ * offline packing of the weights and an accelerated online multiply):
  *
  *   offline:  tm_pack_w4     int4 codes + scales + zeros -> packed weight
  *   online:   tm_gemm_w4a16  C[M,N] = A[M,K] * W[K,N],
@@ -122,7 +122,7 @@ typedef struct {
 tm_status tm_pack_w4(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N,
                      int group, tm_dtype dtype, void *stream, tm_packed **out);
 
-/* Online GEMM (TurboMind paper, arXiv abstract: "online acceleration";
+/* Online GEMM (TurboMind paper, arXiv abstract: the online half of the pipeline;
  * pith.science review, Figure 9: dequantization overlapped with the MMA).
  *   A  device, [M][K] values of the handle's dtype, 16-byte aligned
  *   W  packed weight from tm_pack_w4 with matching K and N

@@ -3,10 +3,10 @@
 Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this module.  It shares no code with the CUDA path.
 
-What the method computes (TurboMind paper, arXiv abstract: the GEMM pipeline
-is "offline weight packing + online acceleration" of a mixed-precision
-matrix multiply; pith.science review, Figure 6: runtime I2F conversion and
-scaling of the packed low-bit values before the MMA):
+What the method computes (TurboMind paper, arXiv abstract: a mixed-precision
+matrix multiply whose weights are packed once offline and consumed by an
+accelerated online kernel; pith.science review, Figure 6: runtime I2F
+conversion and scaling of the packed low-bit values before the MMA):
 
     W[k, n] = RNE_T( s[g, n] * (q[k, n] - z[g, n]) ),   g = k // G
     C       = A @ W            (accumulated exactly here, in float64)
