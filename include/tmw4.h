@@ -181,8 +181,9 @@ tm_status tm_select(const tm_packed *W, int M, tm_config *out);
 /* Variant selection by measured throughput (the pages give no selection
  * rule; it follows from the measured crossover between the GEMV and
  * tensor-core kernels).  Times every legal variant for each M in Ms[0..nM)
- * with CUDA events on `stream` (synchronises it), flushing L2 between
- * timings, and records the fastest (ties: lowest index) in the process-wide
+ * with CUDA events on `stream` (synchronises it): the median of seven
+ * single launches, each after an L2 flush.  Records the fastest (ties:
+ * lowest index) in the process-wide
  * table used by tm_gemm_w4a16.  If the environment variable TM_TUNE_CACHE
  * names a file, the table is saved there.  best_out (host, may be NULL)
  * receives nM configs. */

@@ -835,9 +835,11 @@ extern "C" tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *st
       // warm-up (also sizes the workspace)
       s = run_gemm(A, W, C, M, c, st);
       if (s != TM_OK) continue;
-      float times[3];
+      // median of kTuneReps single launches, each after an L2 flush
+      constexpr int kTuneReps = 7;
+      float times[kTuneReps];
       bool good = true;
-      for (int r = 0; r < 3 && good; ++r) {
+      for (int r = 0; r < kTuneReps && good; ++r) {
         cudaMemsetAsync(flush, r, flush_bytes, st);
         cudaEventRecord(e0, st);
         good = run_gemm(A, W, C, M, c, st) == TM_OK;
@@ -846,8 +848,8 @@ extern "C" tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *st
         cudaEventElapsedTime(&times[r], e0, e1);
       }
       if (!good) continue;
-      std::sort(times, times + 3);
-      const double us = times[1] * 1000.0;
+      std::sort(times, times + kTuneReps);
+      const double us = times[kTuneReps / 2] * 1000.0;
       if (us < best_us) {
         best_us = us;
         best = c;
