@@ -66,6 +66,26 @@ def problem_bytes(M: int, K: int, N: int, group: int, symmetric: bool) -> float:
     return weight_bytes(K, N, group, symmetric) + 2.0 * M * K + 2.0 * M * N
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (a job takes as long as its
+    slowest rank).  device: where the reduction tensor lives (the GPU for
+    NCCL, None for gloo)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: every rank processes units_per_rank (weak
+    scaling), all ranks together in `seconds` (the slowest rank's time)."""
+    return world * units_per_rank / seconds
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a16_gemm_gb300", "csrc")
@@ -307,11 +327,8 @@ def run_ours(args, rank: int, world: int):
     # whole-job numbers
     wbytes_step = sum(weight_bytes(*shapes[si], wl.group, wl.symmetric) for si, M in problems)
     flops_step = sum(2.0 * M * shapes[si][0] * shapes[si][1] for si, M in problems)
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
-    value = world * K_steps * wbytes_step / elapsed / 1e9
+    elapsed = max_over_ranks(elapsed, world, dev)
+    value = job_rate(K_steps * wbytes_step, world, elapsed) / 1e9
     ms_per_step = elapsed / K_steps * 1e3
 
     # end to end through the public API with host buffers (pinned), copies timed
@@ -338,8 +355,8 @@ def run_ours(args, rank: int, world: int):
                 c_host[(si, M)].copy_(outs[(si, M)], non_blocking=True)
         e1.record(stream)
         stream.synchronize()
-    e2e_s = e0.elapsed_time(e1) * 1e-3
-    e2e_value = world * e_steps * wbytes_step / e2e_s / 1e9
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, dev)
+    e2e_value = job_rate(e_steps * wbytes_step, world, e2e_s) / 1e9
 
     peaks, peak_src = load_peaks()
     roof = None
