@@ -364,14 +364,28 @@ def run_ours(args, rank: int, world: int):
         dom = max(per, key=lambda k: per[k][0])
         tot_s, tot_b, n_l = per[dom]
         achieved = tot_b / tot_s / 1e9
+        # measured DRAM bytes per launch of the dominant kernel: the mean over
+        # this run's problems that ran with it, each captured once with the
+        # same kernel sources and variant; null if any is missing
         traffic = None
         tp = os.path.join(ROOT, "profiles", "traffic.json")
         if os.path.exists(tp):
             with open(tp) as f:
                 tj = json.load(f)
             ent = tj.get(WORKLOAD, {})
-            if ent.get("source_hash") == kernel_source_hash() and ent.get("kernel") == dom:
-                traffic = ent.get("dram_bytes_per_launch")
+            if ent.get("source_hash") == kernel_source_hash():
+                rec = {(x["case"], x.get("variant")): x["dram_read"] + x["dram_write"]
+                       for x in ent.get("per_problem", [])}
+                mine = []
+                for si, M in problems:
+                    v = variants[(si, M)]
+                    if variant_name(v) != dom:
+                        continue
+                    key = (f"{shapes[si][0]},{shapes[si][1]},{M}",
+                           f"{v['kernel']}:{v['block_m']}:{v['split_k']}:{v['dq_warps']}")
+                    mine.append(rec.get(key))
+                if mine and all(x is not None for x in mine):
+                    traffic = round(sum(mine) / len(mine))
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "kernel": dom, "launches": n_l, "avg_launch_us": round(tot_s / n_l * 1e6, 3),
