@@ -86,6 +86,22 @@ def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
     return world * units_per_rank / seconds
 
 
+def recorded_traffic(ent: dict, source_hash: str, ran: list) -> int | None:
+    """Measured DRAM bytes per launch of the dominant kernel: the mean of the
+    recorded captures of the problems that ran with it, ran = [(K, N, M,
+    variant dict)], each captured with the same kernel sources and variant.
+    None if the sources changed or any problem has no capture."""
+    if not ran or ent.get("source_hash") != source_hash:
+        return None
+    rec = {(x["case"], x.get("variant")): x["dram_read"] + x["dram_write"]
+           for x in ent.get("per_problem", [])}
+    got = [rec.get((f"{K},{N},{M}", f"{v['kernel']}:{v['block_m']}:{v['split_k']}:{v['dq_warps']}"))
+           for K, N, M, v in ran]
+    if any(x is None for x in got):
+        return None
+    return round(sum(got) / len(got))
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a16_gemm_gb300", "csrc")
@@ -364,28 +380,14 @@ def run_ours(args, rank: int, world: int):
         dom = max(per, key=lambda k: per[k][0])
         tot_s, tot_b, n_l = per[dom]
         achieved = tot_b / tot_s / 1e9
-        # measured DRAM bytes per launch of the dominant kernel: the mean over
-        # this run's problems that ran with it, each captured once with the
-        # same kernel sources and variant; null if any is missing
         traffic = None
         tp = os.path.join(ROOT, "profiles", "traffic.json")
         if os.path.exists(tp):
             with open(tp) as f:
-                tj = json.load(f)
-            ent = tj.get(WORKLOAD, {})
-            if ent.get("source_hash") == kernel_source_hash():
-                rec = {(x["case"], x.get("variant")): x["dram_read"] + x["dram_write"]
-                       for x in ent.get("per_problem", [])}
-                mine = []
-                for si, M in problems:
-                    v = variants[(si, M)]
-                    if variant_name(v) != dom:
-                        continue
-                    key = (f"{shapes[si][0]},{shapes[si][1]},{M}",
-                           f"{v['kernel']}:{v['block_m']}:{v['split_k']}:{v['dq_warps']}")
-                    mine.append(rec.get(key))
-                if mine and all(x is not None for x in mine):
-                    traffic = round(sum(mine) / len(mine))
+                ent = json.load(f).get(WORKLOAD, {})
+            ran = [(shapes[si][0], shapes[si][1], M, variants[(si, M)]) for si, M in problems
+                   if variant_name(variants[(si, M)]) == dom]
+            traffic = recorded_traffic(ent, kernel_source_hash(), ran)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "kernel": dom, "launches": n_l, "avg_launch_us": round(tot_s / n_l * 1e6, 3),

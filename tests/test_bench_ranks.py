@@ -59,3 +59,20 @@ def test_single_rank_is_the_identity():
 
     assert bench.max_over_ranks(1.25, 1) == 1.25
     assert bench.job_rate(10.0, 1, 2.0) == 5.0
+
+
+def test_recorded_traffic_matches_problems_and_sources():
+    import bench
+
+    ent = {"source_hash": "abc", "per_problem": [
+        {"case": "4096,6144,16", "variant": "tc_decode:16:1:8", "dram_read": 100.0, "dram_write": 4.0},
+        {"case": "4096,4096,16", "variant": "tc_decode:16:1:8", "dram_read": 60.0, "dram_write": 0.0},
+    ]}
+    v8 = dict(kernel="tc_decode", block_m=16, split_k=1, dq_warps=8)
+    v12 = dict(v8, dq_warps=12)
+    both = [(4096, 6144, 16, v8), (4096, 4096, 16, v8)]
+    assert bench.recorded_traffic(ent, "abc", both) == 82
+    assert bench.recorded_traffic(ent, "other", both) is None          # sources changed
+    assert bench.recorded_traffic(ent, "abc", [(4096, 6144, 16, v12)]) is None   # another variant
+    assert bench.recorded_traffic(ent, "abc", both + [(4096, 28672, 16, v8)]) is None  # not captured
+    assert bench.recorded_traffic(ent, "abc", []) is None
