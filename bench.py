@@ -1,17 +1,27 @@
 """Benchmark of the W4A16 GEMM hot path on one GB300 (or N replicas).
 
-One step = the whole decode-shaped sweep of an 8B-class decoder layer: the
-four layer shapes (K, N) = (4096, 6144), (4096, 4096), (4096, 28672),
-(14336, 4096) times M in {1, 4, 16}, asymmetric int4, group 128, fp16
-activations and output, fp32 accumulation: 12 GEMM launches through the
-C-ABI library, with the packed weights (offline repack, timed separately)
+Headline (``value``): one step = the whole decode-shaped sweep of an 8B-class
+decoder layer: the four layer shapes (K, N) = (4096, 6144), (4096, 4096),
+(4096, 28672), (14336, 4096) times M in {1, 4, 16}, asymmetric int4, group
+128, fp16 activations and output, fp32 accumulation: 12 GEMM launches through
+the C-ABI library, with the packed weights (offline repack, timed separately)
 and the activations resident in HBM.  Weight copies are rotated so that no
-launch finds its weights in L2 (distinct weight bytes per step exceed the
-L2 size; even and odd steps use disjoint copy sets).
+launch finds its weights in L2 (distinct weight bytes per step exceed the L2
+size; even and odd steps use disjoint copy sets).  All timed steps are one
+CUDA graph timed with CUDA events on the launch stream.
+
+Per-config block (``configs``): every (shape, M) problem of the decode,
+prefill, 70B-class and symmetric-G64 workloads, each timed on its own as a
+CUDA graph of 50 launches over rotated weight copies (more than 3x the L2),
+replayed 10 times (median and min), with TFLOP/s, weight GB/s and the
+fraction of the roofline that bounds it (HBM on the algorithmic bytes for
+small M, the dense 16-bit tensor-core peak for large M, the larger of the two
+times in between).  The dominant kernel's ``roofline`` entry uses these
+per-problem times.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (numpy dequant + float64 matmul) on the host cores on a column sample of the
-same workload instead.
+decode workload instead.
 """
 
 from __future__ import annotations
@@ -30,6 +40,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "decode_8b"
+CONFIG_WORKLOADS = ("decode_8b", "prefill_8b", "class_70b", "sym_g64")
+GRAPH_LAUNCHES = 50      # launches per per-problem graph
+GRAPH_REPEATS = 10       # timed replays per problem (median and min)
 
 
 def parse():
@@ -51,6 +64,10 @@ def parse():
     ap.add_argument("--variant", type=str, default=None,
                     help="with --case: kernel:block_m:split_k:dq_warps (default: tuned/auto)")
     ap.add_argument("--reps", type=int, default=6, help="with --case: launches")
+    ap.add_argument("--configs", type=str, default=",".join(CONFIG_WORKLOADS),
+                    help="workloads of the per-problem block ('' to skip it)")
+    ap.add_argument("--config-cpu-seconds", type=float, default=1.0,
+                    help="CPU time of the oracle sample per shape in the per-config block")
     return ap.parse_args()
 
 
@@ -192,6 +209,157 @@ class ClockSampler:
                 "samples": len(rows), "samples_under_load": len(loaded)}
 
 
+# ------------------------------------------------------- per-problem timing
+def roofline_terms(M: int, K: int, N: int, group: int, symmetric: bool, seconds: float,
+                   peaks: dict) -> dict:
+    """Roofline of one GEMM: t_hbm = algorithmic bytes / HBM peak, t_tc =
+    2MNK / 16-bit tensor-core peak (burst: each problem is timed on its own);
+    frac = max(t_hbm, t_tc) / measured time.  bound: 'hbm' for M <= 16,
+    'tensor' for M >= 2048, 'both' in between (both fractions reported)."""
+    t_hbm = problem_bytes(M, K, N, group, symmetric) / (peaks["hbm_gbs"] * 1e9)
+    t_tc = 2.0 * M * N * K / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if M <= 16 else "tensor" if M >= 2048 else "both"
+    return {"bound": bound, "frac_hbm": round(t_hbm / seconds, 4), "frac_tc": round(t_tc / seconds, 4),
+            "frac": round(max(t_hbm, t_tc) / seconds, 4)}
+
+
+def graph_time(launch, stream, launches: int, repeats: int) -> list[float]:
+    """Seconds per launch of `launch(i)`, i = 0..launches-1, captured in one
+    CUDA graph and replayed `repeats` times (CUDA events on the launch stream)."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            launch(i)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(launches):
+            launch(i)
+    out = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        stream.synchronize()
+        for _ in range(repeats):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            out.append(e0.elapsed_time(e1) * 1e-3 / launches)
+    del g
+    return out
+
+
+def variant_name(v: dict, dtype: str = "f16") -> str:
+    if v["kernel"] == "gemv":
+        return f"gemv_kernel<{dtype},{v['block_m']}>"
+    if v["kernel"] == "decode_mma":
+        return f"decode_mma_kernel<{dtype},{v['block_m'] // 16}>"
+    if v["kernel"] == "tc_decode":
+        return f"tc_decode_kernel<{dtype},{v['block_m']},{v['dq_warps']}>"
+    return f"tc_gemm_kernel<{dtype},{v['block_m']},{v['dq_warps']}>"
+
+
+def oracle_problem_seconds(qw, a_bits, M: int, budget_s: float) -> tuple[float, str]:
+    """CPU oracle time of one full (M, K, N) problem, measured on a column
+    sample (all K) and a row sample and extrapolated linearly: dequant time
+    scales with the columns, the float64 matmul with rows x columns."""
+    import numpy as np
+
+    import oracle
+
+    K, N = qw.q.shape
+    rows = min(M, 64)
+    ncols = 128
+    while True:
+        cols = slice(0, ncols)
+        z = None if qw.zeros is None else qw.zeros[:, cols]
+        t0 = time.perf_counter()
+        w = oracle.dequant_bits(qw.q[:, cols], qw.scales[:, cols], z, qw.group, qw.dtype)
+        t1 = time.perf_counter()
+        oracle.gemm_ref(a_bits[:rows], w, qw.dtype)
+        t2 = time.perf_counter()
+        if t2 - t0 >= budget_s / 4 or ncols >= N:
+            break
+        ncols = min(N, ncols * 4)
+    full = (t1 - t0) * (N / ncols) + (t2 - t1) * (M / rows) * (N / ncols)
+    kind = "measured" if (ncols >= N and rows >= M) else "extrapolated"
+    return full, f"{kind} from {rows} rows x {ncols} columns"
+
+
+def config_sweep(wl_name: str, dev, stream, peaks: dict, tune: bool, cpu_budget_s: float) -> dict:
+    """Times every (shape, M) of one workload as a graph of GRAPH_LAUNCHES
+    launches over rotated weight copies; the CPU oracle on a bounded sample
+    of each problem beside it."""
+    import math
+
+    import torch
+
+    from w4a16_gemm_gb300 import binding, synth
+
+    wl = synth.WORKLOADS[wl_name]
+    dt = torch.float16 if wl.dtype == "f16" else torch.bfloat16
+    L2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    problems = []
+    cpu_s_total, cpu_notes = 0.0, []
+    for si, (K, N) in enumerate(wl.shapes):
+        qw = synth.weight(wl_name, si)
+        p = binding.to_device(qw, dev)
+        wb = weight_bytes(K, N, wl.group, wl.symmetric)
+        R = min(64, math.ceil(3 * L2 / wb) + 1)
+        Ws = [binding.pack(p.q, p.scales, p.zeros, qw.group) for _ in range(R)]
+        del p
+        if tune:
+            binding.tune(Ws[0], list(wl.ms))
+        for M in wl.ms:
+            a = synth.activations(wl_name, si, M)
+            A = binding.acts_to_device(a, dt, dev)
+            C = torch.empty((M, N), dtype=dt, device=dev)
+            v = binding.select(Ws[0], M)
+            ts = graph_time(lambda i: binding.gemm(A, Ws[i % R], out=C, stream=stream), stream,
+                            GRAPH_LAUNCHES, GRAPH_REPEATS)
+            binding.poll_error(stream)
+            t_med, t_min = statistics.median(ts), min(ts)
+            rec = {"K": K, "N": N, "M": M, "variant": v, "kernel": variant_name(v, wl.dtype),
+                   "us": round(t_med * 1e6, 3), "us_min": round(t_min * 1e6, 3),
+                   "tflops": round(2.0 * M * N * K / t_med / 1e12, 2),
+                   "weight_gbs": round(wb / t_med / 1e9, 1),
+                   "bytes": problem_bytes(M, K, N, wl.group, wl.symmetric)}
+            rec.update(roofline_terms(M, K, N, wl.group, wl.symmetric, t_med, peaks))
+            if cpu_budget_s > 0:
+                t_cpu, how = oracle_problem_seconds(qw, a, M, cpu_budget_s)
+                rec["cpu_oracle_s"] = round(t_cpu, 3)
+                cpu_s_total += t_cpu
+                cpu_notes.append(how)
+            problems.append(rec)
+            del A, C
+        for w in Ws:
+            w.free()
+        del Ws, qw
+        torch.cuda.synchronize()
+    t_gpu = sum(r["us"] for r in problems) * 1e-6
+    flops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in problems)
+    wbytes = sum(weight_bytes(r["K"], r["N"], wl.group, wl.symmetric) for r in problems)
+    out = {"problems": problems,
+           "tflops": round(flops / t_gpu / 1e12, 2), "weight_gbs": round(wbytes / t_gpu / 1e9, 1),
+           "seconds_per_pass": round(t_gpu, 6)}
+    for bound in ("hbm", "tensor", "both"):
+        fr = [r["frac"] for r in problems if r["bound"] == bound]
+        if fr:
+            out[f"frac_{bound}_min"] = min(fr)
+            out[f"frac_{bound}_median"] = round(statistics.median(fr), 4)
+    if cpu_budget_s > 0:
+        extrap = any("extrapolated" in n for n in cpu_notes)
+        out["cpu_baseline"] = {
+            "value": round(flops / cpu_s_total / 1e12, 6), "unit": "TFLOP/s",
+            "weight_gbs": round(wbytes / cpu_s_total / 1e9, 4), "cores": cpu_cores(), "kind": "oracle",
+            "sample": ("extrapolated: " if extrap else "") +
+                      "per problem, numpy dequant (RNE) of a column sample over all K and a float64 "
+                      "matmul of a row sample, scaled linearly to the full problem"}
+    return out
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank: int, world: int):
     import numpy as np
@@ -246,23 +414,12 @@ def run_ours(args, rank: int, world: int):
 
     variants = {(si, M): binding.select(packed[(0, si, M)], M) for si, M in problems}
 
-    def variant_name(v):
-        if v["kernel"] == "gemv":
-            return f"gemv_kernel<f16,{v['block_m']}>"
-        if v["kernel"] == "tc_decode":
-            return f"tc_decode_kernel<f16,{v['block_m']},{v['dq_warps']}>"
-        return f"tc_gemm_kernel<f16,{v['block_m']},{v['dq_warps']}>"
-
     stream = torch.cuda.Stream(device=dev)
 
-    def launch_step(step: int, events=None):
+    def launch_step(step: int):
         s = step % n_sets
-        for j, (si, M) in enumerate(problems):
-            if events is not None:
-                events[j][0].record(stream)
+        for si, M in problems:
             binding.gemm(acts[(si, M)], packed[(s, si, M)], out=outs[(si, M)], stream=stream)
-            if events is not None:
-                events[j][1].record(stream)
 
     # warm-up (also sizes the split-K workspace of this stream outside capture)
     with torch.cuda.stream(stream):
@@ -272,26 +429,12 @@ def run_ours(args, rank: int, world: int):
     binding.poll_error(stream)
 
     K_steps = args.steps
-    # graph A: all K timed steps back to back (the `value` timing)
+    # all K timed steps back to back in one graph (the `value` timing)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for k in range(K_steps):
             launch_step(k)
-    # graph B: the same K steps with a timing-event pair around every launch
-    # (event record nodes), for per-kernel durations
-    external_ok = True
-    try:
-        ev = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-               for _ in problems] for _ in range(K_steps)]
-        graph_ev = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_ev, stream=stream):
-            for k in range(K_steps):
-                launch_step(k, ev[k])
-    except (TypeError, RuntimeError):
-        external_ok = False
-        ev = None
-        graph_ev = None
-    # clock-sampled warm replays, then the timed replays
+    # clock-sampled warm replays, then the timed replay
     sampler = ClockSampler(gpu_id(dev))
     sampler.start()
     # graphs replay on the current stream: make it the launch stream
@@ -317,28 +460,9 @@ def run_ours(args, rank: int, world: int):
         if world > 1:
             torch.distributed.barrier()
         elapsed = t0.elapsed_time(t1) * 1e-3
-        ev_elapsed = None
-        if graph_ev is not None:
-            t0.record(stream)
-            graph_ev.replay()
-            t1.record(stream)
-            torch.cuda.synchronize()
-            ev_elapsed = t0.elapsed_time(t1) * 1e-3
     clocks = sampler.stop()
     binding.poll_error(stream)
-
-    # per-launch durations
-    per = {}   # variant -> [total seconds, total algorithmic bytes, launches]
-    if external_ok:
-        for k in range(K_steps):
-            for j, (si, M) in enumerate(problems):
-                d = ev[k][j][0].elapsed_time(ev[k][j][1]) * 1e-3
-                K, N = shapes[si]
-                vname = variant_name(variants[(si, M)])
-                rec = per.setdefault(vname, [0.0, 0.0, 0])
-                rec[0] += d
-                rec[1] += problem_bytes(M, K, N, wl.group, wl.symmetric)
-                rec[2] += 1
+    del graph
 
     # whole-job numbers
     wbytes_step = sum(weight_bytes(*shapes[si], wl.group, wl.symmetric) for si, M in problems)
@@ -373,38 +497,47 @@ def run_ours(args, rank: int, world: int):
         stream.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, dev)
     e2e_value = job_rate(e_steps * wbytes_step, world, e2e_s) / 1e9
+    for w in packed.values():
+        w.free()
+    del packed, acts, outs, a_dev, a_host, c_host
+    torch.cuda.synchronize()
 
+    # per-problem block: every (shape, M) of each workload, graph of 50 launches each
     peaks, peak_src = load_peaks()
+    configs = {}
+    for name in [x for x in args.configs.split(",") if x]:
+        configs[name] = config_sweep(name, dev, stream, peaks, tune=not args.no_tune,
+                                     cpu_budget_s=args.config_cpu_seconds if rank == 0 else 0.0)
+
+    # roofline of the dominant kernel of the headline step: the variant with the
+    # most time per step, from the per-problem graph timings of the decode sweep
     roof = None
-    if per:
+    dec = configs.get(WORKLOAD)
+    if dec is not None:
+        per = {}
+        for r in dec["problems"]:
+            rec = per.setdefault(r["kernel"], [0.0, 0.0, 0, []])
+            rec[0] += r["us"] * 1e-6
+            rec[1] += r["bytes"]
+            rec[2] += 1
+            rec[3].append((r["K"], r["N"], r["M"], r["variant"]))
         dom = max(per, key=lambda k: per[k][0])
-        tot_s, tot_b, n_l = per[dom]
+        tot_s, tot_b, n_l, ran = per[dom]
         achieved = tot_b / tot_s / 1e9
         traffic = None
         tp = os.path.join(ROOT, "profiles", "traffic.json")
         if os.path.exists(tp):
             with open(tp) as f:
                 ent = json.load(f).get(WORKLOAD, {})
-            ran = [(shapes[si][0], shapes[si][1], M, variants[(si, M)]) for si, M in problems
-                   if variant_name(variants[(si, M)]) == dom]
             traffic = recorded_traffic(ent, kernel_source_hash(), ran)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "kernel": dom, "launches": n_l, "avg_launch_us": round(tot_s / n_l * 1e6, 3),
+                "kernel": dom, "problems": n_l, "avg_launch_us": round(tot_s / n_l * 1e6, 3),
                 "algorithmic_bytes_per_launch": round(tot_b / n_l),
+                "duration_source": f"median of {GRAPH_REPEATS} replays of a CUDA graph of "
+                                   f"{GRAPH_LAUNCHES} launches per problem (rotated weight copies)",
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                 else "fallback 6.8 TB/s"}
-    per_problem = None
-    if external_ok:
-        per_problem = []
-        for j, (si, M) in enumerate(problems):
-            ds = [ev[k][j][0].elapsed_time(ev[k][j][1]) * 1e-3 for k in range(K_steps)]
-            d = statistics.median(ds)
-            K, N = shapes[si]
-            per_problem.append({"K": K, "N": N, "M": M, "variant": variants[(si, M)],
-                                "us": round(d * 1e6, 2),
-                                "weight_gbs": round(weight_bytes(K, N, wl.group, wl.symmetric) / d / 1e9, 1),
-                                "tflops": round(2.0 * M * K * N / d / 1e12, 3)})
 
     line = {
         "metric": "W4A16 GEMM weight GB/s, 8B-class decode sweep (4 layer shapes x M in {1,4,16})",
@@ -425,12 +558,13 @@ def run_ours(args, rank: int, world: int):
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
                 "how": "eager C-ABI calls via the Python binding; A copied from pinned host, C copied back, every call"},
         "gpu_launches": K_steps * len(problems),
-        "ms_per_step_event_graph": None if ev_elapsed is None else round(ev_elapsed / K_steps * 1e3, 4),
         "clocks": clocks,
         "pack": {"seconds_per_shape": {f"{shapes[si][0]}x{shapes[si][1]}": round(t * 1e6, 1)
                                        for si, t in pack_times.items()},
                  "unit": "us", "note": "offline repack (tm_pack_w4), timed once per shape"},
-        "per_problem": per_problem,
+        "variants": {f"{shapes[si][0]}x{shapes[si][1]}xM{M}": variants[(si, M)] for si, M in problems},
+        "configs": configs,
+        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "tensor_tflops": peaks["bf16_tflops"], "source": peak_src},
     }
     return line
 

@@ -59,8 +59,13 @@ enum {
   TM_KERNEL_AUTO = 0,     /* pick from the tuned table, else the built-in rule */
   TM_KERNEL_GEMV = 1,     /* CUDA-core split-K GEMV, M <= 8                    */
   TM_KERNEL_TC = 2,       /* tcgen05/TMEM kernel, weights staged by TMA        */
-  TM_KERNEL_TC_DECODE = 3 /* tcgen05/TMEM kernel for small M (block_m 16..64),
-                             weights streamed from HBM straight into registers */
+  TM_KERNEL_TC_DECODE = 3, /* tcgen05/TMEM kernel for small M (block_m 16..64):
+                              persistent stream-K grid, weights staged in shared
+                              memory by bulk copies, dequantized into TMEM */
+  TM_KERNEL_DECODE_MMA = 4 /* split-K streaming kernel for M <= 32: weights
+                              loaded straight into registers, dequantized there
+                              and multiplied by register-operand tensor-core
+                              MMAs (mma.sync), group scale applied in fp32 */
 };
 
 /* A kernel variant: family, rows of A per CTA tile (TC: 16, 32, 64, 128 or
@@ -144,10 +149,10 @@ tm_status tm_gemm_w4a16(const void *A, const tm_packed *W, void *C, int M, int N
 tm_status tm_gemm_w4a16_ex(const void *A, const tm_packed *W, void *C, int M, int N, int K,
                            const tm_config *cfg, void *stream);
 
-/* As tm_gemm_w4a16, for callers that cannot allocate device memory (an
- * application that owns all GPU memory through its own pool, or a stream
- * being captured when tm_gemm_w4a16's workspace would have to grow).  The
- * paper has no counterpart; this is a deployment variant of the same GEMM.
+/* As tm_gemm_w4a16, for callers that cannot allocate device memory: an
+ * application that owns all GPU memory through its own pool allocator and
+ * forbids allocations behind its back.  The paper has no counterpart; this
+ * is a deployment variant of the same GEMM.
  *   Allocates nothing: no cudaMalloc/cudaFree and no allocating library
  *   call.  Split-K partials and arrival counters live in static device
  *   arrays of the library (8 MiB of partials and 16384 counters, held on
@@ -160,8 +165,9 @@ tm_status tm_gemm_w4a16_ex(const void *A, const tm_packed *W, void *C, int M, in
  *   contents: calls that overlap on the GPU (different streams, or
  *   different host threads) race and give wrong results; order them.
  *   Each call clears the counters it uses with cudaMemsetAsync on `stream`.
- *   A bounded wait that gives up is recorded in a static device word that
- *   tm_poll_error does not read; C is then undefined. */
+ *   A bounded wait that gives up is recorded in a static device word of
+ *   its own, which tm_poll_error reads and clears together with the
+ *   regular error word (C of that call is then undefined). */
 tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, void *C, int M, int N, int K,
                                 void *stream);
 
@@ -175,18 +181,30 @@ tm_status tm_packed_free(tm_packed *W, void *stream);
 /* Fills *info (host) with the handle's shape and device pointers. */
 tm_status tm_packed_get(const tm_packed *W, tm_packed_info *info);
 
-/* The variant tm_gemm_w4a16 would run for this handle and M (host only). */
+/* The variant tm_gemm_w4a16 would run for this handle and M (host only):
+ * the environment override TM_VARIANT="kernel:block_m:split_k:dq_warps"
+ * (kernel gemv, tc, tc_decode, decode_mma or its number) when it can run
+ * this shape, else the tuned table's entry for M's row bucket, else the
+ * built-in rule (measured crossovers: the register-MMA decode kernel for
+ * M <= 16, the tcgen05 decode kernel up to 64 rows, the tcgen05 kernel
+ * beyond). */
 tm_status tm_select(const tm_packed *W, int M, tm_config *out);
 
 /* Variant selection by measured throughput (the pages give no selection
- * rule; it follows from the measured crossover between the GEMV and
- * tensor-core kernels).  Times every legal variant for each M in Ms[0..nM)
- * with CUDA events on `stream` (synchronises it): the median of seven
- * single launches, each after an L2 flush.  Records the fastest (ties:
- * lowest index) in the process-wide
- * table used by tm_gemm_w4a16.  If the environment variable TM_TUNE_CACHE
- * names a file, the table is saved there.  best_out (host, may be NULL)
- * receives nM configs. */
+ * rule; it follows from the measured crossovers between the kernels).  For
+ * each M in Ms[0..nM), times every legal variant on `stream` (synchronises
+ * it) the way applications run them: a CUDA graph of back-to-back launches
+ * (programmatic dependent launch on) over rotated copies of the weight, so
+ * that no launch finds its weights in L2; the median of three replays.  The
+ * built-in choice is measured first and a later variant replaces the best so
+ * far only if it is at least 2% faster, which keeps picks stable under
+ * timing noise.  The winner is recorded in the process-wide table used by
+ * tm_gemm_w4a16 under the key (N, K, group, dtype, symmetric, row bucket),
+ * the row bucket being the next power of two >= M.  If the environment
+ * variable TM_TUNE_CACHE names a file, the table is saved there.  best_out
+ * (host, may be NULL) receives nM configs.  Allocates temporary device
+ * copies of the weight (at most 7) and frees them before returning.
+ * Deviation from the plain tm_tune(Ms, W, stream) signature: best_out. */
 tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *stream, tm_config *best_out);
 
 /* Pipeline geometry of the tcgen05 variant (block_m, dq_warps); host only,
@@ -223,8 +241,10 @@ tm_status tm_tune_load(const char *path);
 tm_status tm_tune_save(const char *path);
 
 /* Synchronises `stream`, then reads and clears the current device's error
- * word: TM_ERR_TIMEOUT if a bounded wait gave up, TM_ERR_INVALID_ARG if a
- * code byte was above 15, TM_OK otherwise. */
+ * words (the regular one and the static one of tm_gemm_w4a16_noalloc):
+ * TM_ERR_TIMEOUT if a bounded wait gave up, TM_ERR_INVALID_ARG if a code
+ * byte was above 15, TM_OK otherwise.  Allocates nothing after the first
+ * call on a device. */
 tm_status tm_poll_error(void *stream);
 
 /* Self-test of the bounded wait used by every kernel: launches one CTA

@@ -26,7 +26,6 @@ from .w4a16 import (  # noqa: F401
     dequant_bits,
     dequant_f64,
     gemm_ref,
-    gemm_ref_rows,
     pack_ref,
     unpack_ref,
     pack_scales_ref,

@@ -16,7 +16,7 @@ with q, z in [0, 15], s a 16-bit float of type T (fp16 or bf16) and A an
 most 11 significant bits, |q-z| at most 4), so RNE_T is the single rounding
 of the exact real product.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * logical weight W is [K, N], C = A @ W with A [M, K] and C [M, N], both
     row-major; scales/zeros are [K/G, N];
   * symmetric quantization has no stored zero and uses z = 8;
@@ -157,13 +157,6 @@ def gemm_ref(a_bits, w_bits, dtype: str) -> np.ndarray:
     GEMM tolerance.  C_ref is not rounded to 16 bits.
     """
     A = act_bits_to_f64(a_bits, dtype)
-    W = act_bits_to_f64(w_bits, dtype)
-    return A @ W
-
-
-def gemm_ref_rows(a_bits, w_bits, dtype: str, rows) -> np.ndarray:
-    """C_ref restricted to the given rows of A (for sampled checks)."""
-    A = act_bits_to_f64(np.asarray(a_bits)[np.asarray(rows)], dtype)
     W = act_bits_to_f64(w_bits, dtype)
     return A @ W
 

@@ -34,10 +34,22 @@ ILLEGAL = {(16, 16), (64, 16), (256, 16)}
 DECODE_ILLEGAL = {(64, 12), (64, 16)}   # 3-4 warpgroups leave too few TMEM columns at block_m 64
 
 
+def _decode_variants(M):
+    """Every legal tcgen05-decode variant and, for M <= 32, the register-MMA
+    decode kernel with and without split-K."""
+    out = [dict(kernel="tc_decode", block_m=bm, dq_warps=dq)
+           for bm in (16, 32, 64) for dq in (4, 8, 12, 16) if (bm, dq) not in DECODE_ILLEGAL]
+    if M <= 32:
+        out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=2)]
+    return out
+
+
 def _variants(M):
     out = []
     if M <= 8:
         out += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
+    if M <= 32:
+        out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=3)]
     for bm in (16, 32, 64, 128, 256):
         for sk in (1, 3):
             for dq in (4, 8, 16):
@@ -124,11 +136,16 @@ def test_q_equal_zero_gives_exact_zero(dt):
     qz = synth.QuantWeight(q, qw.scales, qw.zeros, G, dt)
     W = packed_from(qz)
     A = binding.acts_to_device(a, TORCH_DT[dt])
-    for cfg in [None, dict(kernel="gemv", split_k=2) if M <= 8 else None,
-                dict(kernel="tc", block_m=64, split_k=2)]:
+    A8 = A[:8].contiguous()
+    for cfg in [None, dict(kernel="tc", block_m=64, split_k=2)] + _decode_variants(M):
         C = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
-        assert torch.count_nonzero(C.float()) == 0
+        assert torch.count_nonzero(C.float()) == 0, cfg
+    for cfg in [dict(kernel="gemv", split_k=2), dict(kernel="decode_mma", split_k=4)]:
+        C = gemm_poisoned(A8, W, config=cfg)
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(C.float()) == 0, cfg
+    binding.poll_error()
 
 
 def test_one_hot_rows_reproduce_dequantized_weight():
@@ -141,15 +158,21 @@ def test_one_hot_rows_reproduce_dequantized_weight():
         a[i, k] = 0x3C00
     W = packed_from(qw)
     A = binding.acts_to_device(a, torch.float16)
-    for cfg in [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=4),
-                dict(kernel="tc", block_m=16, split_k=1), dict(kernel="tc", block_m=16, split_k=3),
+    for cfg in [dict(kernel="tc", block_m=16, split_k=1), dict(kernel="tc", block_m=16, split_k=3),
                 dict(kernel="tc", block_m=128, split_k=1, dq_warps=8),
-                dict(kernel="tc", block_m=32, split_k=5, dq_warps=8)]:
-        if cfg["kernel"] == "gemv" and len(ks) > 8:
-            continue
+                dict(kernel="tc", block_m=32, split_k=5, dq_warps=8),
+                dict(kernel="decode_mma", split_k=4)] + _decode_variants(len(ks)):
         C = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
         assert np.array_equal(bits_of(C), w[ks]), cfg
+    # the CUDA-core GEMV takes at most 8 rows: the last 8 one-hot rows
+    A8 = A[1:].contiguous()
+    for cfg in [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=4),
+                dict(kernel="decode_mma", split_k=1)]:
+        C = gemm_poisoned(A8, W, config=cfg)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits_of(C), w[ks[1:]]), cfg
+    binding.poll_error()
 
 
 def test_identity_activation_reproduces_weight():
@@ -160,10 +183,18 @@ def test_identity_activation_reproduces_weight():
     a = np.where(np.eye(K, dtype=bool), np.uint16(0x3C00), np.uint16(0))
     W = packed_from(qw)
     A = binding.acts_to_device(a, torch.float16)
-    for bm in (64, 128, 256):
-        C = gemm_poisoned(A, W, config=dict(kernel="tc", block_m=bm))
+    for cfg in [dict(kernel="tc", block_m=bm) for bm in (64, 128, 256)] + \
+            [c for c in _decode_variants(K) if c["kernel"] == "tc_decode"]:
+        C = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
-        assert np.array_equal(bits_of(C), w), bm
+        assert np.array_equal(bits_of(C), w), cfg
+    # the register-MMA decode kernel takes at most 32 rows: slabs of I
+    for k0 in (0, 96, 224):
+        for sk in (1, 2):
+            C = gemm_poisoned(A[k0:k0 + 32].contiguous(), W, config=dict(kernel="decode_mma", split_k=sk))
+            torch.cuda.synchronize()
+            assert np.array_equal(bits_of(C), w[k0:k0 + 32]), (k0, sk)
+    binding.poll_error()
 
 
 @pytest.mark.parametrize("M", [1, 5, 48, 300])
@@ -183,13 +214,16 @@ def test_power_of_two_scales_are_exact(M):
     W = packed_from(qw)
     A = binding.acts_to_device(a, torch.float16)
     cfgs = [None, dict(kernel="tc", block_m=16, split_k=4), dict(kernel="tc", block_m=64, split_k=2),
-            dict(kernel="tc", block_m=256)]
+            dict(kernel="tc", block_m=256)] + _decode_variants(M)
     if M <= 8:
         cfgs += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
+    if M <= 32:
+        cfgs += [dict(kernel="decode_mma", split_k=8)]
     for cfg in cfgs:
         C = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
         assert np.array_equal(c_values(C), c_ref), cfg
+    binding.poll_error()
 
 
 def test_symmetric_equals_asymmetric_with_zero_eight():
@@ -199,11 +233,12 @@ def test_symmetric_equals_asymmetric_with_zero_eight():
     Wa = packed_from(synth.QuantWeight(qw.q, qw.scales, np.full((K // G, N), 8, np.uint8), G, "f16"))
     A = binding.acts_to_device(a, torch.float16)
     assert torch.equal(binding.dequant(Ws).view(torch.int16), binding.dequant(Wa).view(torch.int16))
-    for cfg in [None, dict(kernel="tc", block_m=32, split_k=2)]:
+    for cfg in [None, dict(kernel="tc", block_m=32, split_k=2)] + _decode_variants(M):
         Cs = gemm_poisoned(A, Ws, config=cfg)
         Ca = gemm_poisoned(A, Wa, config=cfg)
         torch.cuda.synchronize()
-        assert torch.equal(Cs.view(torch.int16), Ca.view(torch.int16))
+        assert torch.equal(Cs.view(torch.int16), Ca.view(torch.int16)), cfg
+    binding.poll_error()
 
 
 def test_long_k_every_legal_variant():
@@ -233,6 +268,34 @@ def test_long_k_every_legal_variant():
             assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, cfg
 
 
+@pytest.mark.parametrize("M,G,dt", [(1, 128, "f16"), (16, 64, "bf16"), (32, 128, "f16"),
+                                    (9, 128, "bf16")])
+def test_long_k_decode_mma(M, G, dt):
+    """K = 8192: many wrap-arounds of the copy ring, split counts that leave
+    ragged last splits, both group sizes and types."""
+    K, N = 8192, 384
+    qw, a = synth.random_problem(31 + M, M, K, N, G, dt)
+    c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, dt), dt)
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, TORCH_DT[dt])
+    ran = 0
+    for sk in (1, 2, 3, 5, 7, 16, 40):
+        if sk > K // G:
+            continue
+        try:
+            C = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
+        except binding.TmError as e:
+            # a K range whose activations do not fit in shared memory is refused
+            assert e.status == binding.TM_ERR_UNSUPPORTED and "shared memory" in str(e) and sk <= 3, \
+                (sk, str(e))
+            continue
+        ran += 1
+        torch.cuda.synchronize()
+        binding.poll_error()
+        assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, sk
+    assert ran >= 4
+
+
 def test_illegal_variants_are_rejected():
     """Variants whose parity waits could run two phases ahead are refused."""
     qw, a = synth.random_problem(22, 16, 512, 256)
@@ -246,6 +309,14 @@ def test_illegal_variants_are_rejected():
         with pytest.raises(binding.TmError) as e:
             binding.gemm(A, W, config=dict(kernel="tc_decode", block_m=bm, dq_warps=dq))
         assert e.value.status == binding.TM_ERR_UNSUPPORTED
+    # the register-MMA decode kernel: at most 32 rows, at most one split per group
+    A33 = binding.acts_to_device(np.zeros((33, 512), np.uint16), torch.float16)
+    with pytest.raises(binding.TmError) as e:
+        binding.gemm(A33, W, config=dict(kernel="decode_mma"))
+    assert e.value.status == binding.TM_ERR_UNSUPPORTED
+    with pytest.raises(binding.TmError) as e:
+        binding.gemm(A, W, config=dict(kernel="decode_mma", split_k=5))   # 4 groups of 128
+    assert e.value.status == binding.TM_ERR_UNSUPPORTED
 
 
 def test_m_zero_is_noop_and_argument_errors():
@@ -326,7 +397,8 @@ def test_alternating_problems_decode_kernel():
     refs = [oracle_sampled(q, a, rows, cols) for q in (qw, qw2)]
     for cfg in (dict(kernel="tc_decode", block_m=64, dq_warps=4),
                 dict(kernel="tc_decode", block_m=32, dq_warps=8),
-                dict(kernel="tc_decode", block_m=16, dq_warps=8)):
+                dict(kernel="tc_decode", block_m=16, dq_warps=8),
+                dict(kernel="decode_mma", split_k=5)):
         first = []
         for i in range(2):
             C = gemm_poisoned(A, Ws[i], config=cfg)

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libtmw4.so")
 
 TM_OK, TM_ERR_INVALID_ARG, TM_ERR_UNSUPPORTED, TM_ERR_CUDA, TM_ERR_OOM, TM_ERR_TIMEOUT = range(6)
 TM_F16, TM_BF16 = 0, 1
-TM_KERNEL_AUTO, TM_KERNEL_GEMV, TM_KERNEL_TC, TM_KERNEL_TC_DECODE = 0, 1, 2, 3
+TM_KERNEL_AUTO, TM_KERNEL_GEMV, TM_KERNEL_TC, TM_KERNEL_TC_DECODE, TM_KERNEL_DECODE_MMA = 0, 1, 2, 3, 4
 STATUS_NAMES = {0: "TM_OK", 1: "TM_ERR_INVALID_ARG", 2: "TM_ERR_UNSUPPORTED", 3: "TM_ERR_CUDA",
                 4: "TM_ERR_OOM", 5: "TM_ERR_TIMEOUT"}
 
@@ -38,7 +38,7 @@ class TmConfig(ctypes.Structure):
                 ("split_k", ctypes.c_int32), ("dq_warps", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
-        return {"kernel": {1: "gemv", 2: "tc", 3: "tc_decode"}.get(self.kernel, self.kernel),
+        return {"kernel": {1: "gemv", 2: "tc", 3: "tc_decode", 4: "decode_mma"}.get(self.kernel, self.kernel),
                 "block_m": self.block_m, "split_k": self.split_k, "dq_warps": self.dq_warps}
 
 
@@ -207,7 +207,7 @@ def gemm(A: torch.Tensor, W: PackedW4, out: torch.Tensor | None = None, config: 
 
 def make_config(kernel="tc", block_m=16, split_k=1, dq_warps=0) -> TmConfig:
     k = {"auto": TM_KERNEL_AUTO, "gemv": TM_KERNEL_GEMV, "tc": TM_KERNEL_TC,
-         "tc_decode": TM_KERNEL_TC_DECODE}.get(kernel, kernel)
+         "tc_decode": TM_KERNEL_TC_DECODE, "decode_mma": TM_KERNEL_DECODE_MMA}.get(kernel, kernel)
     return TmConfig(int(k), int(block_m), int(split_k), int(dq_warps))
 
 

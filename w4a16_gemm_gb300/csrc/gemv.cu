@@ -234,22 +234,11 @@ size_t gemv_smem_bytes(int rows_tmpl, int kb_per_split) {
 
 template <bool BF16, int MT>
 static cudaError_t launch_gemv_t(const GemmArgs &a, cudaStream_t st) {
-  const size_t smem = gemv_smem_bytes(MT, a.kb_per_split);
-  static size_t attr_bytes = 0;  // largest opt-in set so far (per process)
-  static int attr_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const size_t smem = gemv_smem_bytes(MT, a.kb_per_split);   // at most 200 KB (checked by the caller)
+  cudaError_t e = smem_optin<gemv_kernel<BF16, MT>>(200 * 1024);
   if (e != cudaSuccess) return e;
-  if (attr_device != dev || smem > attr_bytes) {
-    const size_t want = 200 * 1024;
-    e = cudaFuncSetAttribute(gemv_kernel<BF16, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(want));
-    if (e != cudaSuccess) return e;
-    attr_bytes = want;
-    attr_device = dev;
-  }
   dim3 grid(a.N / ATOM_N, a.splits);
-  return launch_kernel(gemv_kernel<BF16, MT>, grid, dim3(256), smem, st, a.pdl != 0, 1u, a);
+  return launch_kernel(gemv_kernel<BF16, MT>, grid, dim3(256), smem, st, a.pdl != 0, a);
 }
 
 cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, cudaStream_t st) {

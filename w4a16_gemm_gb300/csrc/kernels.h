@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,33 +46,44 @@ struct GemmArgs {
 };
 
 // Launch kern<<<grid, block, smem, st>>>(args...), with programmatic stream
-// serialization when pdl is set (see GemmArgs::pdl) and in clusters of
-// cluster_x CTAs along x when cluster_x > 1.
+// serialization when pdl is set (see GemmArgs::pdl).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                 cudaStream_t st, bool pdl, unsigned cluster_x, Args... args) {
+                                 cudaStream_t st, bool pdl, Args... args) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   unsigned n = 0;
   if (pdl) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
   }
-  if (cluster_x > 1) {
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = cluster_x;
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
-  }
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Opts kernel Kern into `bytes` of dynamic shared memory on the current
+// device.  The attribute belongs to the device's context, so it is set once
+// per device; concurrent first calls from several host threads are safe.
+// `bytes` must be the same on every call for a given kernel.
+constexpr int kMaxOptinDevices = 64;
+template <auto Kern>
+inline cudaError_t smem_optin(int bytes) {
+  static std::once_flag once[kMaxOptinDevices];
+  static cudaError_t result[kMaxOptinDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxOptinDevices) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    result[dev] = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+  return result[dev];
 }
 
 // GEMV (CUDA cores): rows_tmpl in {1,2,4,8} >= M.  Shared memory bytes:
@@ -101,6 +113,15 @@ void tc_decode_plan(int M, int N, int K, int block_m, int sms, int *grid, long l
                     int *ws_slots);
 cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                              int dq_warps, int grid, cudaStream_t st);
+
+// Split-K streaming kernel with register-operand tensor-core MMAs (M <= 32):
+// nt16 = decode_mma_nt16(M) m16 tiles of activation rows (0: M too large);
+// kb_per_split must be a multiple of group/64.  Shared memory (staged
+// activations) per CTA:
+int decode_mma_nt16(int M);
+size_t decode_mma_smem_bytes(int nt16, int kb_per_split);
+constexpr size_t kDecodeMmaMaxSmem = 200 * 1024;
+cudaError_t launch_decode_mma(const GemmArgs &a, bool bf16, cudaStream_t st);
 
 // Bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t st);

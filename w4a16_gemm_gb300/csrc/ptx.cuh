@@ -239,19 +239,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16 (fp16 or bf16 inputs, fp32
-// accumulate).  A is 128 x 16 (one TMEM lane per row, K packed two per
-// 32-bit column), B is described by a shared-memory matrix descriptor.
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Four MMAs over one 64-K block: A columns a_tmem + 0/8/16/24 (16 K each),
 // B descriptors b_desc + 0/2/4/6 (32 bytes further along K each, in 16-byte
 // units of the descriptor's start address).  `first` clears D on the first
@@ -324,30 +311,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_type, uint32_t M, u
          | (ab_type << 10)        // B format
          | ((N >> 3) << 17)       // N / 8
          | ((M >> 4) << 24);      // M / 16
-}
-
-// ---------------------------------------------------------- 16-bit x2 math
-// Exact-rounding packed ops (the .rn qualifier keeps the compiler from
-// contracting sub-then-mul into a fused multiply-add).
-__device__ __forceinline__ uint32_t sub_rn_f16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t mul_rn_f16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t sub_rn_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t mul_rn_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
 }
 
 }  // namespace tmw4

@@ -744,17 +744,10 @@ template <bool BF16, int BLOCK_M, int DQ_WG>
 static cudaError_t launch_dec_t(const GemmArgs &a, const CUtensorMap &tmap, int grid, cudaStream_t st) {
   auto kern = tc_decode_kernel<BF16, BLOCK_M, DQ_WG>;
   const int smem = static_cast<int>(dec_smem_bytes(BLOCK_M, DQ_WG));
-  static int attr_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = smem_optin<tc_decode_kernel<BF16, BLOCK_M, DQ_WG>>(smem);
   if (e != cudaSuccess) return e;
-  if (attr_device != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_device = dev;
-  }
   return launch_kernel(kern, dim3(grid), dim3(dec_threads(DQ_WG)), static_cast<size_t>(smem), st,
-                       a.pdl != 0, 1u, tmap, a);
+                       a.pdl != 0, tmap, a);
 }
 
 template <bool BF16, int BLOCK_M>

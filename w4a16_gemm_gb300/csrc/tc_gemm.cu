@@ -406,17 +406,10 @@ template <bool BF16, int BLOCK_M, int DQ_WG>
 static cudaError_t launch_tc_t(const GemmArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
   auto kern = tc_gemm_kernel<BF16, BLOCK_M, DQ_WG>;
   const size_t smem = smem_bytes_for(BLOCK_M);
-  static int attr_device = -1;  // shared-memory opt-in, once per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = smem_optin<tc_gemm_kernel<BF16, BLOCK_M, DQ_WG>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  if (attr_device != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_device = dev;
-  }
   dim3 grid(a.N / BLOCK_N, (a.M + BLOCK_M - 1) / BLOCK_M, a.splits);
-  return launch_kernel(kern, grid, dim3(64 + 128 * DQ_WG), smem, st, a.pdl != 0, 1u, tmap, a);
+  return launch_kernel(kern, grid, dim3(64 + 128 * DQ_WG), smem, st, a.pdl != 0, tmap, a);
 }
 
 template <bool BF16, int BLOCK_M>
