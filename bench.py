@@ -255,7 +255,7 @@ def variant_name(v: dict, dtype: str = "f16") -> str:
     if v["kernel"] == "gemv":
         return f"gemv_kernel<{dtype},{v['block_m']}>"
     if v["kernel"] == "decode_mma":
-        return f"decode_mma_kernel<{dtype},{v['block_m'] // 16}>"
+        return f"decode_mma_kernel<{dtype},{v['block_m'] // 8}>"
     if v["kernel"] == "tc_decode":
         return f"tc_decode_kernel<{dtype},{v['block_m']},{v['dq_warps']}>"
     return f"tc_gemm_kernel<{dtype},{v['block_m']},{v['dq_warps']}>"

@@ -62,10 +62,12 @@ enum {
   TM_KERNEL_TC_DECODE = 3, /* tcgen05/TMEM kernel for small M (block_m 16..64):
                               persistent stream-K grid, weights staged in shared
                               memory by bulk copies, dequantized into TMEM */
-  TM_KERNEL_DECODE_MMA = 4 /* split-K streaming kernel for M <= 32: weights
-                              loaded straight into registers, dequantized there
-                              and multiplied by register-operand tensor-core
-                              MMAs (mma.sync), group scale applied in fp32 */
+  TM_KERNEL_DECODE_MMA = 4 /* persistent stream-K kernel for M <= 16: weights
+                              streamed through shared memory by cp.async,
+                              dequantized in registers and multiplied by
+                              register-operand tensor-core MMAs (mma.sync),
+                              group scale applied in fp32; split_k = CTAs per
+                              SM of the persistent grid (0: all that fit) */
 };
 
 /* A kernel variant: family, rows of A per CTA tile (TC: 16, 32, 64, 128 or

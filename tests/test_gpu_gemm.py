@@ -35,12 +35,12 @@ DECODE_ILLEGAL = {(64, 12), (64, 16)}   # 3-4 warpgroups leave too few TMEM colu
 
 
 def _decode_variants(M):
-    """Every legal tcgen05-decode variant and, for M <= 32, the register-MMA
-    decode kernel with and without split-K."""
+    """Every legal tcgen05-decode variant and, for M <= 16, the register-MMA
+    decode kernel on persistent grids of one and of all resident CTAs per SM."""
     out = [dict(kernel="tc_decode", block_m=bm, dq_warps=dq)
            for bm in (16, 32, 64) for dq in (4, 8, 12, 16) if (bm, dq) not in DECODE_ILLEGAL]
-    if M <= 32:
-        out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=2)]
+    if M <= 16:
+        out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=0)]
     return out
 
 
@@ -48,7 +48,7 @@ def _variants(M):
     out = []
     if M <= 8:
         out += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
-    if M <= 32:
+    if M <= 16:
         out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=3)]
     for bm in (16, 32, 64, 128, 256):
         for sk in (1, 3):
@@ -188,12 +188,12 @@ def test_identity_activation_reproduces_weight():
         C = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
         assert np.array_equal(bits_of(C), w), cfg
-    # the register-MMA decode kernel takes at most 32 rows: slabs of I
-    for k0 in (0, 96, 224):
+    # the register-MMA decode kernel takes at most 16 rows: slabs of I
+    for k0 in (0, 96, 240):
         for sk in (1, 2):
-            C = gemm_poisoned(A[k0:k0 + 32].contiguous(), W, config=dict(kernel="decode_mma", split_k=sk))
+            C = gemm_poisoned(A[k0:k0 + 16].contiguous(), W, config=dict(kernel="decode_mma", split_k=sk))
             torch.cuda.synchronize()
-            assert np.array_equal(bits_of(C), w[k0:k0 + 32]), (k0, sk)
+            assert np.array_equal(bits_of(C), w[k0:k0 + 16]), (k0, sk)
     binding.poll_error()
 
 
@@ -217,7 +217,7 @@ def test_power_of_two_scales_are_exact(M):
             dict(kernel="tc", block_m=256)] + _decode_variants(M)
     if M <= 8:
         cfgs += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
-    if M <= 32:
+    if M <= 16:
         cfgs += [dict(kernel="decode_mma", split_k=8)]
     for cfg in cfgs:
         C = gemm_poisoned(A, W, config=cfg)
@@ -268,32 +268,41 @@ def test_long_k_every_legal_variant():
             assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, cfg
 
 
-@pytest.mark.parametrize("M,G,dt", [(1, 128, "f16"), (16, 64, "bf16"), (32, 128, "f16"),
-                                    (9, 128, "bf16")])
+@pytest.mark.parametrize("M,G,dt", [(1, 128, "f16"), (16, 64, "bf16"), (9, 128, "bf16")])
 def test_long_k_decode_mma(M, G, dt):
-    """K = 8192: many wrap-arounds of the copy ring, split counts that leave
-    ragged last splits, both group sizes and types."""
+    """K = 8192: many wrap-arounds of the copy ring, tiles cut between CTAs of
+    persistent grids of several sizes, both group sizes and types."""
     K, N = 8192, 384
     qw, a = synth.random_problem(31 + M, M, K, N, G, dt)
     c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, dt), dt)
     W = packed_from(qw)
     A = binding.acts_to_device(a, TORCH_DT[dt])
-    ran = 0
-    for sk in (1, 2, 3, 5, 7, 16, 40):
-        if sk > K // G:
-            continue
-        try:
-            C = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
-        except binding.TmError as e:
-            # a K range whose activations do not fit in shared memory is refused
-            assert e.status == binding.TM_ERR_UNSUPPORTED and "shared memory" in str(e) and sk <= 3, \
-                (sk, str(e))
-            continue
-        ran += 1
+    for sk in (1, 2, 3, 5, 0):
+        C = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
         torch.cuda.synchronize()
         binding.poll_error()
         assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, sk
-    assert ran >= 4
+
+
+@pytest.mark.parametrize("K,N,G", [(256, 16384, 128), (1024, 8192, 64), (4096, 1152, 128)])
+@pytest.mark.parametrize("M", [1, 16])
+def test_stream_k_segments_decode_mma(K, N, G, M):
+    """Persistent grids whose CTAs cover whole tiles, the end of one tile and
+    the start of the next, or a piece strictly inside one tile; compared
+    with the oracle on every output."""
+    qw, a = synth.random_problem(40 + K // 64 + M, M, K, N, G, "f16")
+    c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, "f16"), "f16")
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, torch.float16)
+    for sk in (1, 2, 0):
+        C = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
+        torch.cuda.synchronize()
+        binding.poll_error()
+        assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, sk
+        # determinism: a second launch is bit-identical
+        C2 = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(torch.int16), C2.view(torch.int16)), sk
 
 
 def test_illegal_variants_are_rejected():
@@ -309,13 +318,10 @@ def test_illegal_variants_are_rejected():
         with pytest.raises(binding.TmError) as e:
             binding.gemm(A, W, config=dict(kernel="tc_decode", block_m=bm, dq_warps=dq))
         assert e.value.status == binding.TM_ERR_UNSUPPORTED
-    # the register-MMA decode kernel: at most 32 rows, at most one split per group
-    A33 = binding.acts_to_device(np.zeros((33, 512), np.uint16), torch.float16)
+    # the register-MMA decode kernel takes at most 16 rows
+    A17 = binding.acts_to_device(np.zeros((17, 512), np.uint16), torch.float16)
     with pytest.raises(binding.TmError) as e:
-        binding.gemm(A33, W, config=dict(kernel="decode_mma"))
-    assert e.value.status == binding.TM_ERR_UNSUPPORTED
-    with pytest.raises(binding.TmError) as e:
-        binding.gemm(A, W, config=dict(kernel="decode_mma", split_k=5))   # 4 groups of 128
+        binding.gemm(A17, W, config=dict(kernel="decode_mma"))
     assert e.value.status == binding.TM_ERR_UNSUPPORTED
 
 
@@ -397,8 +403,7 @@ def test_alternating_problems_decode_kernel():
     refs = [oracle_sampled(q, a, rows, cols) for q in (qw, qw2)]
     for cfg in (dict(kernel="tc_decode", block_m=64, dq_warps=4),
                 dict(kernel="tc_decode", block_m=32, dq_warps=8),
-                dict(kernel="tc_decode", block_m=16, dq_warps=8),
-                dict(kernel="decode_mma", split_k=5)):
+                dict(kernel="tc_decode", block_m=16, dq_warps=8)):
         first = []
         for i in range(2):
             C = gemm_poisoned(A, Ws[i], config=cfg)
@@ -406,6 +411,34 @@ def test_alternating_problems_decode_kernel():
             assert oracle.max_err_ratio(c_values(C, rows, cols), refs[i], rel=TOL) <= 1.0, (cfg, i)
             first.append(C.view(torch.int16).clone())
         for r in range(40):
+            C = gemm_poisoned(A, Ws[r % 2], config=cfg)
+            torch.cuda.synchronize()
+            assert torch.equal(C.view(torch.int16), first[r % 2]), (cfg, r)
+        binding.poll_error()
+
+
+def test_alternating_problems_decode_mma():
+    """The same stale-data check for the register-MMA decode kernel: two
+    weights of one shape alternate, each launch is compared bit for bit with
+    the first launch of its problem, and those with the oracle."""
+    M = 16
+    qw = synth.weight("sym_g64", 0)
+    a = synth.activations("sym_g64", 0, 32)[:M].copy()
+    roll = lambda x: np.ascontiguousarray(np.roll(x, 128, axis=1))
+    qw2 = synth.QuantWeight(roll(qw.q), roll(qw.scales), None, qw.group, qw.dtype)
+    A = binding.acts_to_device(a, torch.float16)
+    Ws = [packed_from(qw), packed_from(qw2)]
+    cols = sample_indices(qw.N, 160, seed=6)
+    rows = np.arange(M)
+    refs = [oracle_sampled(q, a, rows, cols) for q in (qw, qw2)]
+    for cfg in (dict(kernel="decode_mma", split_k=0), dict(kernel="decode_mma", split_k=1)):
+        first = []
+        for i in range(2):
+            C = gemm_poisoned(A, Ws[i], config=cfg)
+            torch.cuda.synchronize()
+            assert oracle.max_err_ratio(c_values(C, rows, cols), refs[i], rel=TOL) <= 1.0, (cfg, i)
+            first.append(C.view(torch.int16).clone())
+        for r in range(30):
             C = gemm_poisoned(A, Ws[r % 2], config=cfg)
             torch.cuda.synchronize()
             assert torch.equal(C.view(torch.int16), first[r % 2]), (cfg, r)

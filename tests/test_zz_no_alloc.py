@@ -69,18 +69,33 @@ def _needed_scratch(W, M, cfg):
         if plan["partial_slots"] <= 1:
             return 0, 0
         return plan["tiles"] * plan["partial_slots"] * 128 * cfg["block_m"] * 4, plan["tiles"]
+    if cfg["kernel"] == "decode_mma":
+        # persistent stream-K grid: CTAs per SM x SMs over (tile, group) units;
+        # contributors of a tile = CTAs whose ranges meet its units
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        cps = binding.select(W, M)["split_k"]          # CTAs per SM, clamped to what fits
+        GR, T = W.K // W.group, W.N // 128
+        U = T * GR
+        G = max(1, min(U, cps * sms))
+        begin = lambda c: c * U // G
+        def owner(u):
+            c = u * G // U
+            while c + 1 < G and begin(c + 1) <= u:
+                c += 1
+            while c > 0 and begin(c) > u:
+                c -= 1
+            return c
+        slots = max(owner((t + 1) * GR - 1) - owner(t * GR) + 1 for t in range(T))
+        return (0, 0) if slots <= 1 else (T * slots * M * 128 * 4, T)
     gran = 1
     if cfg["kernel"] == "tc":
         gran = 4 if cfg["block_m"] <= 16 else 2 if cfg["block_m"] <= 64 else 1
-    elif cfg["kernel"] == "decode_mma":
-        gran = W.group // 64
     per = -(-KB // cfg.get("split_k", 1))
     per = -(-per // gran) * gran
     splits = -(-KB // per)
     if splits == 1:
         return 0, 0
-    counters = W.N // 64 if cfg["kernel"] == "gemv" else W.N // 128 if cfg["kernel"] == "decode_mma" \
-        else (W.N // 128) * (-(-M // cfg["block_m"]))
+    counters = W.N // 64 if cfg["kernel"] == "gemv" else (W.N // 128) * (-(-M // cfg["block_m"]))
     return splits * M * W.N * 4, counters
 
 
@@ -88,7 +103,7 @@ def _needed_scratch(W, M, cfg):
 CASES = [
     (4, 4096, 1152, "f16", dict(kernel="gemv", split_k=4)),
     (1, 2048, 640, "bf16", dict(kernel="gemv", split_k=1)),
-    (16, 14336, 1152, "f16", dict(kernel="decode_mma", split_k=7)),
+    (16, 14336, 1152, "f16", dict(kernel="decode_mma", split_k=2)),
     (3, 1024, 640, "bf16", dict(kernel="decode_mma", split_k=1)),
     (16, 4096, 1152, "f16", dict(kernel="tc_decode", block_m=16, dq_warps=8)),
     (40, 2048, 640, "f16", dict(kernel="tc_decode", block_m=32, dq_warps=4)),
@@ -124,7 +139,7 @@ def test_alternating_shapes_reuse_the_scratch():
     """Two problems whose splits differ alternate on the shared scratch: each
     call must clear what it needs and not depend on the previous contents."""
     probs = []
-    for (M, K, N, cfg) in ((8, 8192, 640, dict(kernel="decode_mma", split_k=16)),
+    for (M, K, N, cfg) in ((8, 8192, 640, dict(kernel="decode_mma", split_k=3)),
                            (5, 4096, 1152, dict(kernel="gemv", split_k=3))):
         qw, a = synth.random_problem(60 + M, M, K, N)
         W = packed_from(qw)

@@ -266,6 +266,18 @@ static int gemv_rows_tmpl(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 :
 // Is cfg runnable for this shape?  (Fills defaults for zero fields.)
 static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::string *why) {
   const int KB = W->K / 64;
+  if (c->kernel == TM_KERNEL_DECODE_MMA) {
+    if (decode_mma_nt8(M) == 0) {
+      if (why) *why = "DECODE_MMA handles M <= 16";
+      return false;
+    }
+    // split_k: persistent CTAs per SM (clamped to what fits; 0 = all that fit)
+    const int occ = decode_mma_ctas_per_sm(W->dtype == TM_BF16, M, W->group);
+    if (c->split_k <= 0 || c->split_k > occ) c->split_k = occ;
+    c->block_m = 8 * decode_mma_nt8(M);
+    c->dq_warps = 0;
+    return true;
+  }
   if (c->split_k <= 0) c->split_k = 1;
   if (c->split_k > KB) {
     if (why) *why = "split_k larger than K/64";
@@ -306,27 +318,6 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
     }
     return true;
   }
-  if (c->kernel == TM_KERNEL_DECODE_MMA) {
-    const int nt16 = decode_mma_nt16(M);
-    if (nt16 == 0) {
-      if (why) *why = "DECODE_MMA handles M <= 32";
-      return false;
-    }
-    const int gs = W->group / 64;                 // 64-K blocks per group
-    if (c->split_k > KB / gs) {
-      if (why) *why = "split_k larger than the number of quantization groups";
-      return false;
-    }
-    int per = (KB + c->split_k - 1) / c->split_k;
-    per = (per + gs - 1) / gs * gs;
-    if (decode_mma_smem_bytes(nt16, per) > kDecodeMmaMaxSmem) {
-      if (why) *why = "DECODE_MMA K range too long for shared memory; raise split_k";
-      return false;
-    }
-    c->block_m = 16 * nt16;
-    c->dq_warps = 0;
-    return true;
-  }
   if (c->kernel == TM_KERNEL_TC_DECODE) {
     if (c->block_m != 16 && c->block_m != 32 && c->block_m != 64) {
       if (why) *why = "TC_DECODE block_m must be 16, 32 or 64";
@@ -348,14 +339,31 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
   return false;
 }
 
-// Built-in rule used when the tuned table has no entry for this shape.
+// Built-in rule used when the tuned table has no entry for this shape, from
+// the crossovers measured on GB300: the CUDA-core GEMV for one or two rows
+// (about three CTAs per SM over K splits), the tcgen05 decode kernel up to 64
+// rows, the tcgen05 kernel beyond.  The register-MMA decode kernel is picked
+// by the tuner where it measures faster.
 static tm_config default_config(const tm_packed *W, int M, int dev) {
+  const int KB = W->K / 64;
+  const int sms = sm_count(dev);
   tm_config c{};
+  std::string why;
+  if (M <= 2) {
+    const int strips = W->N / 64;
+    c = tm_config{TM_KERNEL_GEMV, 0, std::max(1, (3 * sms + strips / 2) / strips), 0};
+    c.split_k = std::min(c.split_k, KB);
+    while (!normalize_config(W, M, &c, &why) && c.split_k < KB) c.split_k = std::min(KB, c.split_k * 2);
+    if (normalize_config(W, M, &c, &why)) return c;
+  }
+  if (M <= 64) {
+    c = tm_config{TM_KERNEL_TC_DECODE, M <= 16 ? 16 : M <= 32 ? 32 : 64, 1, 8};
+    if (normalize_config(W, M, &c, &why)) return c;
+  }
+  c = tm_config{};
   c.kernel = TM_KERNEL_TC;
   c.block_m = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   c.dq_warps = 8;
-  const int KB = W->K / 64;
-  const int sms = sm_count(dev);
   const int per_sm = c.block_m <= 64 ? 2 : 1;
   const int tiles = (W->N / 128) * ((M + c.block_m - 1) / c.block_m);
   int s = 1;
@@ -365,7 +373,6 @@ static tm_config default_config(const tm_packed *W, int M, int dev) {
     s = std::min(s, 32);
   }
   c.split_k = s;
-  std::string why;
   normalize_config(W, M, &c, &why);
   return c;
 }
@@ -447,6 +454,20 @@ static void plan_work(const tm_packed *W, int M, const tm_config &cfg, GemmArgs 
   const int KB = W->K / 64;
   *ws_floats = 0;
   *n_counters = 0;
+  if (cfg.kernel == TM_KERNEL_DECODE_MMA) {
+    long long tiles = 0;
+    int slots = 1;
+    decode_mma_plan(M, W->N, W->K, W->group, cfg.split_k * sm_count(W->device), dec_grid, &tiles,
+                    &slots);
+    a->kb_per_split = KB;
+    a->splits = 1;
+    a->ws_slots = slots;
+    if (slots > 1) {
+      *ws_floats = static_cast<size_t>(tiles) * slots * M * 128;
+      *n_counters = static_cast<size_t>(tiles);
+    }
+    return;
+  }
   if (cfg.kernel == TM_KERNEL_TC_DECODE) {
     long long tiles = 0;
     int slots = 1;
@@ -460,18 +481,16 @@ static void plan_work(const tm_packed *W, int M, const tm_config &cfg, GemmArgs 
     }
     return;
   }
-  const int gran = cfg.kernel == TM_KERNEL_TC            ? tc_kblocks_per_stage(cfg.block_m)
-                   : cfg.kernel == TM_KERNEL_DECODE_MMA ? W->group / 64
-                                                        : 1;
+  const int gran = cfg.kernel == TM_KERNEL_TC ? tc_kblocks_per_stage(cfg.block_m) : 1;
   int per = (KB + cfg.split_k - 1) / cfg.split_k;
   per = (per + gran - 1) / gran * gran;
   a->kb_per_split = per;
   a->splits = (KB + per - 1) / per;
   if (a->splits > 1) {
     *ws_floats = static_cast<size_t>(a->splits) * M * W->N;
-    *n_counters = cfg.kernel == TM_KERNEL_GEMV          ? static_cast<size_t>(W->N / 64)
-                  : cfg.kernel == TM_KERNEL_DECODE_MMA ? static_cast<size_t>(W->N / 128)
-                  : static_cast<size_t>(W->N / 128) * ((M + cfg.block_m - 1) / cfg.block_m);
+    *n_counters = cfg.kernel == TM_KERNEL_GEMV
+                      ? static_cast<size_t>(W->N / 64)
+                      : static_cast<size_t>(W->N / 128) * ((M + cfg.block_m - 1) / cfg.block_m);
   }
 }
 
@@ -483,7 +502,10 @@ static tm_status launch_planned(const void *A, const tm_packed *W, int M, const 
   if (cfg.kernel == TM_KERNEL_GEMV) {
     e = launch_gemv(a, bf16, gemv_rows_tmpl(M), st);
   } else if (cfg.kernel == TM_KERNEL_DECODE_MMA) {
-    e = launch_decode_mma(a, bf16, st);
+    CUtensorMap map;
+    tm_status s = encode_act_map(A, M, W->K, bf16, cfg.block_m, 1, &map, &a.act_map_3d);
+    if (s != TM_OK) return s;
+    e = launch_decode_mma(a, map, bf16, dec_grid, st);
   } else if (cfg.kernel == TM_KERNEL_TC_DECODE) {
     CUtensorMap map;
     tm_status s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_decode_kblocks_per_stage(), &map,
@@ -867,8 +889,8 @@ static std::vector<tm_config> candidates(const tm_packed *W, int M, int dev) {
   };
   add(default_config(W, M, dev));
   const int splits[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32};
-  if (M <= 32) {
-    for (int s : splits) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 0});
+  if (M <= 16) {
+    for (int s = 1; s <= 8; ++s) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 0});
   }
   if (M <= 8) {
     for (int s : splits) add(tm_config{TM_KERNEL_GEMV, 0, s, 0});
@@ -946,13 +968,30 @@ static double time_variant_graph(const void *A, const std::vector<const tm_packe
   return ms[1] * 1e-3 / launches;
 }
 
+// The tuner's own stream on device `dev` (non-blocking, created once): the
+// caller's stream may be the legacy default stream, which cannot be
+// captured into a graph.
+static tm_status tune_stream(int dev, cudaStream_t *out) {
+  static cudaStream_t streams[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (streams[dev] == nullptr)
+    TM_CUDA(cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking), "cudaStreamCreate(tuner)");
+  *out = streams[dev];
+  return TM_OK;
+}
+
 extern "C" tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *stream,
                              tm_config *best_out) {
   tm_status s = check_handle(W);
   if (s != TM_OK) return s;
   if (Ms == nullptr || nM <= 0) return fail(TM_ERR_INVALID_ARG, "Ms must hold nM > 0 values");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (stream_capturing(st)) return fail(TM_ERR_UNSUPPORTED, "tm_tune cannot run during capture");
+  cudaStream_t user_st = static_cast<cudaStream_t>(stream);
+  if (stream_capturing(user_st)) return fail(TM_ERR_UNSUPPORTED, "tm_tune cannot run during capture");
+  // everything below runs on the tuner's stream, after the caller's work
+  TM_CUDA(cudaStreamSynchronize(user_st), "cudaStreamSynchronize");
+  cudaStream_t st = nullptr;
+  s = tune_stream(W->device, &st);
+  if (s != TM_OK) return s;
   int maxM = 0;
   for (int i = 0; i < nM; ++i) {
     if (Ms[i] <= 0) return fail(TM_ERR_INVALID_ARG, "Ms values must be positive");
@@ -1034,7 +1073,7 @@ extern "C" tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *st
     if (best_out) best_out[i] = best;
   }
   cleanup();
-  tm_status perr = tm_poll_error(stream);
+  tm_status perr = tm_poll_error(st);
   if (perr != TM_OK) return perr;
   const char *p = getenv("TM_TUNE_CACHE");
   if (p && *p) return tm_tune_save(p);

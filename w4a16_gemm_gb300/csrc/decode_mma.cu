@@ -1,66 +1,86 @@
-// decode_mma.cu -- split-K streaming kernel for small row counts (M <= 32)
+// decode_mma.cu -- persistent stream-K kernel for small row counts (M <= 16)
 // whose multiply-accumulate runs on the tensor cores with register operands.
 //
-// At decode sizes the GEMM is bound by HBM, and with the dequantization
-// spread over many threads the SM's instruction issue is the next limit:
-// every instruction spent per packed 32-bit word (eight weights) lowers the
-// bandwidth a full GPU can sustain.  This kernel therefore keeps the
-// per-word work minimal:
-//   * each thread streams its own 8-byte slices of the packed blocks with
-//     64-bit non-coherent loads (a warp instruction covers two whole
-//     128-byte lines), DM_DEPTH 64-K blocks ahead, straight into registers;
-//   * codes become (q - z) exactly in 16-bit floats (exponent-magic OR,
-//     then one exact subtract; TurboMind paper, pith.science review,
-//     Figure 6: integer-to-float conversion before the scaling);
-//   * the registers feed mma.sync m16n8k16 directly as its A operand (16
-//     weight columns x 16 K), the activations are the B operand (8 rows per
-//     n8 tile), and the fp32 accumulator of one quantization group is scaled
-//     once per group: C += s * sum_k a_k (q_k - z).  With s applied in fp32
-//     the only roundings are those of the fp32 sums and the final one to the
-//     16-bit output.
+// At decode sizes the GEMM is bound by HBM: every packed weight byte is
+// used M times, and the kernel must keep enough weight bytes in flight while
+// spending as few instructions per packed 32-bit word (eight weights) as it
+// can.  Per block of 64 K x 128 columns a CTA
+//   * streams the packed weights through a per-warp shared-memory ring with
+//     16-byte cp.async copies (DM_DEPTH - 1 blocks in flight per warp; the
+//     group's scales and zeros travel in the same ring);
+//   * turns each thread's codes into (q - z) exactly in 16-bit floats
+//     (exponent-magic OR, then one exact subtract; TurboMind paper,
+//     pith.science review, Figure 6: integer-to-float conversion before the
+//     scaling);
+//   * feeds them to mma.sync m16n8k16 as the A operand (16 weight columns x
+//     16 K); the activations are the B operand (8 rows per n8 tile), read
+//     straight from global memory (L1-cached, one step ahead): with the K
+//     order below, a thread's B fragment of one 16-K step is 8 contiguous
+//     bytes of one activation row;
+//   * accumulates one quantization group in fp32 and scales it once:
+//     C += s * sum_k a_k (q_k - z).  With s applied in fp32 the only
+//     roundings are those of the fp32 sums and the final one to 16 bits.
 // The K order inside each MMA is a permutation of the actual K order that
 // both operands share: thread (g, t) of the fragment layout holds, for
 // every column it owns, the 16 consecutive K values [16t, 16t + 16) of a
 // 64-K block -- exactly half of one 16-byte chunk of the packed layout (a
-// chunk is 32 consecutive K of one column) -- and the activations are read
+// chunk is 32 consecutive K of one column) -- and reads the activations
 // with the same mapping.  No shuffle is needed on either side.
 //
-// CTA: 4 warps, one 128-column tile of the packed weight, one K range
-// (split-K over grid.y).  Warp w owns columns 32w + 8j + g (j = 0..3; two
-// m16 tiles: rows g / g+8 of tile 0 are columns g / g+8, of tile 1 columns
-// g+16 / g+24).  Activations of the CTA's K range are staged once in shared
-// memory (rows M..8*NT8-1 zero).  With split-K, fp32 partials go to the
-// workspace and the last CTA of a tile to arrive adds them in split order,
-// so results do not depend on scheduling.
+// Work split (stream-K): the units are (128-column tile, quantization
+// group) pairs in tile-major order, and a persistent grid of CTAs -- as many
+// as are resident on the GPU at once -- takes equal contiguous ranges of
+// them.  Because the packed layout is tile-major, a CTA's weights are one
+// contiguous byte range.  A CTA's range covers the end of one tile, whole
+// tiles and the start of another; a whole tile is written directly, a cut
+// one as an fp32 partial per contributor, and after every CTA of the tile
+// has published its partial (one acq_rel atomic each, issued when the CTA
+// has finished its range so that no warp waits for it mid-stream) the last
+// one to arrive adds the partials in contributor order.  Results do not
+// depend on scheduling.
+//
+// CTA: 4 warps; warp w owns columns 32w + 8c + g (c = 0..3) of the current
+// tile: m16 tile mt holds columns c = 2mt (rows g) and c = 2mt + 1 (rows
+// g + 8).
+#include <algorithm>
 #include <cstdint>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tc_epilogue.cuh"
 #include "tmw4_device.cuh"
 
 namespace tmw4 {
 
+// Debug builds (-DTMW4_TRACE): %globaltimer of CTA-level events of the first
+// 2048 CTAs into GemmArgs::trace[event * 2048 + CTA], the CTA's SM in slot 7.
+#ifdef TMW4_TRACE
+#define DM_TRACE(ev)                                                                           \
+  do {                                                                                         \
+    const unsigned cta_ = blockIdx.x + gridDim.x * blockIdx.y;                                 \
+    if (p.trace != nullptr && threadIdx.x == 0 && cta_ < 2048) {                               \
+      p.trace[(ev) * 2048 + cta_] = static_cast<long long>(globaltimer_ns());                  \
+      unsigned smid_;                                                                          \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid_));                                       \
+      p.trace[7 * 2048 + cta_] = smid_;                                                        \
+    }                                                                                          \
+  } while (0)
+#else
+#define DM_TRACE(ev) \
+  do {               \
+  } while (0)
+#endif
+
 namespace {
 
-constexpr int DM_THREADS = 128;
-constexpr int DM_DEPTH = 8;      // ring slots per warp: up to DM_DEPTH - 1 blocks in flight
-constexpr int DM_SLOT = 1024;    // one warp's share of a 64-K block: 32 columns x 32 bytes
-constexpr int DM_META = 80;      // a group's scales (64 B) and zeros (16 B) for one warp
-
-// 16-byte asynchronous copy global -> shared (cached in L2 only).  The
-// copies of one thread are committed in groups and waited for with
-// cp.async.wait_group; the data is visible to the copying thread after the
-// wait, and to the rest of its warp after a following __syncwarp.
-__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+constexpr int DM_CONSUMERS = 128;   // four warps that dequantize and multiply
+constexpr int DM_THREADS = 160;     // + one producer warp
+constexpr int DM_DEPTH = 8;         // ring stages: up to DM_DEPTH blocks in flight
+constexpr int DM_W_BYTES = 4096;    // one 64-K block of the tile's packed weights
+constexpr int DM_META_BYTES = 320;  // a group's scales (256 B) and zeros (64 B) for the tile
 
 // Eight codes of one packed word (value e at nibble (0,4,1,5,2,6,3,7)[e]) ->
 // four 16-bit pairs (q_e - z), exact: {e0,e1}, {e2,e3}, {e4,e5}, {e6,e7},
@@ -158,299 +178,383 @@ __device__ __forceinline__ uint16_t f32_to_bits16(float x) {
 
 }  // namespace
 
-// Shared memory of a CTA:
-//   weight ring   [warp][DM_DEPTH][c 0..3][lane][8 B]: slot r of warp w holds
-//                 the warp's 1 KB of one 64-K block, the 8 bytes each lane
-//                 consumes at [c][lane] (filled by 16-byte copies that span
-//                 two neighbouring lanes);
-//   group data    [warp][DM_DEPTH][80 B]: scales of the warp's 32 columns
-//                 (64 B) and their zero nibbles (16 B), in the slot of the
-//                 block that starts the group;
-//   activations   one 16-byte A-fragment quad per (m16 tile, 16-K step,
-//                 lane): {a[g][K..K+1], a[g+8][K..K+1], a[g][K+2..K+3],
-//                 a[g+8][K+2..K+3]} with K = 16t + 4i inside 64-K block kb
-//                 (i = step within the block), in lane order, so a warp's
-//                 128-bit read is 512 contiguous bytes.
-constexpr int DM_RING_BYTES = 4 * DM_DEPTH * (DM_SLOT + DM_META);
-
-size_t decode_mma_smem_bytes(int nt16, int kb_per_split) {
-  return DM_RING_BYTES + static_cast<size_t>(nt16) * kb_per_split * 4 * 32 * 16;
+// Shared memory of a CTA: a ring of DM_DEPTH stages filled by the producer
+// warp with TMA copies, one stage per 64-K block:
+//   activations   [8 NT8 rows][128 B] (TMA tensor copy, 128-byte swizzle:
+//                 16-byte chunk c of row r sits at chunk c ^ (r % 8); rows
+//                 past M are filled with zeros by the copy);
+//   weights       the block's 4096 packed bytes as stored (one bulk copy);
+//   group data    the tile's 128 scales (256 B) and 64 zero bytes, in the
+//                 stage of the block that starts a group (two bulk copies).
+// full[s] completes when a stage has landed (transaction bytes), empty[s]
+// when the four consumer warps have read it.
+__host__ __device__ constexpr int dm_stage_bytes(int nt8) {
+  return (1024 * nt8 + DM_W_BYTES + DM_META_BYTES + 1023) / 1024 * 1024;
 }
+__host__ __device__ constexpr int dm_smem_bytes(int nt8) { return DM_DEPTH * dm_stage_bytes(nt8) + 1024; }
 
-// NT16: m16 tiles of activation rows (M <= 16 * NT16).  GS: 64-K blocks per
-// quantization group (1 for G = 64, 2 for G = 128); kb_per_split is a
-// multiple of GS, so every split starts on a group boundary.
+// NT8: n8 tiles of activation rows (M <= 8 * NT8).  GS: 64-K blocks per
+// quantization group (1 for G = 64, 2 for G = 128).
 //
-// Fragment roles (mma.sync m16n8k16, row.col): A = activations (16 rows x 16
-// K), B = dequantized weights (16 K x 8 columns), D = C^T tile in fp32.
-// Thread (g, t) = (lane / 4, lane % 4) holds B column g: for K step i of a
-// 64-K block, b0 = pair (16t + 4i, +1) and b1 = pair (16t + 4i + 2, +3) of
-// that column -- the pairs 2(i%2) and 2(i%2)+1 of word i/2 of its 8-byte
-// slice -- and the A quad above, so both operands see the same K order.
-template <bool BF16, int NT16, int GS>
-__global__ void __launch_bounds__(DM_THREADS) decode_mma_kernel(GemmArgs p) {
-  extern __shared__ uint4 dm_smem[];
+// Fragment roles (mma.sync m16n8k16, row.col): A = dequantized weights (16
+// columns x 16 K), B = activations (16 K x 8 rows), D = C^T tile in fp32.
+// For 16-K step i of a 64-K block, thread (g, t) holds
+//   a0, a2 = pairs 2(i%2), 2(i%2)+1 of word i/2 of its slice of column c = 2mt
+//   a1, a3 = the same pairs of column c = 2mt + 1
+//            (actual K 16t + 4i + {0,1} and 16t + 4i + {2,3})
+//   b0, b1 = activation row 8 j8 + g at the same K: 8 contiguous bytes.
+template <bool BF16, int NT8, int GS>
+__global__ void __launch_bounds__(DM_THREADS)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
+  extern __shared__ uint8_t dm_smem_raw[];
   constexpr int D = DM_DEPTH;
-  static_assert(D % GS == 0, "group starts must fall on fixed ring slots");
-  const int nt = blockIdx.x, split = blockIdx.y;
-  const int KB = p.K / 64;
-  const int kb0 = split * p.kb_per_split;
-  const int nsteps = min(KB, kb0 + p.kb_per_split) - kb0;
+  constexpr int STAGE = dm_stage_bytes(NT8);
+  constexpr int ACT_BYTES = 1024 * NT8;
+  constexpr int W0 = ACT_BYTES, META0 = ACT_BYTES + DM_W_BYTES;
+  static_assert((D & (D - 1)) == 0 && STAGE % 1024 == 0, "ring geometry");
+  __shared__ uint64_t full_bar[D], empty_bar[D];
+  __shared__ int seg_tile[2], seg_last[2];
+  __shared__ int abort_flag_s;
+  volatile int *abort_flag = &abort_flag_s;
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(dm_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int G_rows = p.K / p.group;
-  const int KS = 4 * p.kb_per_split;          // 16-K steps of a full split
+  const int KB = p.K / 64;
+  const int GR = p.K / p.group;                    // groups (units) per tile
+  const long long U = static_cast<long long>(p.N / TILE_N) * GR;
+  const long long Gc = gridDim.x;
+  const long long u0 = unit_begin(blockIdx.x, U, Gc);
+  const int nb = static_cast<int>(unit_begin(blockIdx.x + 1, U, Gc) - u0) * GS;   // blocks of this CTA
+  const long long b0 = u0 * GS;                    // its first block in tile-major order
   const bool has_zeros = p.zeros != nullptr;
-
-  uint8_t *smem = reinterpret_cast<uint8_t *>(dm_smem);
-  const uint32_t ring = smem_u32(smem) + warp * D * DM_SLOT;                       // slot r: + r * DM_SLOT
-  const uint32_t meta = smem_u32(smem) + 4 * D * DM_SLOT + warp * D * DM_META;     // slot r: + r * DM_META
-  const uint8_t *meta_p = smem + 4 * D * DM_SLOT + warp * D * DM_META;
-  uint4 *act = reinterpret_cast<uint4 *>(smem + DM_RING_BYTES);
-
-  // copies of block s (relative to kb0): lane (g, h, e) = (L/4, (L/2)%2, L%2)
-  // copies the 16-byte chunk half h of column 32w + 8c + g for c = 2e, 2e+1
-  // into [c][lanes 4g + 2h, +1] of the slot
-  const int h_cp = (lane >> 1) & 1, e_cp = lane & 1;
-  const uint8_t *wsrc = p.qw + (static_cast<size_t>(nt) * KB + kb0) * BLOCK_BYTES + (warp >> 1) * ATOM_BYTES +
-                        h_cp * 1024 + ((warp & 1) * 32 + 16 * e_cp + g) * 16;
-  const uint32_t wdst = ring + (2 * e_cp) * 256 + 32 * g + 16 * h_cp;
-  // group u of the split: lanes 0-3 copy the warp's 64 bytes of scales
-  // (columns 32w + 8q .. +8, q = lane), lane 4 its 16 zero bytes
-  const uint8_t *msrc =
-      lane < 4 ? reinterpret_cast<const uint8_t *>(p.scales + (static_cast<size_t>(nt) * G_rows + kb0 / GS) * TILE_N +
-                                                   32 * warp + 8 * lane)
-               : (lane == 4 && has_zeros
-                      ? p.zeros + (static_cast<size_t>(nt) * G_rows + kb0 / GS) * (TILE_N / 2) + 16 * warp
-                      : nullptr);
-  const size_t mstride = lane < 4 ? TILE_N * 2 : TILE_N / 2;    // bytes per group
-  const uint32_t mdst = meta + (lane < 4 ? 16 * lane : 64);
-
-  auto issue = [&](int s) {
-    if (s < nsteps) {
-      const int r = s % D;
-      const uint8_t *src = wsrc + static_cast<size_t>(s) * BLOCK_BYTES;
-      cp_async16(wdst + r * DM_SLOT, src);
-      cp_async16(wdst + r * DM_SLOT + 256, src + 128);
-      if (s % GS == 0 && msrc != nullptr) cp_async16(mdst + r * DM_META, msrc + (s / GS) * mstride);
-    }
-    cp_async_commit();   // one group per block, empty past the end
-  };
-
-  // the packed weights do not depend on earlier kernels in the stream: the
-  // first blocks are requested before waiting for them
-#pragma unroll
-  for (int s = 0; s < D - 1; ++s) issue(s);
-  pdl_wait();
-  pdl_launch_dependents();
-
-  // activations of this K range -> interleaved A quads (rows >= M are zero).
-  // Lane (g, t) of warp w fills, for every half block hb (32 K) with
-  // hb % 4 == w, the quads of 16-K steps 2hb and 2hb + 1 of its own fragment
-  // position: one 16-byte load per row covers both.
-#pragma unroll
-  for (int mt = 0; mt < NT16; ++mt) {
-    const int m0 = 16 * mt + g, m1 = m0 + 8;
-    const uint16_t *r0 = p.A + static_cast<size_t>(m0) * p.K + kb0 * 64 + 16 * t;
-    const uint16_t *r1 = p.A + static_cast<size_t>(m1) * p.K + kb0 * 64 + 16 * t;
-    const bool has0 = m0 < p.M, has1 = m1 < p.M;
-    for (int hb = warp; hb < 2 * nsteps; hb += 4) {
-      // 16-K steps 2hb and 2hb + 1 of this lane start at K = 64 (hb / 2) + 16t + 8 (hb % 2) and 4 later
-      const int koff = (hb >> 1) * 64 + (hb & 1) * 8;
-      uint4 u = make_uint4(0u, 0u, 0u, 0u), v = make_uint4(0u, 0u, 0u, 0u);
-      if (has0) u = *reinterpret_cast<const uint4 *>(r0 + koff);
-      if (has1) v = *reinterpret_cast<const uint4 *>(r1 + koff);
-      uint4 *dst = act + (mt * KS + 2 * hb) * 32 + lane;
-      dst[0] = make_uint4(u.x, v.x, u.y, v.y);
-      dst[32] = make_uint4(u.z, v.z, u.w, v.w);
-    }
-  }
-  __syncthreads();
-
-  float acc[NT16][4][4];
-  float accg[NT16][4][4];
-#pragma unroll
-  for (int mt = 0; mt < NT16; ++mt)
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[mt][c][e] = 0.f;
-
-  uint32_t zm[4], z16[4];   // per column of the current group: (MAGIC + z), -(64 + z) (fp16)
-  float sc_lo[4], sc_hi[4]; // per column pair of the current group: the scales
-  const int zsh = (g >> 1) * 8 + (g & 1) * 4;
-  const uint2 *wread = reinterpret_cast<const uint2 *>(smem + warp * D * DM_SLOT) + lane;   // + r*128 + c*32
-  const uint4 *aq = act + lane;               // A quad of 16-K step ks: aq[ks * 32]
-
-#pragma unroll 1
-  for (int s0 = 0; s0 < nsteps; s0 += D) {
-#pragma unroll
-    for (int r = 0; r < D; ++r) {
-      const int s = s0 + r;
-      if (s >= nsteps) break;
-      // block s has landed (at most D - 2 younger groups pending) and every
-      // lane is past its reads of the slot refilled next (block s - 1)
-      cp_async_wait<D - 2>();
-      __syncwarp();
-      issue(s + D - 1);
-      uint2 w[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) w[c] = wread[r * (DM_SLOT / 8) + c * 32];
-      if (r % GS == 0) {
-        // group start: its scales and zero points
-        const uint8_t *m = meta_p + r * DM_META;
-        const uint4 zw = has_zeros ? *reinterpret_cast<const uint4 *>(m + 64) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t sp2 = *reinterpret_cast<const uint32_t *>(m + 16 * c + 4 * t);
-          sc_lo[c] = bits16_to_f32<BF16>(sp2 & 0xFFFFu);
-          sc_hi[c] = bits16_to_f32<BF16>(sp2 >> 16);
-          const uint32_t zwc = c == 0 ? zw.x : c == 1 ? zw.y : c == 2 ? zw.z : zw.w;
-          const uint32_t z = has_zeros ? (zwc >> zsh) & 0xFu : 8u;
-          zm[c] = z * 0x00010001u + Magic<BF16>::pair;
-          z16[c] = z * 0x00100010u + 0xD400D400u;   // fp16 -(64 + z) in both halves
-        }
-#pragma unroll
-        for (int mt = 0; mt < NT16; ++mt)
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) accg[mt][c][e] = 0.f;
-      }
-#pragma unroll
-      for (int wi = 0; wi < 2; ++wi) {
-        uint32_t bq[4][4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) codes_minus_zero<BF16>(wi == 0 ? w[c].x : w[c].y, zm[c], z16[c], bq[c]);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-#pragma unroll
-          for (int mt = 0; mt < NT16; ++mt) {
-            const uint4 a = aq[(mt * KS + 4 * s + 2 * wi + j) * 32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              mma_16816<BF16>(accg[mt][c], a.x, a.y, a.z, a.w, bq[c][2 * j], bq[c][2 * j + 1]);
-          }
-        }
-      }
-      if (r % GS == GS - 1) {
-        // end of a group: C += s * sum over the group
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int mt = 0; mt < NT16; ++mt) {
-            ffma2(acc[mt][c][0], acc[mt][c][1], sc_lo[c], sc_hi[c], accg[mt][c][0], accg[mt][c][1]);
-            ffma2(acc[mt][c][2], acc[mt][c][3], sc_lo[c], sc_hi[c], accg[mt][c][2], accg[mt][c][3]);
-          }
-      }
-    }
-  }
-  cp_async_wait<0>();
-
-  // accumulator element e of (mt, c): row m = 16 mt + g + 8 (e >> 1),
-  // column n = 128 nt + 32 w + 8 c + 2t + (e & 1); elements e and e + 1 are
-  // two adjacent columns of one row
   const int M = p.M, N = p.N;
-  const int nbase = nt * TILE_N + 32 * warp + 2 * t;
-  if (p.splits == 1) {
-#pragma unroll
-    for (int mt = 0; mt < NT16; ++mt)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int m = 16 * mt + g + 8 * h;
-          const int n = nbase + 8 * c;
-          if (m < M)
-            *reinterpret_cast<uint32_t *>(p.C + static_cast<size_t>(m) * N + n) =
-                static_cast<uint32_t>(f32_to_bits16<BF16>(acc[mt][c][2 * h])) |
-                (static_cast<uint32_t>(f32_to_bits16<BF16>(acc[mt][c][2 * h + 1])) << 16);
-        }
-    return;
+
+  if (threadIdx.x < D) {
+    mbar_init(full_bar + threadIdx.x, 1);
+    mbar_init(empty_bar + threadIdx.x, 4);
+    fence_mbar_init();
   }
-#pragma unroll
-  for (int mt = 0; mt < NT16; ++mt)
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int m = 16 * mt + g + 8 * h;
-        const int n = nbase + 8 * c;
-        if (m < M)
-          *reinterpret_cast<float2 *>(p.ws + (static_cast<size_t>(split) * M + m) * N + n) =
-              make_float2(acc[mt][c][2 * h], acc[mt][c][2 * h + 1]);
-      }
-  // the barrier orders the CTA's partial writes before one thread's
-  // release-acquire arrival on the tile counter (cumulative release); the
-  // second barrier passes the acquire on to the whole CTA
-  __shared__ int s_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned prev = atomic_add_acq_rel_gpu(p.counters + nt, 1u);
-    s_last = (prev == static_cast<unsigned>(p.splits - 1));
-  }
+  if (threadIdx.x == 0) abort_flag_s = 0;
   __syncwarp();
   __syncthreads();
-  if (!s_last) return;
-  const size_t stride = static_cast<size_t>(M) * N;
+  pdl_launch_dependents();
+  DM_TRACE(0);
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_a);
+      const int nfirst = min(nb, D);
+      int kb = static_cast<int>(b0 % KB);
+      auto copy_weights = [&](int i) {
+        uint8_t *st = smem + (i & (D - 1)) * STAGE;
+        const bool grp = i % GS == 0;
+        mbar_arrive_expect_tx(full_bar + (i & (D - 1)),
+                              ACT_BYTES + DM_W_BYTES + (grp ? 256 + (has_zeros ? 64 : 0) : 0));
+        tma_bulk_g2s(st + W0, p.qw + (b0 + i) * BLOCK_BYTES, DM_W_BYTES, full_bar + (i & (D - 1)));
+        if (grp) {
+          const long long u = u0 + i / GS;
+          tma_bulk_g2s(st + META0, p.scales + u * TILE_N, 256, full_bar + (i & (D - 1)));
+          if (has_zeros) tma_bulk_g2s(st + META0 + 256, p.zeros + u * (TILE_N / 2), 64, full_bar + (i & (D - 1)));
+        }
+      };
+      auto copy_acts = [&](int i, int kbi) {
+        uint8_t *st = smem + (i & (D - 1)) * STAGE;
+        if (p.act_map_3d)
+          tma_load_3d(st, &tmap_a, 0, 0, kbi, full_bar + (i & (D - 1)));
+        else
+          tma_load_2d(st, &tmap_a, kbi * 64, 0, full_bar + (i & (D - 1)));
+      };
+      // the packed weights do not depend on earlier kernels in the stream:
+      // the first stages' weights are requested before waiting for them,
+      // their activations once the previous kernel has completed
+      for (int i = 0; i < nfirst; ++i) copy_weights(i);
+      pdl_wait();
+      for (int i = 0; i < nfirst; ++i) {
+        copy_acts(i, kb);
+        if (++kb == KB) kb = 0;
+      }
+      int issued = nfirst;
+      for (int i = nfirst; i < nb; ++i) {
+        // stage i % D is free once the consumers have read block i - D
+        if (!mbar_wait_bounded(empty_bar + (i & (D - 1)), ((i / D) & 1) ^ 1u, p.limit_ns, abort_flag, p.err,
+                               SITE_PRODUCER_EMPTY, i))
+          break;
+        copy_weights(i);
+        copy_acts(i, kb);
+        if (++kb == KB) kb = 0;
+        issued = i + 1;
+      }
+      // every copy issued must have landed before the CTA exits
+      for (int i = max(0, issued - D); i < issued; ++i)
+        mbar_wait_bounded(full_bar + (i & (D - 1)), (i / D) & 1, p.limit_ns, nullptr, p.err, SITE_DRAIN_TMA, i);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, t = lane & 3;
+  float acc[2][NT8][4];
+  float accg[2][NT8][4];
+  uint32_t zm[4], z16[4];     // per column of the current group: (MAGIC + z), -(64 + z) (fp16)
+  float sc[4];                // per column of the current group: the scale
+  const int zsh = (g >> 1) * 8 + (g & 1) * 4;
+  // this thread's reads in a stage: weights of column 32w + 8c + g at
+  // wrd + 128c; scales at mrd + 16c (+ 2 bytes per column), zeros at mzd;
+  // B fragment of n8 tile j8, 16-K step i: row 8 j8 + g, chunk (2t + i/2) ^ g
+  const int wrd = W0 + (warp >> 1) * ATOM_BYTES + (t >> 1) * 1024 + ((warp & 1) * 32 + g) * 16 + (t & 1) * 8;
+  const int mrd = META0 + 2 * (32 * warp + g);
+  const int mzd = META0 + 256 + 16 * warp;
+  int brd[4];
 #pragma unroll
-  for (int mt = 0; mt < NT16; ++mt)
+  for (int i = 0; i < 4; ++i) brd[i] = g * 128 + (((2 * t + (i >> 1)) ^ g) << 4) + ((i & 1) << 3);
+  int nseg = 0;
+  bool ok = true;
+  // cut segments of the range (the first and the last may be cut), from the
+  // range alone, so that every consumer warp takes the same barriers below
+  // even if one of them gave up a wait
+  const long long t_first = b0 / KB, t_last = (b0 + nb - 1) / KB;
+  const bool first_cut = b0 % KB != 0 || b0 + nb < (t_first + 1) * KB;
+  const bool last_cut = t_last != t_first && (b0 + nb) % KB != 0;
+  const int nseg_range = (first_cut ? 1 : 0) + (last_cut ? 1 : 0);
+
+  int i = 0;
+  int kb_c = static_cast<int>(b0 % KB), t_c = static_cast<int>(b0 / KB);
+#pragma unroll 1
+  while (i < nb && ok) {
+    // a tile segment: blocks [i, i + len) of tile t_c
+    const int len = min(nb - i, KB - kb_c);
+    const bool whole = kb_c == 0 && len == KB;
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int m = 16 * mt + g + 8 * h;
-        const int n = nbase + 8 * c;
-        if (m < M) {
-          // fixed split order; this CTA's own partial from registers
-          const float2 *src = reinterpret_cast<const float2 *>(p.ws + static_cast<size_t>(m) * N + n);
-          const float2 mine = make_float2(acc[mt][c][2 * h], acc[mt][c][2 * h + 1]);
-          float2 sum = make_float2(0.f, 0.f);
-          int q0 = 0;
-          for (; q0 + 8 <= p.splits; q0 += 8) {
-            float2 v[8];
+      for (int j8 = 0; j8 < NT8; ++j8)
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = q0 + q == split ? mine : __ldcg(src + (q0 + q) * stride / 2);
+        for (int e = 0; e < 4; ++e) acc[mt][j8][e] = 0.f;
+#pragma unroll 1
+    for (int ig = i; ig < i + len && ok; ig += GS) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              sum.x += v[q].x;
-              sum.y += v[q].y;
+      for (int u = 0; u < GS; ++u) {
+        const int ib = ig + u;
+        const int sidx = ib & (D - 1);
+        if (!mbar_wait_warp(full_bar + sidx, (ib / D) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL, ib)) {
+          ok = false;
+          break;
+        }
+        const uint8_t *st = smem + sidx * STAGE;
+        uint2 w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint2 *>(st + wrd + 128 * c);
+        if (u == 0) {
+          // group start: its scales and zero points
+          const uint4 zw = has_zeros ? *reinterpret_cast<const uint4 *>(st + mzd) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            sc[c] = bits16_to_f32<BF16>(*reinterpret_cast<const uint16_t *>(st + mrd + 16 * c));
+            const uint32_t zwc = c == 0 ? zw.x : c == 1 ? zw.y : c == 2 ? zw.z : zw.w;
+            const uint32_t z = has_zeros ? (zwc >> zsh) & 0xFu : 8u;
+            zm[c] = z * 0x00010001u + Magic<BF16>::pair;
+            z16[c] = z * 0x00100010u + 0xD400D400u;   // fp16 -(64 + z) in both halves
+          }
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int j8 = 0; j8 < NT8; ++j8)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) accg[mt][j8][e] = 0.f;
+        }
+#pragma unroll
+        for (int wi = 0; wi < 2; ++wi) {
+          uint2 bf[NT8][2];
+#pragma unroll
+          for (int j8 = 0; j8 < NT8; ++j8)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              bf[j8][j] = *reinterpret_cast<const uint2 *>(st + j8 * 1024 + brd[2 * wi + j]);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            uint32_t lo[4], hi[4];
+            codes_minus_zero<BF16>(wi == 0 ? w[2 * mt].x : w[2 * mt].y, zm[2 * mt], z16[2 * mt], lo);
+            codes_minus_zero<BF16>(wi == 0 ? w[2 * mt + 1].x : w[2 * mt + 1].y, zm[2 * mt + 1],
+                                   z16[2 * mt + 1], hi);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int j8 = 0; j8 < NT8; ++j8)
+                mma_16816<BF16>(accg[mt][j8], lo[2 * j], hi[2 * j], lo[2 * j + 1], hi[2 * j + 1],
+                                bf[j8][j].x, bf[j8][j].y);
+          }
+        }
+        // the stage has been read: release it to the producer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar + sidx);
+        if (u == GS - 1) {
+          // end of a group: C += s * sum over the group
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int j8 = 0; j8 < NT8; ++j8) {
+              ffma2(acc[mt][j8][0], acc[mt][j8][1], sc[2 * mt], sc[2 * mt], accg[mt][j8][0], accg[mt][j8][1]);
+              ffma2(acc[mt][j8][2], acc[mt][j8][3], sc[2 * mt + 1], sc[2 * mt + 1], accg[mt][j8][2],
+                    accg[mt][j8][3]);
             }
-          }
-          for (; q0 < p.splits; ++q0) {
-            const float2 v = q0 == split ? mine : __ldcg(src + q0 * stride / 2);
-            sum.x += v.x;
-            sum.y += v.y;
-          }
-          *reinterpret_cast<uint32_t *>(p.C + static_cast<size_t>(m) * N + n) =
-              static_cast<uint32_t>(f32_to_bits16<BF16>(sum.x)) |
-              (static_cast<uint32_t>(f32_to_bits16<BF16>(sum.y)) << 16);
         }
       }
-  if (threadIdx.x == 0) p.counters[nt] = 0u;
+    }
+    if (!ok) break;
+    // the segment ends: a whole tile goes to C, a cut one to its contributor
+    // slot (published when the range is done).  Accumulator element e of
+    // (mt, j8): column col = 32 w + 8 (2 mt + e / 2) + g of tile t_c,
+    // activation row m = 8 j8 + 2t + e % 2
+    float *part = nullptr;
+    if (!whole) {
+      const int jc = static_cast<int>(blockIdx.x) - cta_of_unit(static_cast<long long>(t_c) * GR, U, Gc);
+      part = p.ws + (static_cast<size_t>(t_c) * p.ws_slots + jc) * M * TILE_N;
+      if (threadIdx.x == 0) seg_tile[nseg] = t_c;
+      ++nseg;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int j8 = 0; j8 < NT8; ++j8)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int m = 8 * j8 + 2 * t + (e & 1);
+          const int col = 32 * warp + 8 * (2 * mt + (e >> 1)) + g;
+          if (m < M) {
+            if (whole)
+              p.C[static_cast<size_t>(m) * N + static_cast<size_t>(t_c) * TILE_N + col] =
+                  f32_to_bits16<BF16>(acc[mt][j8][e]);
+            else
+              part[m * TILE_N + col] = acc[mt][j8][e];
+          }
+        }
+    i += len;
+    kb_c = 0;
+    ++t_c;
+  }
+  DM_TRACE(3);
+  (void)nseg;
+  if (nseg_range == 0) return;   // every tile the range touches was whole
+
+  // publish the cut segments: the barrier orders every consumer's partial
+  // writes before one thread's release-acquire arrival per tile (cumulative
+  // release); the second barrier passes the outcome (and the acquire) on.
+  // After a wait gave up (the abort flag; C is then undefined and the error
+  // is reported by tm_poll_error) nothing is published.
+  named_bar_sync(1, DM_CONSUMERS);
+  const bool aborted = *abort_flag != 0;
+  if (threadIdx.x == 0 && !aborted) {
+    // both arrivals are issued before either result is used
+    const unsigned prev0 = atomic_add_acq_rel_gpu(p.counters + seg_tile[0], 1u);
+    const unsigned prev1 = nseg_range > 1 ? atomic_add_acq_rel_gpu(p.counters + seg_tile[1], 1u) : 0u;
+    for (int k = 0; k < nseg_range; ++k) {
+      const int tt = seg_tile[k];
+      const int ncontrib = cta_of_unit(static_cast<long long>(tt) * GR + GR - 1, U, Gc) -
+                           cta_of_unit(static_cast<long long>(tt) * GR, U, Gc) + 1;
+      seg_last[k] = (k == 0 ? prev0 : prev1) == static_cast<unsigned>(ncontrib - 1);
+    }
+  }
+  named_bar_sync(1, DM_CONSUMERS);
+  DM_TRACE(4);
+  if (aborted) return;
+  for (int k = 0; k < nseg_range; ++k) {
+    if (!seg_last[k]) continue;
+    // the last contributor of tile tt adds all partials in contributor order
+    const int tt = seg_tile[k];
+    const int ncontrib = cta_of_unit(static_cast<long long>(tt) * GR + GR - 1, U, Gc) -
+                         cta_of_unit(static_cast<long long>(tt) * GR, U, Gc) + 1;
+    const float *base = p.ws + static_cast<size_t>(tt) * p.ws_slots * M * TILE_N;
+    for (int idx = threadIdx.x; idx < M * TILE_N; idx += DM_CONSUMERS) {
+      float sum = 0.f;
+      int q0 = 0;
+      for (; q0 + 4 <= ncontrib; q0 += 4) {
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = __ldcg(base + static_cast<size_t>(q0 + q) * M * TILE_N + idx);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sum += v[q];
+      }
+      for (; q0 < ncontrib; ++q0) sum += __ldcg(base + static_cast<size_t>(q0) * M * TILE_N + idx);
+      const int m = idx / TILE_N, col = idx % TILE_N;
+      p.C[static_cast<size_t>(m) * N + static_cast<size_t>(tt) * TILE_N + col] = f32_to_bits16<BF16>(sum);
+    }
+    if (threadIdx.x == 0) p.counters[tt] = 0u;
+  }
+  DM_TRACE(5);
 }
 
-template <bool BF16, int NT16, int GS>
-static cudaError_t launch_dm_t(const GemmArgs &a, cudaStream_t st) {
-  auto kern = decode_mma_kernel<BF16, NT16, GS>;
-  cudaError_t e = smem_optin<decode_mma_kernel<BF16, NT16, GS>>(static_cast<int>(kDecodeMmaMaxSmem));
+template <bool BF16, int NT8, int GS>
+static cudaError_t launch_dm_t(const GemmArgs &a, const CUtensorMap &tmap, int grid, cudaStream_t st) {
+  auto kern = decode_mma_kernel<BF16, NT8, GS>;
+  cudaError_t e = smem_optin<decode_mma_kernel<BF16, NT8, GS>>(dm_smem_bytes(NT8));
   if (e != cudaSuccess) return e;
-  const size_t smem = decode_mma_smem_bytes(NT16, a.kb_per_split);
-  dim3 grid(a.N / TILE_N, a.splits);
-  return launch_kernel(kern, grid, dim3(DM_THREADS), smem, st, a.pdl != 0, a);
+  return launch_kernel(kern, dim3(grid), dim3(DM_THREADS), static_cast<size_t>(dm_smem_bytes(NT8)), st,
+                       a.pdl != 0, tmap, a);
 }
 
-template <bool BF16, int NT16>
-static cudaError_t launch_dm_g(const GemmArgs &a, cudaStream_t st) {
-  return a.group == 64 ? launch_dm_t<BF16, NT16, 1>(a, st) : launch_dm_t<BF16, NT16, 2>(a, st);
+template <bool BF16, int NT8>
+static cudaError_t launch_dm_g(const GemmArgs &a, const CUtensorMap &tmap, int grid, cudaStream_t st) {
+  return a.group == 64 ? launch_dm_t<BF16, NT8, 1>(a, tmap, grid, st) : launch_dm_t<BF16, NT8, 2>(a, tmap, grid, st);
 }
 
-int decode_mma_nt16(int M) { return M <= 16 ? 1 : M <= 32 ? 2 : 0; }
+// Resident CTAs per SM of the kernel instantiation for (bf16, M, group).
+template <bool BF16, int NT8, int GS>
+static int dm_occupancy_t() {
+  static std::once_flag once[kMaxOptinDevices];
+  static int occ[kMaxOptinDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxOptinDevices) return 1;
+  std::call_once(once[dev], [&] {
+    int v = 0;
+    if (smem_optin<decode_mma_kernel<BF16, NT8, GS>>(dm_smem_bytes(NT8)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, decode_mma_kernel<BF16, NT8, GS>, DM_THREADS,
+                                                      dm_smem_bytes(NT8)) != cudaSuccess ||
+        v <= 0)
+      v = 1;
+    occ[dev] = v;
+  });
+  return occ[dev];
+}
 
-cudaError_t launch_decode_mma(const GemmArgs &a, bool bf16, cudaStream_t st) {
-  switch (decode_mma_nt16(a.M)) {
-    case 1: return bf16 ? launch_dm_g<true, 1>(a, st) : launch_dm_g<false, 1>(a, st);
-    case 2: return bf16 ? launch_dm_g<true, 2>(a, st) : launch_dm_g<false, 2>(a, st);
+template <bool BF16, int NT8>
+static int dm_occupancy_g(int group) {
+  return group == 64 ? dm_occupancy_t<BF16, NT8, 1>() : dm_occupancy_t<BF16, NT8, 2>();
+}
+
+int decode_mma_nt8(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : 0; }
+
+int decode_mma_ctas_per_sm(bool bf16, int M, int group) {
+  switch (decode_mma_nt8(M)) {
+    case 1: return bf16 ? dm_occupancy_g<true, 1>(group) : dm_occupancy_g<false, 1>(group);
+    case 2: return bf16 ? dm_occupancy_g<true, 2>(group) : dm_occupancy_g<false, 2>(group);
+    default: return 1;
+  }
+}
+
+void decode_mma_plan(int M, int N, int K, int group, int max_ctas, int *grid, long long *tiles,
+                     int *slots) {
+  const long long GR = K / group;
+  const long long T = N / TILE_N;
+  const long long U = T * GR;
+  const long long G = std::max<long long>(1, std::min<long long>(max_ctas, U));
+  int maxc = 1;
+  for (long long t = 0; t < T; ++t) {
+    const int c = cta_of_unit((t + 1) * GR - 1, U, G) - cta_of_unit(t * GR, U, G) + 1;
+    if (c > maxc) maxc = c;
+  }
+  *grid = static_cast<int>(G);
+  *tiles = T;
+  *slots = maxc;
+  (void)M;
+}
+
+cudaError_t launch_decode_mma(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int grid,
+                              cudaStream_t st) {
+  switch (decode_mma_nt8(a.M)) {
+    case 1: return bf16 ? launch_dm_g<true, 1>(a, tmap_a, grid, st) : launch_dm_g<false, 1>(a, tmap_a, grid, st);
+    case 2: return bf16 ? launch_dm_g<true, 2>(a, tmap_a, grid, st) : launch_dm_g<false, 2>(a, tmap_a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

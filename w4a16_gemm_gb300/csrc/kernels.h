@@ -114,14 +114,20 @@ void tc_decode_plan(int M, int N, int K, int block_m, int sms, int *grid, long l
 cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                              int dq_warps, int grid, cudaStream_t st);
 
-// Split-K streaming kernel with register-operand tensor-core MMAs (M <= 32):
-// nt16 = decode_mma_nt16(M) m16 tiles of activation rows (0: M too large);
-// kb_per_split must be a multiple of group/64.  Shared memory (staged
-// activations) per CTA:
-int decode_mma_nt16(int M);
-size_t decode_mma_smem_bytes(int nt16, int kb_per_split);
-constexpr size_t kDecodeMmaMaxSmem = 200 * 1024;
-cudaError_t launch_decode_mma(const GemmArgs &a, bool bf16, cudaStream_t st);
+// Persistent stream-K kernel with register-operand tensor-core MMAs
+// (M <= 16; decode_mma_nt8(M) n8 tiles of activation rows, 0 if M is too
+// large).  decode_mma_ctas_per_sm: resident CTAs per SM of the instantiation
+// for (bf16, M, group); decode_mma_plan: the grid for at most max_ctas CTAs,
+// the tile count (split-K counters) and the fp32 partial slots per tile
+// (1: no tile is cut between CTAs).
+int decode_mma_nt8(int M);
+int decode_mma_ctas_per_sm(bool bf16, int M, int group);
+void decode_mma_plan(int M, int N, int K, int group, int max_ctas, int *grid, long long *tiles,
+                     int *slots);
+// tmap_a: activation tensor map with box 64 x (8 * decode_mma_nt8(M)) and the
+// 128-byte swizzle (3-D with one 64-K block per copy, or 2-D)
+cudaError_t launch_decode_mma(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int grid,
+                              cudaStream_t st);
 
 // Bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t st);

@@ -119,18 +119,6 @@ __host__ __device__ constexpr long long dec_smem_bytes(int block_m, int dq_wg) {
          static_cast<long long>(dec_wst(block_m, dq_wg)) * W_STAGE_BYTES + 1024;
 }
 
-// Stream-K partition: CTA c owns units [unit_begin(c), unit_begin(c + 1)).
-__host__ __device__ __forceinline__ long long unit_begin(long long c, long long U, long long G) {
-  return c * U / G;
-}
-// The CTA whose range holds unit u.
-__host__ __device__ __forceinline__ int cta_of_unit(long long u, long long U, long long G) {
-  long long c = u * G / U;
-  while (c + 1 < G && unit_begin(c + 1, U, G) <= u) ++c;
-  while (c > 0 && unit_begin(c, U, G) > u) --c;
-  return static_cast<int>(c);
-}
-
 // Position of a unit: tile t (= mt * NT + nt) and stage s of that tile.
 // Loops step it forward instead of dividing a 64-bit unit index: a 64-bit
 // division by a runtime value costs a few hundred cycles per loop trip.

@@ -47,6 +47,19 @@ __host__ __device__ __forceinline__ size_t zero_byte(int g, int n, int G_rows) {
   return (static_cast<size_t>(n >> 7) * G_rows + g) * (TILE_N / 2) + ((n & 127) >> 1);
 }
 
+// Stream-K partition of U work units over a persistent grid of G CTAs: CTA c
+// owns units [unit_begin(c), unit_begin(c + 1)).
+__host__ __device__ __forceinline__ long long unit_begin(long long c, long long U, long long G) {
+  return c * U / G;
+}
+// The CTA whose range holds unit u.
+__host__ __device__ __forceinline__ int cta_of_unit(long long u, long long U, long long G) {
+  long long c = u * G / U;
+  while (c + 1 < G && unit_begin(c + 1, U, G) <= u) ++c;
+  while (c > 0 && unit_begin(c, U, G) > u) --c;
+  return static_cast<int>(c);
+}
+
 // Exponent "magic" that turns a 4-bit code c placed in the low mantissa bits
 // into the exact value MAGIC + c: 1024 + c for fp16 (0x6400), 128 + c for
 // bf16 (0x4300).  Subtracting (MAGIC + z) is exact, so the following multiply

@@ -21,16 +21,41 @@ quantization):
                clipped to +-64, fp16
 
 Seeds: the tiny problem draws weights then activations from
-``default_rng(0)``; every other problem draws weights from
-``default_rng(SeedSequence([cfg, shape, 0]))`` and the activations for row
-count M from ``default_rng(SeedSequence([cfg, shape, 1, M]))``.
+``default_rng(0)``; every other problem draws its weights in chunks of
+CHUNK_ROWS rows of K, chunk j from ``default_rng(SeedSequence([cfg, shape, 0,
+j]))`` (a multiple of every group size, so quantization groups never straddle
+chunks), and the activations for row count M in chunks of CHUNK_ROWS rows of
+M, chunk j from ``default_rng(SeedSequence([cfg, shape, 1, M, j]))``.  The
+chunks are independent streams, drawn in parallel threads.
 """
 
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
 from dataclasses import dataclass
 
 import numpy as np
+
+CHUNK_ROWS = 1024
+
+
+def _threads() -> int:
+    try:
+        return max(1, min(16, len(os.sched_getaffinity(0))))
+    except AttributeError:
+        return max(1, min(16, os.cpu_count() or 1))
+
+
+def _chunked(rows: int, fn) -> np.ndarray:
+    """Concatenates fn(j, r0, r1) over row chunks [r0, r1) of CHUNK_ROWS rows,
+    computed in parallel threads (numpy releases the GIL in the heavy work)."""
+    bounds = [(j, r0, min(rows, r0 + CHUNK_ROWS)) for j, r0 in enumerate(range(0, rows, CHUNK_ROWS))]
+    if len(bounds) == 1:
+        return fn(*bounds[0])
+    with cf.ThreadPoolExecutor(max_workers=_threads()) as ex:
+        parts = list(ex.map(lambda b: fn(*b), bounds))
+    return parts
 
 SHAPES_8B = ((4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096))
 SHAPES_70B = ((8192, 10240), (8192, 8192), (8192, 57344), (28672, 8192))
@@ -157,10 +182,20 @@ def weight(workload: str, shape_idx: int) -> QuantWeight:
     K, N = wl.shapes[shape_idx]
     if wl.cfg_id == 0:
         rng = np.random.default_rng(0)
-    else:
-        rng = np.random.default_rng(np.random.SeedSequence([wl.cfg_id, shape_idx, 0]))
-    w = rng.standard_normal((K, N), dtype=np.float32) * np.float32(0.02)
-    return quantize_rtn(w, wl.group, wl.dtype, wl.symmetric)
+        w = rng.standard_normal((K, N), dtype=np.float32) * np.float32(0.02)
+        return quantize_rtn(w, wl.group, wl.dtype, wl.symmetric)
+
+    def chunk(j, r0, r1):
+        rng = np.random.default_rng(np.random.SeedSequence([wl.cfg_id, shape_idx, 0, j]))
+        w = rng.standard_normal((r1 - r0, N), dtype=np.float32) * np.float32(0.02)
+        return quantize_rtn(w, wl.group, wl.dtype, wl.symmetric)
+
+    parts = _chunked(K, chunk)
+    if isinstance(parts, QuantWeight):
+        return parts
+    return QuantWeight(np.concatenate([q.q for q in parts]), np.concatenate([q.scales for q in parts]),
+                       None if wl.symmetric else np.concatenate([q.zeros for q in parts]),
+                       wl.group, wl.dtype)
 
 
 def activations(workload: str, shape_idx: int, M: int) -> np.ndarray:
@@ -170,9 +205,14 @@ def activations(workload: str, shape_idx: int, M: int) -> np.ndarray:
     if wl.cfg_id == 0:
         rng = np.random.default_rng(0)
         rng.standard_normal((K, N), dtype=np.float32)  # weights come first
-    else:
-        rng = np.random.default_rng(np.random.SeedSequence([wl.cfg_id, shape_idx, 1, M]))
-    return _draw_acts(rng, M, K, wl.act_dist, wl.dtype)
+        return _draw_acts(rng, M, K, wl.act_dist, wl.dtype)
+
+    def chunk(j, r0, r1):
+        rng = np.random.default_rng(np.random.SeedSequence([wl.cfg_id, shape_idx, 1, M, j]))
+        return _draw_acts(rng, r1 - r0, K, wl.act_dist, wl.dtype)
+
+    parts = _chunked(M, chunk)
+    return parts if isinstance(parts, np.ndarray) else np.concatenate(parts)
 
 
 def random_problem(seed: int, M: int, K: int, N: int, group: int = 128, dtype: str = "f16",
