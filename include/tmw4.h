@@ -62,12 +62,19 @@ enum {
   TM_KERNEL_TC_DECODE = 3, /* tcgen05/TMEM kernel for small M (block_m 16..64):
                               persistent stream-K grid, weights staged in shared
                               memory by bulk copies, dequantized into TMEM */
-  TM_KERNEL_DECODE_MMA = 4 /* persistent stream-K kernel for M <= 16: weights
-                              streamed through shared memory by cp.async,
+  TM_KERNEL_DECODE_MMA = 4 /* kernel for M <= 16: weights streamed through
+                              shared memory by bulk copies of a producer warp,
                               dequantized in registers and multiplied by
                               register-operand tensor-core MMAs (mma.sync),
-                              group scale applied in fp32; split_k = CTAs per
-                              SM of the persistent grid (0: all that fit) */
+                              group scale applied in fp32.  Two work splits,
+                              chosen by dq_warps:
+                                0  persistent stream-K grid; split_k = CTAs
+                                   per SM (0: all that fit);
+                                1  one thread-block cluster of split_k CTAs
+                                   (1..16) per 128-column tile, each taking
+                                   an equal group-aligned K range; partial
+                                   sums added through distributed shared
+                                   memory (no workspace) */
 };
 
 /* A kernel variant: family, rows of A per CTA tile (TC: 16, 32, 64, 128 or
@@ -78,7 +85,9 @@ typedef struct {
   int32_t block_m;
   int32_t split_k;
   int32_t dq_warps; /* TC: dequant warps per CTA, 4, 8 or 16 (0 = default);
-                       each group of 4 dequantizes every (dq_warps/4)-th stage */
+                       each group of 4 dequantizes every (dq_warps/4)-th stage;
+                       TC_DECODE: 4, 8 or 12 dequant warps; DECODE_MMA: the
+                       work split (0 stream-K, 1 cluster split-K) */
 } tm_config;
 
 /* Opaque packed weight, owned by the library until tm_packed_free. */

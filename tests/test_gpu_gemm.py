@@ -36,11 +36,14 @@ DECODE_ILLEGAL = {(64, 12), (64, 16)}   # 3-4 warpgroups leave too few TMEM colu
 
 def _decode_variants(M):
     """Every legal tcgen05-decode variant and, for M <= 16, the register-MMA
-    decode kernel on persistent grids of one and of all resident CTAs per SM."""
+    decode kernel on persistent grids of one and of all resident CTAs per SM
+    and in clusters of 4 and of 16 CTAs per tile."""
     out = [dict(kernel="tc_decode", block_m=bm, dq_warps=dq)
            for bm in (16, 32, 64) for dq in (4, 8, 12, 16) if (bm, dq) not in DECODE_ILLEGAL]
     if M <= 16:
-        out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=0)]
+        out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=0),
+                dict(kernel="decode_mma", split_k=4, dq_warps=1),
+                dict(kernel="decode_mma", split_k=16, dq_warps=1)]
     return out
 
 
@@ -49,7 +52,8 @@ def _variants(M):
     if M <= 8:
         out += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
     if M <= 16:
-        out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=3)]
+        out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=3),
+                dict(kernel="decode_mma", split_k=3, dq_warps=1)]
     for bm in (16, 32, 64, 128, 256):
         for sk in (1, 3):
             for dq in (4, 8, 16):
@@ -190,10 +194,10 @@ def test_identity_activation_reproduces_weight():
         assert np.array_equal(bits_of(C), w), cfg
     # the register-MMA decode kernel takes at most 16 rows: slabs of I
     for k0 in (0, 96, 240):
-        for sk in (1, 2):
-            C = gemm_poisoned(A[k0:k0 + 16].contiguous(), W, config=dict(kernel="decode_mma", split_k=sk))
+        for cfg in (dict(split_k=1), dict(split_k=2), dict(split_k=4, dq_warps=1)):
+            C = gemm_poisoned(A[k0:k0 + 16].contiguous(), W, config=dict(kernel="decode_mma", **cfg))
             torch.cuda.synchronize()
-            assert np.array_equal(bits_of(C), w[k0:k0 + 16]), (k0, sk)
+            assert np.array_equal(bits_of(C), w[k0:k0 + 16]), (k0, cfg)
     binding.poll_error()
 
 
@@ -277,11 +281,13 @@ def test_long_k_decode_mma(M, G, dt):
     c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, dt), dt)
     W = packed_from(qw)
     A = binding.acts_to_device(a, TORCH_DT[dt])
-    for sk in (1, 2, 3, 5, 0):
-        C = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
+    cfgs = [dict(split_k=sk) for sk in (1, 2, 3, 5, 0)] + \
+        [dict(split_k=sk, dq_warps=1) for sk in (1, 2, 7, 16)]
+    for cfg in cfgs:
+        C = gemm_poisoned(A, W, config=dict(kernel="decode_mma", **cfg))
         torch.cuda.synchronize()
         binding.poll_error()
-        assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, sk
+        assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, cfg
 
 
 @pytest.mark.parametrize("K,N,G", [(256, 16384, 128), (1024, 8192, 64), (4096, 1152, 128)])
@@ -301,6 +307,30 @@ def test_stream_k_segments_decode_mma(K, N, G, M):
         assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, sk
         # determinism: a second launch is bit-identical
         C2 = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(torch.int16), C2.view(torch.int16)), sk
+
+
+@pytest.mark.parametrize("K,G", [(256, 128), (1024, 64), (14336, 128)])
+@pytest.mark.parametrize("M", [1, 11])
+def test_cluster_split_decode_mma(K, G, M):
+    """Cluster split-K: one cluster of S CTAs per tile, each taking an equal
+    group-aligned K range (the last one shorter, or empty when the groups do
+    not divide evenly), partial sums added through distributed shared
+    memory.  Every cluster size the selection accepts, against the oracle on
+    every output, and bit-identical on a second launch."""
+    N = 640
+    qw, a = synth.random_problem(70 + K // 64 + M, M, K, N, G, "bf16")
+    c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, "bf16"), "bf16")
+    W = packed_from(qw)
+    A = binding.acts_to_device(a, torch.bfloat16)
+    for sk in (1, 2, 3, 5, 8, 11, 16):
+        cfg = dict(kernel="decode_mma", split_k=sk, dq_warps=1)
+        C = gemm_poisoned(A, W, config=cfg)
+        torch.cuda.synchronize()
+        binding.poll_error()
+        assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, sk
+        C2 = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
         assert torch.equal(C.view(torch.int16), C2.view(torch.int16)), sk
 
@@ -431,7 +461,8 @@ def test_alternating_problems_decode_mma():
     cols = sample_indices(qw.N, 160, seed=6)
     rows = np.arange(M)
     refs = [oracle_sampled(q, a, rows, cols) for q in (qw, qw2)]
-    for cfg in (dict(kernel="decode_mma", split_k=0), dict(kernel="decode_mma", split_k=1)):
+    for cfg in (dict(kernel="decode_mma", split_k=0), dict(kernel="decode_mma", split_k=1),
+                dict(kernel="decode_mma", split_k=8, dq_warps=1)):
         first = []
         for i in range(2):
             C = gemm_poisoned(A, Ws[i], config=cfg)

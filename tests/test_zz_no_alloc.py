@@ -69,6 +69,8 @@ def _needed_scratch(W, M, cfg):
         if plan["partial_slots"] <= 1:
             return 0, 0
         return plan["tiles"] * plan["partial_slots"] * 128 * cfg["block_m"] * 4, plan["tiles"]
+    if cfg["kernel"] == "decode_mma" and cfg.get("dq_warps", 0) == 1:
+        return 0, 0          # cluster split-K: partials stay in shared memory
     if cfg["kernel"] == "decode_mma":
         # persistent stream-K grid: CTAs per SM x SMs over (tile, group) units;
         # contributors of a tile = CTAs whose ranges meet its units
@@ -105,6 +107,7 @@ CASES = [
     (1, 2048, 640, "bf16", dict(kernel="gemv", split_k=1)),
     (16, 14336, 1152, "f16", dict(kernel="decode_mma", split_k=2)),
     (3, 1024, 640, "bf16", dict(kernel="decode_mma", split_k=1)),
+    (9, 4096, 1152, "f16", dict(kernel="decode_mma", split_k=6, dq_warps=1)),
     (16, 4096, 1152, "f16", dict(kernel="tc_decode", block_m=16, dq_warps=8)),
     (40, 2048, 640, "f16", dict(kernel="tc_decode", block_m=32, dq_warps=4)),
     (300, 1024, 1152, "bf16", dict(kernel="tc", block_m=128, split_k=2, dq_warps=8)),

@@ -271,10 +271,24 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
       if (why) *why = "DECODE_MMA handles M <= 16";
       return false;
     }
-    // split_k: persistent CTAs per SM (clamped to what fits; 0 = all that fit)
+    c->block_m = 8 * decode_mma_nt8(M);
+    if (c->dq_warps == 1) {
+      // cluster split-K: split_k = CTAs per cluster, normalized to the
+      // group-aligned split that covers K
+      int per = 0;
+      const int S = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group,
+                                             c->split_k <= 0 ? 1 : c->split_k, &per);
+      if (S == 0) {
+        if (why) *why = "DECODE_MMA cluster of that size cannot be resident";
+        return false;
+      }
+      c->split_k = S;
+      return true;
+    }
+    // stream-K: split_k = persistent CTAs per SM (clamped to what fits; 0 =
+    // all that fit)
     const int occ = decode_mma_ctas_per_sm(W->dtype == TM_BF16, M, W->group);
     if (c->split_k <= 0 || c->split_k > occ) c->split_k = occ;
-    c->block_m = 8 * decode_mma_nt8(M);
     c->dq_warps = 0;
     return true;
   }
@@ -454,6 +468,14 @@ static void plan_work(const tm_packed *W, int M, const tm_config &cfg, GemmArgs 
   const int KB = W->K / 64;
   *ws_floats = 0;
   *n_counters = 0;
+  if (cfg.kernel == TM_KERNEL_DECODE_MMA && cfg.dq_warps == 1) {
+    int per = KB;
+    a->splits = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group, cfg.split_k, &per);
+    a->kb_per_split = per;
+    a->ws_slots = 1;
+    *dec_grid = W->N / 128;
+    return;
+  }
   if (cfg.kernel == TM_KERNEL_DECODE_MMA) {
     long long tiles = 0;
     int slots = 1;
@@ -505,7 +527,7 @@ static tm_status launch_planned(const void *A, const tm_packed *W, int M, const 
     CUtensorMap map;
     tm_status s = encode_act_map(A, M, W->K, bf16, cfg.block_m, 1, &map, &a.act_map_3d);
     if (s != TM_OK) return s;
-    e = launch_decode_mma(a, map, bf16, dec_grid, st);
+    e = launch_decode_mma(a, map, bf16, dec_grid, cfg.dq_warps == 1 ? a.splits : 0, st);
   } else if (cfg.kernel == TM_KERNEL_TC_DECODE) {
     CUtensorMap map;
     tm_status s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_decode_kblocks_per_stage(), &map,
@@ -891,6 +913,7 @@ static std::vector<tm_config> candidates(const tm_packed *W, int M, int dev) {
   const int splits[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32};
   if (M <= 16) {
     for (int s = 1; s <= 8; ++s) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 0});
+    for (int s : {1, 2, 3, 4, 6, 8, 12, 16}) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 1});
   }
   if (M <= 8) {
     for (int s : splits) add(tm_config{TM_KERNEL_GEMV, 0, s, 0});

@@ -203,7 +203,16 @@ __host__ __device__ constexpr int dm_smem_bytes(int nt8) { return DM_DEPTH * dm_
 //   a1, a3 = the same pairs of column c = 2mt + 1
 //            (actual K 16t + 4i + {0,1} and 16t + 4i + {2,3})
 //   b0, b1 = activation row 8 j8 + g at the same K: 8 contiguous bytes.
-template <bool BF16, int NT8, int GS>
+// CL selects the work split:
+//   false  stream-K over a persistent grid (above): fp32 partials of cut
+//          tiles in the workspace, reduced by the last CTA to arrive;
+//   true   split-K inside a thread-block cluster: grid (tiles, S) in clusters
+//          of (1, S, 1); rank r of a cluster takes the r-th of S equal,
+//          group-aligned K ranges of the tile; the partials stay in each
+//          CTA's shared memory and rank 0 adds them in rank order through
+//          distributed shared memory after a bounded mbarrier handshake (no
+//          workspace, no atomics).
+template <bool BF16, int NT8, int GS, bool CL>
 __global__ void __launch_bounds__(DM_THREADS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
   extern __shared__ uint8_t dm_smem_raw[];
@@ -213,6 +222,7 @@ __global__ void __launch_bounds__(DM_THREADS)
   constexpr int W0 = ACT_BYTES, META0 = ACT_BYTES + DM_W_BYTES;
   static_assert((D & (D - 1)) == 0 && STAGE % 1024 == 0, "ring geometry");
   __shared__ uint64_t full_bar[D], empty_bar[D];
+  __shared__ uint64_t ready_bar, done_bar;     // cluster mode: partials ready / read
   __shared__ int seg_tile[2], seg_last[2];
   __shared__ int abort_flag_s;
   volatile int *abort_flag = &abort_flag_s;
@@ -224,9 +234,22 @@ __global__ void __launch_bounds__(DM_THREADS)
   const int GR = p.K / p.group;                    // groups (units) per tile
   const long long U = static_cast<long long>(p.N / TILE_N) * GR;
   const long long Gc = gridDim.x;
-  const long long u0 = unit_begin(blockIdx.x, U, Gc);
-  const int nb = static_cast<int>(unit_begin(blockIdx.x + 1, U, Gc) - u0) * GS;   // blocks of this CTA
-  const long long b0 = u0 * GS;                    // its first block in tile-major order
+  // this CTA's blocks: nb consecutive 64-K blocks from block b0 (tile-major)
+  long long u0, b0;
+  int nb;
+  uint32_t rank = 0;
+  const int S = CL ? static_cast<int>(gridDim.y) : 1;
+  if constexpr (CL) {
+    rank = cluster_ctarank();
+    const int kb_start = static_cast<int>(rank) * p.kb_per_split;
+    nb = max(0, min(KB, kb_start + p.kb_per_split) - kb_start);
+    b0 = static_cast<long long>(blockIdx.x) * KB + kb_start;
+    u0 = b0 / GS;
+  } else {
+    u0 = unit_begin(blockIdx.x, U, Gc);
+    nb = static_cast<int>(unit_begin(blockIdx.x + 1, U, Gc) - u0) * GS;
+    b0 = u0 * GS;
+  }
   const bool has_zeros = p.zeros != nullptr;
   const int M = p.M, N = p.N;
 
@@ -235,9 +258,20 @@ __global__ void __launch_bounds__(DM_THREADS)
     mbar_init(empty_bar + threadIdx.x, 4);
     fence_mbar_init();
   }
-  if (threadIdx.x == 0) abort_flag_s = 0;
+  if (threadIdx.x == 0) {
+    abort_flag_s = 0;
+    if constexpr (CL) {
+      mbar_init(&ready_bar, static_cast<uint32_t>(S > 1 ? S - 1 : 1));
+      mbar_init(&done_bar, 1);
+      fence_mbar_init();
+    }
+  }
   __syncwarp();
-  __syncthreads();
+  if constexpr (CL) {
+    cluster_sync();   // every barrier of the cluster is initialised before any remote arrival
+  } else {
+    __syncthreads();
+  }
   pdl_launch_dependents();
   DM_TRACE(0);
 
@@ -319,6 +353,12 @@ __global__ void __launch_bounds__(DM_THREADS)
   const bool last_cut = t_last != t_first && (b0 + nb) % KB != 0;
   const int nseg_range = (first_cut ? 1 : 0) + (last_cut ? 1 : 0);
 
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int j8 = 0; j8 < NT8; ++j8)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][j8][e] = 0.f;
   int i = 0;
   int kb_c = static_cast<int>(b0 % KB), t_c = static_cast<int>(b0 / KB);
 #pragma unroll 1
@@ -408,6 +448,7 @@ __global__ void __launch_bounds__(DM_THREADS)
     // (mt, j8): column col = 32 w + 8 (2 mt + e / 2) + g of tile t_c,
     // activation row m = 8 j8 + 2t + e % 2
     float *part = nullptr;
+    if (CL && !whole) break;   // cluster mode: the one segment's sums stay in registers
     if (!whole) {
       const int jc = static_cast<int>(blockIdx.x) - cta_of_unit(static_cast<long long>(t_c) * GR, U, Gc);
       part = p.ws + (static_cast<size_t>(t_c) * p.ws_slots + jc) * M * TILE_N;
@@ -436,6 +477,77 @@ __global__ void __launch_bounds__(DM_THREADS)
   }
   DM_TRACE(3);
   (void)nseg;
+  if constexpr (CL) {
+    if (S == 1) return;   // the whole tile was written
+    // Cluster split-K: every consumer thread leaves its 8 NT8 sums at its own
+    // slot of this CTA's (now idle) ring; rank 0 adds the slots of ranks
+    // 1..S-1 to its own, in rank order, and writes C.  The handshake: each
+    // rank's thread 0 arrives on rank 0's ready barrier (release, cluster
+    // scope) once its consumers have stored; rank 0 waits for all S - 1,
+    // reads, then arrives on every rank's done barrier, which each rank waits
+    // for before exiting (its shared memory must outlive the reads).
+    // Every wait is bounded.  A rank whose own pipeline gave up still takes
+    // part (C is then undefined, the error word says why), and rank 0 waits
+    // for the others several times longer than any of them can be held up by
+    // its own bounded waits, so that no arrival reaches an exited CTA.
+    constexpr int NV = 2 * NT8 * 4;
+    float *slot = reinterpret_cast<float *>(smem) + threadIdx.x * NV;
+    if (rank != 0) {
+      named_bar_sync(1, DM_CONSUMERS);   // no warp still reads the ring
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int j8 = 0; j8 < NT8; ++j8)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) slot[(mt * NT8 + j8) * 4 + e] = acc[mt][j8][e];
+      named_bar_sync(1, DM_CONSUMERS);
+      if (threadIdx.x == 0) {
+        mbar_arrive_remote(mapa_shared(smem_u32(&ready_bar), 0));
+        mbar_wait_bounded(&done_bar, 0, 16 * p.limit_ns, nullptr, p.err, SITE_CLUSTER_DONE, rank);
+      }
+      named_bar_sync(1, DM_CONSUMERS);
+      return;
+    }
+    if (threadIdx.x == 0) {
+      if (!mbar_wait_bounded(&ready_bar, 0, 8 * p.limit_ns, nullptr, p.err, SITE_CLUSTER_READY, 0))
+        *abort_flag = 1;
+      fence_acq_rel_cluster();
+    }
+    named_bar_sync(1, DM_CONSUMERS);
+    if (*abort_flag == 0) {
+      fence_acq_rel_cluster();
+      const uint32_t my_slot = smem_u32(slot);
+      for (int r = 1; r < S; ++r) {
+        const uint32_t remote = mapa_shared(my_slot, static_cast<uint32_t>(r));
+#pragma unroll
+        for (int q = 0; q < NV / 4; ++q) {
+          const float4 v = ld_shared_cluster_f4(remote + 16 * q);
+          float *a = &acc[0][0][0] + 4 * q;
+          a[0] += v.x;
+          a[1] += v.y;
+          a[2] += v.z;
+          a[3] += v.w;
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int j8 = 0; j8 < NT8; ++j8)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int m = 8 * j8 + 2 * t + (e & 1);
+            const int col = 32 * warp + 8 * (2 * mt + (e >> 1)) + g;
+            if (m < M)
+              p.C[static_cast<size_t>(m) * N + static_cast<size_t>(blockIdx.x) * TILE_N + col] =
+                  f32_to_bits16<BF16>(acc[mt][j8][e]);
+          }
+    }
+    // every rank may leave once rank 0 is done with its shared memory
+    named_bar_sync(1, DM_CONSUMERS);
+    if (threadIdx.x == 0)
+      for (int r = 1; r < S; ++r) mbar_arrive_remote(mapa_shared(smem_u32(&done_bar), static_cast<uint32_t>(r)));
+    return;
+  }
   if (nseg_range == 0) return;   // every tile the range touches was whole
 
   // publish the cut segments: the barrier orders every consumer's partial
@@ -465,20 +577,48 @@ __global__ void __launch_bounds__(DM_THREADS)
     const int tt = seg_tile[k];
     const int ncontrib = cta_of_unit(static_cast<long long>(tt) * GR + GR - 1, U, Gc) -
                          cta_of_unit(static_cast<long long>(tt) * GR, U, Gc) + 1;
+    // Thread x adds the float4s x + 128 r (r < R) of each partial: 4
+    // consecutive columns of one row.  QB contributors' loads are issued
+    // before any of them is added, so that a reduction costs about
+    // ncontrib / QB L2 round trips; the sums still run in contributor order.
     const float *base = p.ws + static_cast<size_t>(tt) * p.ws_slots * M * TILE_N;
-    for (int idx = threadIdx.x; idx < M * TILE_N; idx += DM_CONSUMERS) {
-      float sum = 0.f;
-      int q0 = 0;
-      for (; q0 + 4 <= ncontrib; q0 += 4) {
-        float v[4];
+    constexpr int RMAX = 2 * NT8;          // float4s per thread per partial (M <= 8 NT8)
+    constexpr int QB = 8 / RMAX;
+    const int R = (M * (TILE_N / 4) + DM_CONSUMERS - 1) / DM_CONSUMERS;
+    float4 sum[RMAX];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = __ldcg(base + static_cast<size_t>(q0 + q) * M * TILE_N + idx);
+    for (int r = 0; r < RMAX; ++r) sum[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < ncontrib; q0 += QB) {
+      float4 v[QB][RMAX];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) sum += v[q];
+      for (int q = 0; q < QB; ++q)
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          const int f4 = threadIdx.x + DM_CONSUMERS * r;
+          v[q][r] = (q0 + q < ncontrib && r < R && f4 < M * (TILE_N / 4))
+                        ? __ldcg(reinterpret_cast<const float4 *>(base + static_cast<size_t>(q0 + q) * M * TILE_N) + f4)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+      for (int q = 0; q < QB; ++q)
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          sum[r].x += v[q][r].x;
+          sum[r].y += v[q][r].y;
+          sum[r].z += v[q][r].z;
+          sum[r].w += v[q][r].w;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      const int f4 = threadIdx.x + DM_CONSUMERS * r;
+      if (r < R && f4 < M * (TILE_N / 4)) {
+        const int m = f4 / (TILE_N / 4), col = 4 * (f4 % (TILE_N / 4));
+        const uint32_t lo = f32_to_bits16<BF16>(sum[r].x) | (static_cast<uint32_t>(f32_to_bits16<BF16>(sum[r].y)) << 16);
+        const uint32_t hi = f32_to_bits16<BF16>(sum[r].z) | (static_cast<uint32_t>(f32_to_bits16<BF16>(sum[r].w)) << 16);
+        *reinterpret_cast<uint2 *>(p.C + static_cast<size_t>(m) * N + static_cast<size_t>(tt) * TILE_N + col) =
+            make_uint2(lo, hi);
       }
-      for (; q0 < ncontrib; ++q0) sum += __ldcg(base + static_cast<size_t>(q0) * M * TILE_N + idx);
-      const int m = idx / TILE_N, col = idx % TILE_N;
-      p.C[static_cast<size_t>(m) * N + static_cast<size_t>(tt) * TILE_N + col] = f32_to_bits16<BF16>(sum);
     }
     if (threadIdx.x == 0) p.counters[tt] = 0u;
   }
@@ -486,17 +626,27 @@ __global__ void __launch_bounds__(DM_THREADS)
 }
 
 template <bool BF16, int NT8, int GS>
-static cudaError_t launch_dm_t(const GemmArgs &a, const CUtensorMap &tmap, int grid, cudaStream_t st) {
-  auto kern = decode_mma_kernel<BF16, NT8, GS>;
-  cudaError_t e = smem_optin<decode_mma_kernel<BF16, NT8, GS>>(dm_smem_bytes(NT8));
+static cudaError_t launch_dm_t(const GemmArgs &a, const CUtensorMap &tmap, int grid, int cluster,
+                               cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(dm_smem_bytes(NT8));
+  if (cluster > 0) {
+    auto kern = decode_mma_kernel<BF16, NT8, GS, true>;
+    cudaError_t e = cluster_optin<decode_mma_kernel<BF16, NT8, GS, true>>(dm_smem_bytes(NT8));
+    if (e != cudaSuccess) return e;
+    return launch_kernel_cluster(kern, dim3(grid, cluster), dim3(DM_THREADS), smem, st, a.pdl != 0,
+                                 static_cast<unsigned>(cluster), tmap, a);
+  }
+  auto kern = decode_mma_kernel<BF16, NT8, GS, false>;
+  cudaError_t e = smem_optin<decode_mma_kernel<BF16, NT8, GS, false>>(dm_smem_bytes(NT8));
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, dim3(grid), dim3(DM_THREADS), static_cast<size_t>(dm_smem_bytes(NT8)), st,
-                       a.pdl != 0, tmap, a);
+  return launch_kernel(kern, dim3(grid), dim3(DM_THREADS), smem, st, a.pdl != 0, tmap, a);
 }
 
 template <bool BF16, int NT8>
-static cudaError_t launch_dm_g(const GemmArgs &a, const CUtensorMap &tmap, int grid, cudaStream_t st) {
-  return a.group == 64 ? launch_dm_t<BF16, NT8, 1>(a, tmap, grid, st) : launch_dm_t<BF16, NT8, 2>(a, tmap, grid, st);
+static cudaError_t launch_dm_g(const GemmArgs &a, const CUtensorMap &tmap, int grid, int cluster,
+                               cudaStream_t st) {
+  return a.group == 64 ? launch_dm_t<BF16, NT8, 1>(a, tmap, grid, cluster, st)
+                       : launch_dm_t<BF16, NT8, 2>(a, tmap, grid, cluster, st);
 }
 
 // Resident CTAs per SM of the kernel instantiation for (bf16, M, group).
@@ -508,9 +658,9 @@ static int dm_occupancy_t() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxOptinDevices) return 1;
   std::call_once(once[dev], [&] {
     int v = 0;
-    if (smem_optin<decode_mma_kernel<BF16, NT8, GS>>(dm_smem_bytes(NT8)) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, decode_mma_kernel<BF16, NT8, GS>, DM_THREADS,
-                                                      dm_smem_bytes(NT8)) != cudaSuccess ||
+    if (smem_optin<decode_mma_kernel<BF16, NT8, GS, false>>(dm_smem_bytes(NT8)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, decode_mma_kernel<BF16, NT8, GS, false>,
+                                                      DM_THREADS, dm_smem_bytes(NT8)) != cudaSuccess ||
         v <= 0)
       v = 1;
     occ[dev] = v;
@@ -550,11 +700,68 @@ void decode_mma_plan(int M, int N, int K, int group, int max_ctas, int *grid, lo
   (void)M;
 }
 
+// Whether clusters of S CTAs (1..16) of the cluster-mode instantiation can
+// be resident at all; computed once per (device, S).
+template <bool BF16, int NT8, int GS>
+static bool dm_cluster_fits_t(int S) {
+  static std::once_flag once[kMaxOptinDevices][17];
+  static bool fits[kMaxOptinDevices][17];
+  int dev = 0;
+  if (S < 1 || S > 16 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxOptinDevices) return false;
+  std::call_once(once[dev][S], [&] {
+    fits[dev][S] = false;
+    if (cluster_optin<decode_mma_kernel<BF16, NT8, GS, true>>(dm_smem_bytes(NT8)) != cudaSuccess) return;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1, S);
+    cfg.blockDim = dim3(DM_THREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(dm_smem_bytes(NT8));
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = S;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    fits[dev][S] = cudaOccupancyMaxActiveClusters(&n, decode_mma_kernel<BF16, NT8, GS, true>, &cfg) ==
+                       cudaSuccess &&
+                   n > 0;
+    (void)cudaGetLastError();
+  });
+  return fits[dev][S];
+}
+
+template <bool BF16, int NT8>
+static bool dm_cluster_fits_g(int group, int S) {
+  return group == 64 ? dm_cluster_fits_t<BF16, NT8, 1>(S) : dm_cluster_fits_t<BF16, NT8, 2>(S);
+}
+
+int decode_mma_cluster_split(bool bf16, int M, int K, int group, int requested, int *kb_per_split) {
+  const int KB = K / 64, GS = group / 64;
+  const int req = std::max(1, std::min(requested, 16));
+  int per = (KB + req - 1) / req;
+  per = (per + GS - 1) / GS * GS;
+  const int S = (KB + per - 1) / per;
+  bool fits = false;
+  switch (decode_mma_nt8(M)) {
+    case 1: fits = bf16 ? dm_cluster_fits_g<true, 1>(group, S) : dm_cluster_fits_g<false, 1>(group, S); break;
+    case 2: fits = bf16 ? dm_cluster_fits_g<true, 2>(group, S) : dm_cluster_fits_g<false, 2>(group, S); break;
+    default: break;
+  }
+  if (!fits) return 0;
+  *kb_per_split = per;
+  return S;
+}
+
 cudaError_t launch_decode_mma(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int grid,
-                              cudaStream_t st) {
+                              int cluster, cudaStream_t st) {
   switch (decode_mma_nt8(a.M)) {
-    case 1: return bf16 ? launch_dm_g<true, 1>(a, tmap_a, grid, st) : launch_dm_g<false, 1>(a, tmap_a, grid, st);
-    case 2: return bf16 ? launch_dm_g<true, 2>(a, tmap_a, grid, st) : launch_dm_g<false, 2>(a, tmap_a, grid, st);
+    case 1:
+      return bf16 ? launch_dm_g<true, 1>(a, tmap_a, grid, cluster, st)
+                  : launch_dm_g<false, 1>(a, tmap_a, grid, cluster, st);
+    case 2:
+      return bf16 ? launch_dm_g<true, 2>(a, tmap_a, grid, cluster, st)
+                  : launch_dm_g<false, 2>(a, tmap_a, grid, cluster, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -67,6 +67,32 @@ inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The same with thread-block clusters of cluster_y CTAs along grid.y.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                         cudaStream_t st, bool pdl, unsigned cluster_y, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeClusterDimension;
+  attr[n].val.clusterDim.x = 1;
+  attr[n].val.clusterDim.y = cluster_y;
+  attr[n].val.clusterDim.z = 1;
+  ++n;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Opts kernel Kern into `bytes` of dynamic shared memory on the current
 // device.  The attribute belongs to the device's context, so it is set once
 // per device; concurrent first calls from several host threads are safe.
@@ -82,6 +108,22 @@ inline cudaError_t smem_optin(int bytes) {
   if (dev < 0 || dev >= kMaxOptinDevices) return cudaErrorInvalidDevice;
   std::call_once(once[dev], [&] {
     result[dev] = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+  return result[dev];
+}
+
+// smem_optin, and clusters of up to 16 CTAs (beyond the portable 8).
+template <auto Kern>
+inline cudaError_t cluster_optin(int bytes) {
+  static std::once_flag once[kMaxOptinDevices];
+  static cudaError_t result[kMaxOptinDevices];
+  int dev = 0;
+  cudaError_t e = smem_optin<Kern>(bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::call_once(once[dev], [&] {
+    result[dev] = cudaFuncSetAttribute(Kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   return result[dev];
 }
@@ -114,20 +156,26 @@ void tc_decode_plan(int M, int N, int K, int block_m, int sms, int *grid, long l
 cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                              int dq_warps, int grid, cudaStream_t st);
 
-// Persistent stream-K kernel with register-operand tensor-core MMAs
-// (M <= 16; decode_mma_nt8(M) n8 tiles of activation rows, 0 if M is too
-// large).  decode_mma_ctas_per_sm: resident CTAs per SM of the instantiation
-// for (bf16, M, group); decode_mma_plan: the grid for at most max_ctas CTAs,
-// the tile count (split-K counters) and the fp32 partial slots per tile
-// (1: no tile is cut between CTAs).
+// Kernel with register-operand tensor-core MMAs (M <= 16; decode_mma_nt8(M)
+// n8 tiles of activation rows, 0 if M is too large).  Stream-K mode:
+// decode_mma_ctas_per_sm gives the resident CTAs per SM of the instantiation
+// for (bf16, M, group); decode_mma_plan the grid for at most max_ctas CTAs,
+// the tile count (split-K counters) and the fp32 partial slots per tile (1:
+// no tile is cut between CTAs).  Cluster mode: decode_mma_cluster_split
+// turns a requested cluster size into the group-aligned 64-K blocks per
+// split and the clusters size that covers K with them (0 if no cluster of
+// that size can be resident).
 int decode_mma_nt8(int M);
 int decode_mma_ctas_per_sm(bool bf16, int M, int group);
 void decode_mma_plan(int M, int N, int K, int group, int max_ctas, int *grid, long long *tiles,
                      int *slots);
+int decode_mma_cluster_split(bool bf16, int M, int K, int group, int requested, int *kb_per_split);
 // tmap_a: activation tensor map with box 64 x (8 * decode_mma_nt8(M)) and the
-// 128-byte swizzle (3-D with one 64-K block per copy, or 2-D)
+// 128-byte swizzle (3-D with one 64-K block per copy, or 2-D).  cluster = 0:
+// stream-K over `grid` CTAs; cluster = S > 0: grid (grid tiles, S) in
+// clusters of S with a.kb_per_split blocks per split.
 cudaError_t launch_decode_mma(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int grid,
-                              cudaStream_t st);
+                              int cluster, cudaStream_t st);
 
 // Bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t st);
