@@ -68,13 +68,16 @@ enum {
                               register-operand tensor-core MMAs (mma.sync),
                               group scale applied in fp32.  Two work splits,
                               chosen by dq_warps:
-                                0  persistent stream-K grid; split_k = CTAs
-                                   per SM (0: all that fit);
-                                1  one thread-block cluster of split_k CTAs
-                                   (1..16) per 128-column tile, each taking
-                                   an equal group-aligned K range; partial
-                                   sums added through distributed shared
-                                   memory (no workspace) */
+                                4, 8, 16 (0 = 4)  persistent stream-K grid
+                                   of CTAs with that many consumer warps;
+                                   split_k = CTAs per SM (0: all that fit);
+                                1, 2  one thread-block cluster of split_k
+                                   CTAs (1..16; fewer for large M) per
+                                   128-column tile, each with 4 or 8
+                                   consumer warps and an equal group-aligned
+                                   K range; partial sums added through
+                                   distributed shared memory (no
+                                   workspace) */
 };
 
 /* A kernel variant: family, rows of A per CTA tile (TC: 16, 32, 64, 128 or
@@ -87,7 +90,7 @@ typedef struct {
   int32_t dq_warps; /* TC: dequant warps per CTA, 4, 8 or 16 (0 = default);
                        each group of 4 dequantizes every (dq_warps/4)-th stage;
                        TC_DECODE: 4, 8 or 12 dequant warps; DECODE_MMA: the
-                       work split (0 stream-K, 1 cluster split-K) */
+                       work split and consumer warps (see above) */
 } tm_config;
 
 /* Opaque packed weight, owned by the library until tm_packed_free. */

@@ -36,14 +36,18 @@ DECODE_ILLEGAL = {(64, 12), (64, 16)}   # 3-4 warpgroups leave too few TMEM colu
 
 def _decode_variants(M):
     """Every legal tcgen05-decode variant and, for M <= 16, the register-MMA
-    decode kernel on persistent grids of one and of all resident CTAs per SM
-    and in clusters of 4 and of 16 CTAs per tile."""
+    decode kernel on persistent grids of one and of all resident CTAs per SM,
+    with one, two and four K-groups, and in clusters of 4 and of 16 CTAs per
+    tile."""
     out = [dict(kernel="tc_decode", block_m=bm, dq_warps=dq)
            for bm in (16, 32, 64) for dq in (4, 8, 12, 16) if (bm, dq) not in DECODE_ILLEGAL]
     if M <= 16:
         out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=0),
+                dict(kernel="decode_mma", split_k=0, dq_warps=8),
+                dict(kernel="decode_mma", split_k=1, dq_warps=16),
                 dict(kernel="decode_mma", split_k=4, dq_warps=1),
-                dict(kernel="decode_mma", split_k=16, dq_warps=1)]
+                dict(kernel="decode_mma", split_k=16, dq_warps=1),
+                dict(kernel="decode_mma", split_k=8, dq_warps=2)]
     return out
 
 
@@ -53,6 +57,8 @@ def _variants(M):
         out += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
     if M <= 16:
         out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=3),
+                dict(kernel="decode_mma", split_k=2, dq_warps=8),
+                dict(kernel="decode_mma", split_k=1, dq_warps=16),
                 dict(kernel="decode_mma", split_k=3, dq_warps=1)]
     for bm in (16, 32, 64, 128, 256):
         for sk in (1, 3):
@@ -194,7 +200,8 @@ def test_identity_activation_reproduces_weight():
         assert np.array_equal(bits_of(C), w), cfg
     # the register-MMA decode kernel takes at most 16 rows: slabs of I
     for k0 in (0, 96, 240):
-        for cfg in (dict(split_k=1), dict(split_k=2), dict(split_k=4, dq_warps=1)):
+        for cfg in (dict(split_k=1), dict(split_k=2), dict(split_k=1, dq_warps=16),
+                    dict(split_k=4, dq_warps=1)):
             C = gemm_poisoned(A[k0:k0 + 16].contiguous(), W, config=dict(kernel="decode_mma", **cfg))
             torch.cuda.synchronize()
             assert np.array_equal(bits_of(C), w[k0:k0 + 16]), (k0, cfg)
@@ -282,6 +289,7 @@ def test_long_k_decode_mma(M, G, dt):
     W = packed_from(qw)
     A = binding.acts_to_device(a, TORCH_DT[dt])
     cfgs = [dict(split_k=sk) for sk in (1, 2, 3, 5, 0)] + \
+        [dict(split_k=sk, dq_warps=dq) for sk in (1, 2) for dq in (8, 16)] + \
         [dict(split_k=sk, dq_warps=1) for sk in (1, 2, 7, 16)]
     for cfg in cfgs:
         C = gemm_poisoned(A, W, config=dict(kernel="decode_mma", **cfg))
@@ -300,15 +308,17 @@ def test_stream_k_segments_decode_mma(K, N, G, M):
     c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, "f16"), "f16")
     W = packed_from(qw)
     A = binding.acts_to_device(a, torch.float16)
-    for sk in (1, 2, 0):
-        C = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
+    for cfg in [dict(split_k=sk) for sk in (1, 2, 0)] + \
+            [dict(split_k=sk, dq_warps=dq) for dq in (8, 16) for sk in (1, 0)]:
+        cfg = dict(kernel="decode_mma", **cfg)
+        C = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
         binding.poll_error()
-        assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, sk
+        assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, cfg
         # determinism: a second launch is bit-identical
-        C2 = gemm_poisoned(A, W, config=dict(kernel="decode_mma", split_k=sk))
+        C2 = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
-        assert torch.equal(C.view(torch.int16), C2.view(torch.int16)), sk
+        assert torch.equal(C.view(torch.int16), C2.view(torch.int16)), cfg
 
 
 @pytest.mark.parametrize("K,G", [(256, 128), (1024, 64), (14336, 128)])
@@ -317,15 +327,16 @@ def test_cluster_split_decode_mma(K, G, M):
     """Cluster split-K: one cluster of S CTAs per tile, each taking an equal
     group-aligned K range (the last one shorter, or empty when the groups do
     not divide evenly), partial sums added through distributed shared
-    memory.  Every cluster size the selection accepts, against the oracle on
-    every output, and bit-identical on a second launch."""
+    memory; one and two K-groups per CTA.  Cluster sizes up to 16 (capped
+    for larger M), against the oracle on every output, and bit-identical on
+    a second launch."""
     N = 640
     qw, a = synth.random_problem(70 + K // 64 + M, M, K, N, G, "bf16")
     c_ref = oracle.gemm_ref(a, oracle.dequant_bits(qw.q, qw.scales, qw.zeros, G, "bf16"), "bf16")
     W = packed_from(qw)
     A = binding.acts_to_device(a, torch.bfloat16)
-    for sk in (1, 2, 3, 5, 8, 11, 16):
-        cfg = dict(kernel="decode_mma", split_k=sk, dq_warps=1)
+    for sk, dq in [(s, 1) for s in (1, 2, 3, 5, 8, 11, 16)] + [(s, 2) for s in (2, 5, 16)]:
+        cfg = dict(kernel="decode_mma", split_k=sk, dq_warps=dq)
         C = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
         binding.poll_error()
@@ -348,11 +359,16 @@ def test_illegal_variants_are_rejected():
         with pytest.raises(binding.TmError) as e:
             binding.gemm(A, W, config=dict(kernel="tc_decode", block_m=bm, dq_warps=dq))
         assert e.value.status == binding.TM_ERR_UNSUPPORTED
-    # the register-MMA decode kernel takes at most 16 rows
+    # the register-MMA decode kernel takes at most 16 rows, and 4, 8 or 16
+    # consumer warps (1: clusters)
     A17 = binding.acts_to_device(np.zeros((17, 512), np.uint16), torch.float16)
     with pytest.raises(binding.TmError) as e:
         binding.gemm(A17, W, config=dict(kernel="decode_mma"))
     assert e.value.status == binding.TM_ERR_UNSUPPORTED
+    for dq in (3, 12, 32):
+        with pytest.raises(binding.TmError) as e:
+            binding.gemm(A[:4].contiguous(), W, config=dict(kernel="decode_mma", dq_warps=dq))
+        assert e.value.status == binding.TM_ERR_UNSUPPORTED
 
 
 def test_m_zero_is_noop_and_argument_errors():
@@ -462,6 +478,7 @@ def test_alternating_problems_decode_mma():
     rows = np.arange(M)
     refs = [oracle_sampled(q, a, rows, cols) for q in (qw, qw2)]
     for cfg in (dict(kernel="decode_mma", split_k=0), dict(kernel="decode_mma", split_k=1),
+                dict(kernel="decode_mma", split_k=1, dq_warps=16),
                 dict(kernel="decode_mma", split_k=8, dq_warps=1)):
         first = []
         for i in range(2):

@@ -108,6 +108,8 @@ CASES = [
     (16, 14336, 1152, "f16", dict(kernel="decode_mma", split_k=2)),
     (3, 1024, 640, "bf16", dict(kernel="decode_mma", split_k=1)),
     (9, 4096, 1152, "f16", dict(kernel="decode_mma", split_k=6, dq_warps=1)),
+    (2, 8192, 1152, "bf16", dict(kernel="decode_mma", split_k=1, dq_warps=16)),
+    (12, 4096, 640, "f16", dict(kernel="decode_mma", split_k=2, dq_warps=8)),
     (16, 4096, 1152, "f16", dict(kernel="tc_decode", block_m=16, dq_warps=8)),
     (40, 2048, 640, "f16", dict(kernel="tc_decode", block_m=32, dq_warps=4)),
     (300, 1024, 1152, "bf16", dict(kernel="tc", block_m=128, split_k=2, dq_warps=8)),

@@ -272,11 +272,12 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
       return false;
     }
     c->block_m = 8 * decode_mma_nt8(M);
-    if (c->dq_warps == 1) {
-      // cluster split-K: split_k = CTAs per cluster, normalized to the
-      // group-aligned split that covers K
+    if (c->dq_warps == 1 || c->dq_warps == 2) {
+      // cluster split-K with dq_warps K-groups of four consumer warps:
+      // split_k = CTAs per cluster, normalized to the group-aligned split
+      // that covers K
       int per = 0;
-      const int S = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group,
+      const int S = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group, c->dq_warps,
                                              c->split_k <= 0 ? 1 : c->split_k, &per);
       if (S == 0) {
         if (why) *why = "DECODE_MMA cluster of that size cannot be resident";
@@ -285,11 +286,15 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
       c->split_k = S;
       return true;
     }
-    // stream-K: split_k = persistent CTAs per SM (clamped to what fits; 0 =
-    // all that fit)
-    const int occ = decode_mma_ctas_per_sm(W->dtype == TM_BF16, M, W->group);
+    // stream-K: dq_warps = consumer warps per CTA (4, 8 or 16; 0 = 4),
+    // split_k = persistent CTAs per SM (clamped to what fits; 0 = all that fit)
+    if (c->dq_warps == 0) c->dq_warps = 4;
+    if (c->dq_warps != 4 && c->dq_warps != 8 && c->dq_warps != 16) {
+      if (why) *why = "DECODE_MMA takes dq_warps 4, 8 or 16 (stream-K) or 1, 2 (clusters)";
+      return false;
+    }
+    const int occ = decode_mma_ctas_per_sm(W->dtype == TM_BF16, M, W->group, c->dq_warps / 4);
     if (c->split_k <= 0 || c->split_k > occ) c->split_k = occ;
-    c->dq_warps = 0;
     return true;
   }
   if (c->split_k <= 0) c->split_k = 1;
@@ -363,11 +368,18 @@ static tm_config default_config(const tm_packed *W, int M, int dev) {
   const int sms = sm_count(dev);
   tm_config c{};
   std::string why;
-  if (M <= 2) {
-    const int strips = W->N / 64;
-    c = tm_config{TM_KERNEL_GEMV, 0, std::max(1, (3 * sms + strips / 2) / strips), 0};
-    c.split_k = std::min(c.split_k, KB);
-    while (!normalize_config(W, M, &c, &why) && c.split_k < KB) c.split_k = std::min(KB, c.split_k * 2);
+  // Measured on GB300 (graphs of back-to-back launches over weights larger
+  // than L2): up to 4 rows, weights of at most 16 MB run fastest in clusters
+  // of 8 CTAs per tile (no split-K workspace round trip); otherwise up to 8
+  // rows the persistent stream-K grid of the register-MMA kernel; beyond,
+  // the tcgen05 decode kernel up to 64 rows and the tcgen05 kernel after.
+  const double wbytes = static_cast<double>(W->N) * W->K / 2;
+  if (M <= 4 && wbytes <= 16e6) {
+    c = tm_config{TM_KERNEL_DECODE_MMA, 0, 8, 1};
+    if (normalize_config(W, M, &c, &why)) return c;
+  }
+  if (M <= 8) {
+    c = tm_config{TM_KERNEL_DECODE_MMA, 0, 0, 4};
     if (normalize_config(W, M, &c, &why)) return c;
   }
   if (M <= 64) {
@@ -468,9 +480,9 @@ static void plan_work(const tm_packed *W, int M, const tm_config &cfg, GemmArgs 
   const int KB = W->K / 64;
   *ws_floats = 0;
   *n_counters = 0;
-  if (cfg.kernel == TM_KERNEL_DECODE_MMA && cfg.dq_warps == 1) {
+  if (cfg.kernel == TM_KERNEL_DECODE_MMA && (cfg.dq_warps == 1 || cfg.dq_warps == 2)) {
     int per = KB;
-    a->splits = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group, cfg.split_k, &per);
+    a->splits = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group, cfg.dq_warps, cfg.split_k, &per);
     a->kb_per_split = per;
     a->ws_slots = 1;
     *dec_grid = W->N / 128;
@@ -527,7 +539,8 @@ static tm_status launch_planned(const void *A, const tm_packed *W, int M, const 
     CUtensorMap map;
     tm_status s = encode_act_map(A, M, W->K, bf16, cfg.block_m, 1, &map, &a.act_map_3d);
     if (s != TM_OK) return s;
-    e = launch_decode_mma(a, map, bf16, dec_grid, cfg.dq_warps == 1 ? a.splits : 0, st);
+    e = cfg.dq_warps <= 2 ? launch_decode_mma(a, map, bf16, cfg.dq_warps, dec_grid, a.splits, st)
+                          : launch_decode_mma(a, map, bf16, cfg.dq_warps / 4, dec_grid, 0, st);
   } else if (cfg.kernel == TM_KERNEL_TC_DECODE) {
     CUtensorMap map;
     tm_status s = encode_act_map(A, M, W->K, bf16, cfg.block_m, tc_decode_kblocks_per_stage(), &map,
@@ -912,8 +925,11 @@ static std::vector<tm_config> candidates(const tm_packed *W, int M, int dev) {
   add(default_config(W, M, dev));
   const int splits[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32};
   if (M <= 16) {
-    for (int s = 1; s <= 8; ++s) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 0});
-    for (int s : {1, 2, 3, 4, 6, 8, 12, 16}) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 1});
+    for (int s = 1; s <= 8; ++s) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 4});
+    for (int s = 1; s <= 2; ++s) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 8});
+    add(tm_config{TM_KERNEL_DECODE_MMA, 0, 1, 16});
+    for (int s : {2, 4, 6, 8, 12, 16}) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 1});
+    for (int s : {2, 4, 8}) add(tm_config{TM_KERNEL_DECODE_MMA, 0, s, 2});
   }
   if (M <= 8) {
     for (int s : splits) add(tm_config{TM_KERNEL_GEMV, 0, s, 0});

@@ -157,24 +157,25 @@ cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool 
                              int dq_warps, int grid, cudaStream_t st);
 
 // Kernel with register-operand tensor-core MMAs (M <= 16; decode_mma_nt8(M)
-// n8 tiles of activation rows, 0 if M is too large).  Stream-K mode:
+// n8 tiles of activation rows, 0 if M is too large; kgroups = 1, 2 or 4
+// K-groups of four consumer warps per CTA).  Stream-K mode:
 // decode_mma_ctas_per_sm gives the resident CTAs per SM of the instantiation
-// for (bf16, M, group); decode_mma_plan the grid for at most max_ctas CTAs,
+// for (bf16, M, group, kgroups); decode_mma_plan the grid for at most max_ctas CTAs,
 // the tile count (split-K counters) and the fp32 partial slots per tile (1:
 // no tile is cut between CTAs).  Cluster mode: decode_mma_cluster_split
 // turns a requested cluster size into the group-aligned 64-K blocks per
-// split and the clusters size that covers K with them (0 if no cluster of
+// split and the cluster size that covers K with them (0 if no cluster of
 // that size can be resident).
 int decode_mma_nt8(int M);
-int decode_mma_ctas_per_sm(bool bf16, int M, int group);
+int decode_mma_ctas_per_sm(bool bf16, int M, int group, int kgroups);
 void decode_mma_plan(int M, int N, int K, int group, int max_ctas, int *grid, long long *tiles,
                      int *slots);
-int decode_mma_cluster_split(bool bf16, int M, int K, int group, int requested, int *kb_per_split);
+int decode_mma_cluster_split(bool bf16, int M, int K, int group, int kgroups, int requested, int *kb_per_split);
 // tmap_a: activation tensor map with box 64 x (8 * decode_mma_nt8(M)) and the
 // 128-byte swizzle (3-D with one 64-K block per copy, or 2-D).  cluster = 0:
 // stream-K over `grid` CTAs; cluster = S > 0: grid (grid tiles, S) in
-// clusters of S with a.kb_per_split blocks per split.
-cudaError_t launch_decode_mma(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int grid,
+// clusters of S with a.kb_per_split blocks per split (kgroups 1 or 2).
+cudaError_t launch_decode_mma(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int kgroups, int grid,
                               int cluster, cudaStream_t st);
 
 // Bounded-wait self-test kernel.

@@ -21,9 +21,7 @@ enum WaitSite : unsigned {
   SITE_EPI_ACCUM = 6,
   SITE_DRAIN_TMA = 7,
   SITE_DRAIN_MMA = 8,
-  SITE_SELFTEST = 9,
-  SITE_CLUSTER_READY = 10,
-  SITE_CLUSTER_DONE = 11
+  SITE_SELFTEST = 9
 };
 
 // Geometry of the packed weight (see include/tmw4.h): 128-column tiles,
