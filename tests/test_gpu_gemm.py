@@ -38,7 +38,7 @@ def _decode_variants(M):
     """Every legal tcgen05-decode variant and, for M <= 16, the register-MMA
     decode kernel on persistent grids of one and of all resident CTAs per SM,
     with one, two and four K-groups, and in clusters of 4 and of 16 CTAs per
-    tile."""
+    tile, and the tensor-core GEMV."""
     out = [dict(kernel="tc_decode", block_m=bm, dq_warps=dq)
            for bm in (16, 32, 64) for dq in (4, 8, 12, 16) if (bm, dq) not in DECODE_ILLEGAL]
     if M <= 16:
@@ -47,7 +47,8 @@ def _decode_variants(M):
                 dict(kernel="decode_mma", split_k=1, dq_warps=16),
                 dict(kernel="decode_mma", split_k=4, dq_warps=1),
                 dict(kernel="decode_mma", split_k=16, dq_warps=1),
-                dict(kernel="decode_mma", split_k=8, dq_warps=2)]
+                dict(kernel="decode_mma", split_k=8, dq_warps=2),
+                dict(kernel="gemv", split_k=2, dq_warps=1)]
     return out
 
 
@@ -55,6 +56,8 @@ def _variants(M):
     out = []
     if M <= 8:
         out += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
+    if M <= 16:
+        out += [dict(kernel="gemv", split_k=1, dq_warps=1), dict(kernel="gemv", split_k=3, dq_warps=1)]
     if M <= 16:
         out += [dict(kernel="decode_mma", split_k=1), dict(kernel="decode_mma", split_k=3),
                 dict(kernel="decode_mma", split_k=2, dq_warps=8),
@@ -205,6 +208,11 @@ def test_identity_activation_reproduces_weight():
             C = gemm_poisoned(A[k0:k0 + 16].contiguous(), W, config=dict(kernel="decode_mma", **cfg))
             torch.cuda.synchronize()
             assert np.array_equal(bits_of(C), w[k0:k0 + 16]), (k0, cfg)
+        # the tensor-core GEMV takes up to 16 rows too
+        for sk in (1, 3):
+            C = gemm_poisoned(A[k0:k0 + 16].contiguous(), W, config=dict(kernel="gemv", split_k=sk, dq_warps=1))
+            torch.cuda.synchronize()
+            assert np.array_equal(bits_of(C), w[k0:k0 + 16]), (k0, sk)
     binding.poll_error()
 
 
@@ -382,6 +390,11 @@ def test_m_zero_is_noop_and_argument_errors():
     with pytest.raises(binding.TmError) as e:
         binding.gemm(A9, W, config=dict(kernel="gemv"))     # GEMV takes M <= 8
     assert e.value.status == binding.TM_ERR_UNSUPPORTED
+    A17 = binding.acts_to_device(np.zeros((17, 256), np.uint16), torch.float16)
+    for dq in (1, 2):                                       # tensor-core GEMV: M <= 16; dq_warps 0 or 1
+        with pytest.raises(binding.TmError) as e:
+            binding.gemm(A17 if dq == 1 else A, W, config=dict(kernel="gemv", dq_warps=dq))
+        assert e.value.status == binding.TM_ERR_UNSUPPORTED
     with pytest.raises(binding.TmError) as e:
         binding.gemm(A, W, config=dict(kernel="tc", block_m=48))
     assert e.value.status == binding.TM_ERR_UNSUPPORTED

@@ -105,6 +105,8 @@ def _needed_scratch(W, M, cfg):
 CASES = [
     (4, 4096, 1152, "f16", dict(kernel="gemv", split_k=4)),
     (1, 2048, 640, "bf16", dict(kernel="gemv", split_k=1)),
+    (7, 4096, 1152, "bf16", dict(kernel="gemv", split_k=4, dq_warps=1)),
+    (16, 2048, 640, "f16", dict(kernel="gemv", split_k=2, dq_warps=1)),
     (16, 14336, 1152, "f16", dict(kernel="decode_mma", split_k=2)),
     (3, 1024, 640, "bf16", dict(kernel="decode_mma", split_k=1)),
     (9, 4096, 1152, "f16", dict(kernel="decode_mma", split_k=6, dq_warps=1)),

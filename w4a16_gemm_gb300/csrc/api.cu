@@ -303,17 +303,24 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
     return false;
   }
   if (c->kernel == TM_KERNEL_GEMV) {
-    if (M > 8) {
-      if (why) *why = "GEMV handles M <= 8";
+    // dq_warps: 0 = CUDA-core FMAs (M <= 8), 1 = tensor-core MMAs (M <= 16)
+    if (c->dq_warps != 0 && c->dq_warps != 1) {
+      if (why) *why = "GEMV takes dq_warps 0 (CUDA cores) or 1 (tensor cores)";
+      return false;
+    }
+    const bool mma = c->dq_warps == 1;
+    if (M > (mma ? 16 : 8)) {
+      if (why) *why = mma ? "GEMV with tensor cores handles M <= 16" : "GEMV handles M <= 8";
       return false;
     }
     const int kb_per = (KB + c->split_k - 1) / c->split_k;
-    if (gemv_smem_bytes(gemv_rows_tmpl(M), kb_per) > 200 * 1024) {
+    const int rows = mma ? (M <= 8 ? 8 : 16) : gemv_rows_tmpl(M);
+    const size_t smem = mma ? gemv_mma_smem_bytes(rows / 8, kb_per, W->group) : gemv_smem_bytes(rows, kb_per);
+    if (smem > 200 * 1024) {
       if (why) *why = "GEMV K range too long for shared memory; raise split_k";
       return false;
     }
-    c->block_m = gemv_rows_tmpl(M);
-    c->dq_warps = 0;
+    c->block_m = rows;
     return true;
   }
   if (c->kernel == TM_KERNEL_TC) {
@@ -534,7 +541,7 @@ static tm_status launch_planned(const void *A, const tm_packed *W, int M, const 
   const bool bf16 = W->dtype == TM_BF16;
   cudaError_t e;
   if (cfg.kernel == TM_KERNEL_GEMV) {
-    e = launch_gemv(a, bf16, gemv_rows_tmpl(M), st);
+    e = launch_gemv(a, bf16, cfg.block_m, cfg.dq_warps == 1, st);
   } else if (cfg.kernel == TM_KERNEL_DECODE_MMA) {
     CUtensorMap map;
     tm_status s = encode_act_map(A, M, W->K, bf16, cfg.block_m, 1, &map, &a.act_map_3d);
@@ -933,6 +940,9 @@ static std::vector<tm_config> candidates(const tm_packed *W, int M, int dev) {
   }
   if (M <= 8) {
     for (int s : splits) add(tm_config{TM_KERNEL_GEMV, 0, s, 0});
+  }
+  if (M <= 16) {
+    for (int s : splits) add(tm_config{TM_KERNEL_GEMV, 0, s, 1});
   }
   for (int bm : {16, 32, 64}) {
     if (bm > 16 && bm / 2 >= M) continue;

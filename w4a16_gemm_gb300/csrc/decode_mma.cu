@@ -47,6 +47,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "mma_frag.cuh"
 #include "ptx.cuh"
 #include "tc_epilogue.cuh"
 #include "tmw4_device.cuh"
@@ -85,100 +86,6 @@ namespace {
 
 constexpr int DM_W_BYTES = 4096;    // one 64-K block of the tile's packed weights
 constexpr int DM_META_BYTES = 320;  // a group's scales (256 B) and zeros (64 B) for the tile
-
-// Eight codes of one packed word (value e at nibble (0,4,1,5,2,6,3,7)[e]) ->
-// four 16-bit pairs (q_e - z), exact: {e0,e1}, {e2,e3}, {e4,e5}, {e6,e7},
-// the even element in the low half.
-//   fp16: OR-ing 0x6400 into a nibble in the low mantissa bits gives 1024 + q
-//         exactly; one nibble higher it gives 1024 + 16q exactly.  The first
-//         form minus (1024 + z) and the second form times 1/16 minus (64 + z)
-//         (a fused multiply-add whose exact result is a small integer) are
-//         both exact.  One shift, four lop3 (mask and OR in one), two subtracts
-//         and two fused multiply-adds per word.
-//   bf16: only 7 mantissa bits, so each pair is shifted to the low nibble
-//         first; 0x4300 gives 128 + q exactly, minus (128 + z) is exact.
-// zm = (MAGIC + z) in both halves; z16 = -(64 + z) in both halves (fp16 only).
-// Written in PTX so that each mask-and-OR is one lop3 (the C++ form of the
-// same expression compiled to twice as many logic instructions).
-template <bool BF16>
-__device__ __forceinline__ void codes_minus_zero(uint32_t w, uint32_t zm, uint32_t z16,
-                                                 uint32_t (&out)[4]) {
-  if constexpr (BF16) {
-    asm("{\n\t.reg .b32 s1, s2, s3, x0, x1, x2, x3;\n\t"
-        "shr.b32 s1, %4, 4;\n\t"
-        "shr.b32 s2, %4, 8;\n\t"
-        "shr.b32 s3, %4, 12;\n\t"
-        "lop3.b32 x0, %4, 0x000F000F, 0x43004300, 0xEA;\n\t"
-        "lop3.b32 x1, s1, 0x000F000F, 0x43004300, 0xEA;\n\t"
-        "lop3.b32 x2, s2, 0x000F000F, 0x43004300, 0xEA;\n\t"
-        "lop3.b32 x3, s3, 0x000F000F, 0x43004300, 0xEA;\n\t"
-        "sub.rn.bf16x2 %0, x0, %5;\n\t"
-        "sub.rn.bf16x2 %1, x1, %5;\n\t"
-        "sub.rn.bf16x2 %2, x2, %5;\n\t"
-        "sub.rn.bf16x2 %3, x3, %5;\n\t}"
-        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
-        : "r"(w), "r"(zm));
-    (void)z16;
-  } else {
-    asm("{\n\t.reg .b32 hi, x0, x1, x2, x3;\n\t"
-        "shr.b32 hi, %4, 8;\n\t"
-        "lop3.b32 x0, %4, 0x000F000F, 0x64006400, 0xEA;\n\t"
-        "lop3.b32 x1, %4, 0x00F000F0, 0x64006400, 0xEA;\n\t"
-        "lop3.b32 x2, hi, 0x000F000F, 0x64006400, 0xEA;\n\t"
-        "lop3.b32 x3, hi, 0x00F000F0, 0x64006400, 0xEA;\n\t"
-        "sub.rn.f16x2 %0, x0, %5;\n\t"
-        "fma.rn.f16x2 %1, x1, %7, %6;\n\t"
-        "sub.rn.f16x2 %2, x2, %5;\n\t"
-        "fma.rn.f16x2 %3, x3, %7, %6;\n\t}"
-        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
-        : "r"(w), "r"(zm), "r"(z16), "r"(0x2C002C00u));   // 0x2C00 = 1/16
-  }
-}
-
-// d.xy += s.xy * a.xy, two fp32 lanes in one instruction.
-__device__ __forceinline__ void ffma2(float &d0, float &d1, float s0, float s1, float a0, float a1) {
-  asm("{\n\t.reg .b64 d, s, a;\n\t"
-      "mov.b64 d, {%0, %1};\n\t"
-      "mov.b64 s, {%2, %3};\n\t"
-      "mov.b64 a, {%4, %5};\n\t"
-      "fma.rn.f32x2 d, s, a, d;\n\t"
-      "mov.b64 {%0, %1}, d;\n\t}"
-      : "+f"(d0), "+f"(d1)
-      : "f"(s0), "f"(s1), "f"(a0), "f"(a1));
-}
-
-// d += A(16x16, row) * B(16x8, col), fp32 accumulate.
-template <bool BF16>
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  if constexpr (BF16) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  } else {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
-}
-
-template <bool BF16>
-__device__ __forceinline__ float bits16_to_f32(uint32_t h) {
-  return BF16 ? __uint_as_float(h << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint16_t f32_to_bits16(float x) {
-  if constexpr (BF16) {
-    __nv_bfloat16 b = __float2bfloat16_rn(x);
-    return *reinterpret_cast<uint16_t *>(&b);
-  } else {
-    __half h = __float2half_rn(x);
-    return *reinterpret_cast<uint16_t *>(&h);
-  }
-}
 
 }  // namespace
 
@@ -256,8 +163,7 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? 4 : KG == 2 ? 2 : 1)
   __shared__ int seg_tile[2], seg_last[2];
   __shared__ int abort_flag_s;
   volatile int *abort_flag = &abort_flag_s;
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(dm_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *smem = align_smem_1024(dm_smem_raw);
   uint8_t *const wm_ring = smem + Geo::W_OFF;
   float *const red = reinterpret_cast<float *>(smem + Geo::RED_OFF);
 
@@ -414,7 +320,7 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? 4 : KG == 2 ? 2 : 1)
       for (int u = 0; u < GS; ++u) {
         const int ib = ig + u;
         const int sidx = ib % D;
-        if (!mbar_wait_warp(full_bar + sidx, (ib / D) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL, ib)) {
+        if (!mbar_wait_all(full_bar + sidx, (ib / D) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL, ib)) {
           ok = false;
           break;
         }

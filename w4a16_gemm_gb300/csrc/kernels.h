@@ -128,9 +128,12 @@ inline cudaError_t cluster_optin(int bytes) {
   return result[dev];
 }
 
-// GEMV (CUDA cores): rows_tmpl in {1,2,4,8} >= M.  Shared memory bytes:
+// GEMV: rows_tmpl in {1,2,4,8} >= M on the CUDA cores (mma = false), or
+// 8 / 16 >= M with register-operand tensor-core MMAs (mma = true).  Shared
+// memory bytes of each mode:
 size_t gemv_smem_bytes(int rows_tmpl, int kb_per_split);
-cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, cudaStream_t st);
+size_t gemv_mma_smem_bytes(int nt8, int kb_per_split, int group);
+cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, bool mma, cudaStream_t st);
 
 // tcgen05 kernel.  block_m in {16,32,64,128,256}, dq_warps in {4,8}.
 size_t tc_smem_bytes(int block_m);

@@ -64,6 +64,14 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
   return ok != 0;
 }
 
+// `base` (dynamic shared memory) advanced to the next multiple of 1024 bytes
+// of the shared window.  Pointer arithmetic on the shared array (not a round
+// trip through an integer) lets the compiler keep accesses through the
+// result as shared-memory instructions instead of generic ones.
+__device__ __forceinline__ uint8_t *align_smem_1024(uint8_t *base) {
+  return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

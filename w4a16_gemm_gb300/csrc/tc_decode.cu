@@ -162,8 +162,7 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
   static_assert(dec_smem_bytes(BLOCK_M, DQ_WG) <= 227 * 1024, "shared memory");
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *smem = align_smem_1024(smem_raw);
   uint8_t *sA = smem;                                   // [ASTAGES][WKB][BLOCK_M x 128 B]
   uint8_t *sW = sA + ASTAGES * A_STAGE;                 // [WST][W_STAGE_BYTES]
   uint64_t *wfull_bar = reinterpret_cast<uint64_t *>(sW + WST * W_STAGE_BYTES);  // stage landed

@@ -117,8 +117,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
   static_assert(A_KB % 1024 == 0, "swizzle atoms");
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *smem = align_smem_1024(smem_raw);
   uint8_t *sA = smem;                              // [STAGES][KBS][BLOCK_M x 128 B]
   uint8_t *sW = sA + STAGES * A_STAGE;             // [STAGES][KBS][4096]
   uint8_t *sSC = sW + STAGES * W_STAGE;            // [STAGES][groups][256]
