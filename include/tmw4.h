@@ -7,6 +7,8 @@
  * offline packing of the weights and an accelerated online multiply):
  *
  *   offline:  tm_pack_w4     int4 codes + scales + zeros -> packed weight
+ *             (tm_pack_awq / tm_pack_gptq: the same from AWQ / GPTQ int32
+ *             packed checkpoints)
  *   online:   tm_gemm_w4a16  C[M,N] = A[M,K] * W[K,N],
  *                            W[k,n] = T(s[k/G,n] * (q[k,n] - z[k/G,n]))
  *
@@ -115,7 +117,8 @@ typedef struct tm_packed tm_packed;
  *   zeros:  tile-major [N/128][K/G][64] bytes, each byte two columns (even
  *     column in the low nibble); NULL for the symmetric format (zero 8). */
 typedef struct {
-  int32_t K, N, group;
+  int32_t K, N, group; /* group: the one the kernels run with (64 or 128; a
+                          coarser source group is repeated, see tm_pack_w4) */
   int32_t dtype;     /* tm_dtype */
   int32_t symmetric; /* 1: no stored zeros, zero point 8 */
   int32_t device;
@@ -133,13 +136,45 @@ typedef struct {
  *   scales device, [K/group][N] 16-bit values of type dtype
  *   zeros  device, [K/group][N] uint8 zero points 0..15, or NULL for the
  *          symmetric format (zero point 8)
- *   K % group == 0, group in {64, 128}, K % 64 == 0, N % 128 == 0, K, N > 0;
- *   all pointers 16-byte aligned.
+ *   K % group == 0, group a positive multiple of 64 (per-channel weights:
+ *   group = K), N % 128 == 0, K, N > 0; all pointers 16-byte aligned.
+ *   Groups of 64 and 128 are kept; a coarser group is stored as groups of
+ *   128 (of 64 if it is an odd multiple of 64) with its scale and zero
+ *   repeated, which leaves every dequantized weight unchanged.
  *   On TM_OK *out receives a new handle; the inputs may be reused once
  *   `stream` has passed this call.  The handle's storage is allocated with
  *   cudaMallocAsync on `stream`. */
 tm_status tm_pack_w4(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N,
                      int group, tm_dtype dtype, void *stream, tm_packed **out);
+
+/* The same repack, reading the int4 codes and zero points straight from the
+ * int32-packed layouts in which AWQ and GPTQ checkpoints are distributed
+ * (the pages' evaluated models are AWQ checkpoints: pith.science review,
+ * Figure 11, "Qwen3 8B AWQ"), without an intermediate [K][N] byte array.
+ * Dequantization is the same, W = T(s * (q - z)).
+ *
+ * AWQ ("GEMM" layout):
+ *   qweight device, int32 [K][N/8]: word (k, j) holds columns 8j + c of row
+ *           k, column offset c in nibble p(c) with p = (0,4,1,5,2,6,3,7)
+ *           (even columns in the low four nibbles, odd ones in the high four)
+ *   qzeros  device, int32 [K/group][N/8], the same packing, or NULL
+ *           (symmetric, zero point 8)
+ *   scales  device, [K/group][N] of type dtype
+ * GPTQ:
+ *   qweight device, int32 [K/8][N]: word (r, n) holds rows 8r + i of column
+ *           n in nibble i
+ *   qzeros  device, int32 [K/group][N/8]: column 8c + i in nibble i of word
+ *           (g, c), or NULL (symmetric); zero_offset (0 or 1) is added to
+ *           every stored zero (files of the original GPTQ format store
+ *           zero - 1); a resulting zero above 15 is reported by
+ *           tm_poll_error as TM_ERR_INVALID_ARG.  Groups must be contiguous
+ *           in K (no activation-order row permutation).
+ *   scales  device, [K/group][N] of type dtype
+ * Shapes, alignment, groups and ownership as for tm_pack_w4. */
+tm_status tm_pack_awq(const int32_t *qweight, const int32_t *qzeros, const void *scales, int K, int N,
+                      int group, tm_dtype dtype, void *stream, tm_packed **out);
+tm_status tm_pack_gptq(const int32_t *qweight, const int32_t *qzeros, const void *scales, int zero_offset,
+                       int K, int N, int group, tm_dtype dtype, void *stream, tm_packed **out);
 
 /* Online GEMM (TurboMind paper, arXiv abstract: the online half of the pipeline;
  * pith.science review, Figure 9: dequantization overlapped with the MMA).

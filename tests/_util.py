@@ -54,3 +54,32 @@ def gemm_poisoned(A: torch.Tensor, W, config=None) -> torch.Tensor:
     """binding.gemm into an output pre-filled with NaN, so unwritten elements fail."""
     out = torch.full((A.shape[0], W.N), float("nan"), dtype=W.dtype, device=A.device)
     return binding.gemm(A, W, out=out, config=config)
+
+
+# Packers into the int32 checkpoint layouts (AWQ, GPTQ), written from the
+# column -> nibble direction; oracle/checkpoint.py unpacks nibble -> column.
+def awq_pack(q: np.ndarray) -> np.ndarray:
+    """uint8 [R, N] -> AWQ int32 [R, N/8]: column offset c goes to nibble POS[c]."""
+    POS = (0, 4, 1, 5, 2, 6, 3, 7)
+    R, N = q.shape
+    w = np.zeros((R, N // 8), dtype=np.int64)
+    for c in range(8):
+        w |= q[:, c::8].astype(np.int64) << (4 * POS[c])
+    return w.astype(np.uint32).astype(np.int32)
+
+
+def gptq_pack_qweight(q: np.ndarray) -> np.ndarray:
+    K, N = q.shape
+    w = np.zeros((K // 8, N), dtype=np.int64)
+    for r in range(8):
+        w |= q[r::8, :].astype(np.int64) << (4 * r)
+    return w.astype(np.uint32).astype(np.int32)
+
+
+def gptq_pack_qzeros(z: np.ndarray, zero_offset: int) -> np.ndarray:
+    G, N = z.shape
+    stored = z.astype(np.int64) - zero_offset
+    w = np.zeros((G, N // 8), dtype=np.int64)
+    for c in range(8):
+        w |= stored[:, c::8] << (4 * c)
+    return w.astype(np.uint32).astype(np.int32)

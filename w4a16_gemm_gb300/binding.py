@@ -56,6 +56,8 @@ _LIB = None
 _VP, _I, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
 SIGNATURES = [
     ("tm_pack_w4", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
+    ("tm_pack_awq", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
+    ("tm_pack_gptq", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
     ("tm_gemm_w4a16", _I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
     ("tm_gemm_w4a16_ex", _I, [_VP, _VP, _VP, _I, _I, _I, ctypes.POINTER(TmConfig), _VP]),
     ("tm_gemm_w4a16_noalloc", _I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
@@ -183,7 +185,53 @@ def pack(q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | None, grou
     with torch.cuda.device(q.device):
         _check(lib().tm_pack_w4(q.data_ptr(), scales.data_ptr(), zp, K, N, group, _DT[scales.dtype],
                                 _stream(stream), ctypes.byref(h)))
-    return PackedW4(h.value, K, N, group, scales.dtype, zeros is None, q.device)
+    return _packed(h.value, K, N, scales.dtype, zeros is None, q.device)
+
+
+def _packed(handle: int, K: int, N: int, dtype: torch.dtype, symmetric: bool, device) -> PackedW4:
+    W = PackedW4(handle, K, N, 0, dtype, symmetric, device)
+    W.group = W.info().group        # the group the kernels run with
+    return W
+
+
+def _int32_2d(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype != torch.int32 or t.dim() != 2 or not t.is_cuda:
+        raise ValueError(f"{name} must be a 2-D int32 CUDA tensor")
+    return t.contiguous()
+
+
+def pack_awq(qweight: torch.Tensor, qzeros: torch.Tensor | None, scales: torch.Tensor, group: int,
+             stream=None) -> PackedW4:
+    """tm_pack_awq: qweight int32 [K, N/8], qzeros int32 [K/G, N/8] or None,
+    scales [K/G, N] fp16/bf16 (AWQ "GEMM" layout)."""
+    qweight = _int32_2d(qweight, "qweight")
+    if scales.dtype not in _DT:
+        raise ValueError("scales must be float16 or bfloat16")
+    K, N = qweight.shape[0], qweight.shape[1] * 8
+    scales = scales.contiguous()
+    zp = None if qzeros is None else _int32_2d(qzeros, "qzeros").data_ptr()
+    h = ctypes.c_void_p()
+    with torch.cuda.device(qweight.device):
+        _check(lib().tm_pack_awq(qweight.data_ptr(), zp, scales.data_ptr(), K, N, group, _DT[scales.dtype],
+                                 _stream(stream), ctypes.byref(h)))
+    return _packed(h.value, K, N, scales.dtype, qzeros is None, qweight.device)
+
+
+def pack_gptq(qweight: torch.Tensor, qzeros: torch.Tensor | None, scales: torch.Tensor, group: int,
+              zero_offset: int = 1, stream=None) -> PackedW4:
+    """tm_pack_gptq: qweight int32 [K/8, N], qzeros int32 [K/G, N/8] or None,
+    scales [K/G, N] fp16/bf16; zero_offset is added to every stored zero."""
+    qweight = _int32_2d(qweight, "qweight")
+    if scales.dtype not in _DT:
+        raise ValueError("scales must be float16 or bfloat16")
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    scales = scales.contiguous()
+    zp = None if qzeros is None else _int32_2d(qzeros, "qzeros").data_ptr()
+    h = ctypes.c_void_p()
+    with torch.cuda.device(qweight.device):
+        _check(lib().tm_pack_gptq(qweight.data_ptr(), zp, scales.data_ptr(), zero_offset, K, N, group,
+                                  _DT[scales.dtype], _stream(stream), ctypes.byref(h)))
+    return _packed(h.value, K, N, scales.dtype, qzeros is None, qweight.device)
 
 
 def gemm(A: torch.Tensor, W: PackedW4, out: torch.Tensor | None = None, config: dict | None = None,

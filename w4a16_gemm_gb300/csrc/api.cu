@@ -659,18 +659,29 @@ const char *tm_version(void) { return "tmw4 0.1 (sm_103a)"; }
 
 const char *tm_last_error(void) { return g_last_error.c_str(); }
 
-tm_status tm_pack_w4(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N,
-                     int group, tm_dtype dtype, void *stream, tm_packed **out) {
+// The group the kernels run with for a source group G: 64 or 128.  A
+// coarser group (any multiple of 64, per-channel G = K included) is packed
+// as 128 when it is a multiple of 128, else as 64, each of its scales and
+// zeros repeated over the finer groups it spans: the dequantized weight is
+// identical by construction.
+static int packed_group(int group) { return group % 128 == 0 ? 128 : 64; }
+
+// Packs codes in layout `src` (q: u8 [K][N], AWQ int32 [K][N/8] or GPTQ
+// int32 [K/8][N]), fp16/bf16 scales [K/G][N] and zeros (same layout family
+// as q: u8 [K/G][N] or int32 [K/G][N/8]; NULL = symmetric, z = 8).
+static tm_status pack_common(int src, const void *q, const void *scales, const void *zeros, int zero_offset,
+                             int K, int N, int group, tm_dtype dtype, void *stream, tm_packed **out,
+                             const char *what) {
   if (out == nullptr) return fail(TM_ERR_INVALID_ARG, "out must not be NULL");
   *out = nullptr;
-  if (q == nullptr || scales == nullptr) return fail(TM_ERR_INVALID_ARG, "q and scales must not be NULL");
+  if (q == nullptr || scales == nullptr) return fail(TM_ERR_INVALID_ARG, "codes and scales must not be NULL");
   if (dtype != TM_F16 && dtype != TM_BF16) return fail(TM_ERR_INVALID_ARG, "dtype must be TM_F16 or TM_BF16");
   if (K <= 0 || N <= 0) return fail(TM_ERR_INVALID_ARG, "K and N must be positive");
-  if (group != 64 && group != 128) return fail(TM_ERR_INVALID_ARG, "group must be 64 or 128");
+  if (group <= 0 || group % 64 != 0) return fail(TM_ERR_INVALID_ARG, "group must be a positive multiple of 64");
   if (K % group != 0) return fail(TM_ERR_INVALID_ARG, "K (%d) must be a multiple of group (%d)", K, group);
   if (N % 128 != 0) return fail(TM_ERR_INVALID_ARG, "N (%d) must be a multiple of 128", N);
   if (!aligned16(q) || !aligned16(scales) || (zeros && !aligned16(zeros)))
-    return fail(TM_ERR_INVALID_ARG, "q, scales and zeros must be 16-byte aligned");
+    return fail(TM_ERR_INVALID_ARG, "codes, scales and zeros must be 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int dev = -1;
   tm_status s = current_device(&dev);
@@ -678,36 +689,55 @@ tm_status tm_pack_w4(const uint8_t *q, const void *scales, const uint8_t *zeros,
   unsigned int *err = nullptr;
   s = error_word(dev, &err);
   if (s != TM_OK) return s;
+  const int G = packed_group(group), rep = group / G;
 
   tm_packed *W = new tm_packed{};
   W->magic = kPackedMagic;
   W->K = K;
   W->N = N;
-  W->group = group;
+  W->group = G;
   W->dtype = dtype;
   W->symmetric = zeros == nullptr ? 1 : 0;
   W->device = dev;
   W->qw_bytes = static_cast<size_t>(K) * N / 2;
-  W->scales_bytes = static_cast<size_t>(K / group) * N * 2;
-  W->zeros_bytes = zeros ? static_cast<size_t>(K / group) * (N / 2) : 0;
+  W->scales_bytes = static_cast<size_t>(K / G) * N * 2;
+  W->zeros_bytes = zeros ? static_cast<size_t>(K / G) * (N / 2) : 0;
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&W->qw), W->qw_bytes, st);
   if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void **>(&W->scales), W->scales_bytes, st);
   if (e == cudaSuccess && zeros)
     e = cudaMallocAsync(reinterpret_cast<void **>(&W->zeros), W->zeros_bytes, st);
-  if (e == cudaSuccess) e = launch_repack(q, W->qw, K, N, err, st);
+  if (e == cudaSuccess) e = launch_repack(q, W->qw, K, N, src, err, st);
   if (e == cudaSuccess)
-    e = launch_pack_scales(static_cast<const uint16_t *>(scales), W->scales, K / group, N, st);
-  if (e == cudaSuccess && zeros) e = launch_pack_zeros(zeros, W->zeros, K / group, N, err, st);
+    e = launch_pack_scales(static_cast<const uint16_t *>(scales), W->scales, K / G, N, rep, st);
+  if (e == cudaSuccess && zeros) e = launch_pack_zeros(zeros, W->zeros, K / G, N, rep, src, zero_offset, err, st);
   if (e != cudaSuccess) {
     if (W->qw) cudaFreeAsync(W->qw, st);
     if (W->scales) cudaFreeAsync(W->scales, st);
     if (W->zeros) cudaFreeAsync(W->zeros, st);
     W->magic = 0;
     delete W;
-    return fail_cuda(e, "tm_pack_w4");
+    return fail_cuda(e, what);
   }
   *out = W;
   return TM_OK;
+}
+
+tm_status tm_pack_w4(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N,
+                     int group, tm_dtype dtype, void *stream, tm_packed **out) {
+  return pack_common(SRC_U8, q, scales, zeros, 0, K, N, group, dtype, stream, out, "tm_pack_w4");
+}
+
+tm_status tm_pack_awq(const int32_t *qweight, const int32_t *qzeros, const void *scales, int K, int N,
+                      int group, tm_dtype dtype, void *stream, tm_packed **out) {
+  return pack_common(SRC_AWQ, qweight, scales, qzeros, 0, K, N, group, dtype, stream, out, "tm_pack_awq");
+}
+
+tm_status tm_pack_gptq(const int32_t *qweight, const int32_t *qzeros, const void *scales, int zero_offset,
+                       int K, int N, int group, tm_dtype dtype, void *stream, tm_packed **out) {
+  if (zero_offset != 0 && zero_offset != 1) return fail(TM_ERR_INVALID_ARG, "zero_offset must be 0 or 1");
+  if (K % 8 != 0) return fail(TM_ERR_INVALID_ARG, "K must be a multiple of 8");
+  return pack_common(SRC_GPTQ, qweight, scales, qzeros, zero_offset, K, N, group, dtype, stream, out,
+                     "tm_pack_gptq");
 }
 
 tm_status tm_packed_free(tm_packed *W, void *stream) {

@@ -9,11 +9,14 @@
 
 namespace tmw4 {
 
-cudaError_t launch_repack(const uint8_t *q, uint8_t *qw, int K, int N, unsigned int *err,
+// Source layouts of the repack and zero packing (see pack.cu).
+enum SrcLayout { SRC_U8 = 0, SRC_AWQ = 1, SRC_GPTQ = 2 };
+cudaError_t launch_repack(const void *q, uint8_t *qw, int K, int N, int src, unsigned int *err,
                           cudaStream_t st);
-cudaError_t launch_pack_zeros(const uint8_t *z, uint8_t *zp, int rows, int N, unsigned int *err,
-                              cudaStream_t st);
-cudaError_t launch_pack_scales(const uint16_t *s, uint16_t *sp, int rows, int N, cudaStream_t st);
+// rows packed group rows, each from source row / rep; offset added to zeros
+cudaError_t launch_pack_zeros(const void *z, uint8_t *zp, int rows, int N, int rep, int src, int offset,
+                              unsigned int *err, cudaStream_t st);
+cudaError_t launch_pack_scales(const uint16_t *s, uint16_t *sp, int rows, int N, int rep, cudaStream_t st);
 cudaError_t launch_dequant(const uint8_t *qw, const uint16_t *scales, const uint8_t *zeros,
                            uint16_t *out, int K, int N, int group, bool bf16, cudaStream_t st);
 

@@ -18,14 +18,25 @@ namespace tmw4 {
 // NIBBLE_POS of the layout: value e of a word sits at nibble kNibPos[e].
 __device__ __constant__ int kNibPos[8] = {0, 4, 1, 5, 2, 6, 3, 7};
 
+// Column offset within a group of eight held by nibble i of an AWQ-packed
+// 32-bit word (the AWQ "GEMM" layout interleaves even and odd columns).
+__device__ __constant__ int kAwqCol[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+
+// Source layouts of the codes (SrcLayout):
+//   U8    q [K][N] bytes, one code per byte;
+//   AWQ   int32 [K][N/8]: word (k, j) holds columns 8j + kAwqCol[i] of row k
+//         in nibble i;
+//   GPTQ  int32 [K/8][N]: word (r, n) holds rows 8r + i of column n in
+//         nibble i.
+template <int SRC>
 __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ q,
                                                      uint8_t *__restrict__ qw, int K, int N,
                                                      unsigned int *err) {
   __shared__ uint8_t tile[ATOM_K][ATOM_N + 4];
   const int na = blockIdx.x, kb = blockIdx.y, t = threadIdx.x;
   const int k0 = kb * ATOM_K, n0 = na * ATOM_N;
-  // 64 rows x 64 bytes, 16 bytes per thread
-  {
+  if constexpr (SRC == SRC_U8) {
+    // 64 rows x 64 bytes, 16 bytes per thread
     const int row = t >> 2, col = (t & 3) * 16;
     const uint4 v = *reinterpret_cast<const uint4 *>(q + static_cast<size_t>(k0 + row) * N + n0 + col);
     if (((v.x | v.y | v.z | v.w) & 0xF0F0F0F0u) != 0u) atomicOr(err, TM_DEVERR_BAD_CODE);
@@ -35,6 +46,26 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
 #pragma unroll
       for (int b = 0; b < 4; ++b) tile[row][col + 4 * i + b] = (w[i] >> (8 * b)) & 0xFu;
     }
+  } else if constexpr (SRC == SRC_AWQ) {
+    // 64 rows x 8 words; two words (16 columns) per thread
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(q);
+    const int row = t >> 2, j0 = (t & 3) * 2;
+    const uint2 v = *reinterpret_cast<const uint2 *>(src + static_cast<size_t>(k0 + row) * (N / 8) + n0 / 8 + j0);
+    const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tile[row][8 * (j0 + jj) + kAwqCol[i]] = (w[jj] >> (4 * i)) & 0xFu;
+  } else {
+    // 8 word rows (64 K) x 64 columns; two words (two columns) per thread
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(q);
+    const int r = t >> 5, col = (t & 31) * 2;
+    const uint2 v = *reinterpret_cast<const uint2 *>(src + static_cast<size_t>(k0 / 8 + r) * N + n0 + col);
+    const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tile[8 * r + i][col + c] = (w[c] >> (4 * i)) & 0xFu;
   }
   __syncwarp();   // rejoin lanes that took the error branch before the CTA barrier
   __syncthreads();
@@ -51,26 +82,44 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
   }
 }
 
-// zeros [K/G][N] bytes -> tile-major nibbles; one thread per output byte.
+// zeros -> tile-major nibbles; one thread per output byte.  Packed group
+// row g takes source row g / rep (a coarser group repeated rep times).
+// Sources: U8 [K/G][N] bytes; AWQ int32 [K/G][N/8] in the AWQ column order;
+// GPTQ int32 [K/G][N/8] with column 8c + i in nibble i.  `offset` is added
+// to every zero (GPTQ files store zero - 1); a result above 15 is a bad code.
+template <int SRC>
 __global__ void pack_zeros_kernel(const uint8_t *__restrict__ z, uint8_t *__restrict__ zp,
-                                  int rows, int N, unsigned int *err) {
+                                  int rows, int N, int rep, int offset, unsigned int *err) {
   const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t total = static_cast<size_t>(rows) * (N / 2);
   if (i >= total) return;
   const size_t g = i / (N / 2), c = i % (N / 2);
+  const size_t gs = g / rep;
   const int n = static_cast<int>(2 * c);
-  const uint32_t lo = z[g * N + n], hi = z[g * N + n + 1];
-  if ((lo | hi) > 15u) atomicOr(err, TM_DEVERR_BAD_CODE);
-  zp[zero_byte(static_cast<int>(g), n, rows)] = static_cast<uint8_t>((lo & 0xFu) | ((hi & 0xFu) << 4));
+  uint32_t zz[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int nn = n + h;
+    if constexpr (SRC == SRC_U8) {
+      zz[h] = z[gs * N + nn];
+    } else {
+      const uint32_t w = reinterpret_cast<const uint32_t *>(z)[gs * (N / 8) + nn / 8];
+      const int pos = SRC == SRC_AWQ ? (nn % 8 % 2 == 0 ? (nn % 8) / 2 : 4 + (nn % 8) / 2) : nn % 8;
+      zz[h] = ((w >> (4 * pos)) & 0xFu) + static_cast<uint32_t>(offset);
+    }
+  }
+  if ((zz[0] | zz[1]) > 15u) atomicOr(err, TM_DEVERR_BAD_CODE);
+  zp[zero_byte(static_cast<int>(g), n, rows)] = static_cast<uint8_t>((zz[0] & 0xFu) | ((zz[1] & 0xFu) << 4));
 }
 
-// scales [K/G][N] -> tile-major [N/128][K/G][128]; one thread per scale.
+// scales [K/G][N] -> tile-major [N/128][rows][128]; one thread per packed
+// scale, row g from source row g / rep.
 __global__ void pack_scales_kernel(const uint16_t *__restrict__ s, uint16_t *__restrict__ sp,
-                                   int rows, int N) {
+                                   int rows, int N, int rep) {
   const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<size_t>(rows) * N) return;
   const int g = static_cast<int>(i / N), n = static_cast<int>(i % N);
-  sp[scale_index(g, n, rows)] = s[i];
+  sp[scale_index(g, n, rows)] = s[static_cast<size_t>(g / rep) * N + n];
 }
 
 // One thread per 16-byte chunk: 32 consecutive K values of one column.
@@ -106,25 +155,37 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
   }
 }
 
-cudaError_t launch_repack(const uint8_t *q, uint8_t *qw, int K, int N, unsigned int *err,
+cudaError_t launch_repack(const void *q, uint8_t *qw, int K, int N, int src, unsigned int *err,
                           cudaStream_t st) {
   dim3 grid(N / ATOM_N, K / ATOM_K);
-  repack_kernel<<<grid, 256, 0, st>>>(q, qw, K, N, err);
+  const uint8_t *qb = static_cast<const uint8_t *>(q);
+  switch (src) {
+    case SRC_U8: repack_kernel<SRC_U8><<<grid, 256, 0, st>>>(qb, qw, K, N, err); break;
+    case SRC_AWQ: repack_kernel<SRC_AWQ><<<grid, 256, 0, st>>>(qb, qw, K, N, err); break;
+    case SRC_GPTQ: repack_kernel<SRC_GPTQ><<<grid, 256, 0, st>>>(qb, qw, K, N, err); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack_zeros(const uint8_t *z, uint8_t *zp, int rows, int N, unsigned int *err,
-                              cudaStream_t st) {
+cudaError_t launch_pack_zeros(const void *z, uint8_t *zp, int rows, int N, int rep, int src, int offset,
+                              unsigned int *err, cudaStream_t st) {
   const size_t total = static_cast<size_t>(rows) * (N / 2);
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
-  pack_zeros_kernel<<<blocks, 256, 0, st>>>(z, zp, rows, N, err);
+  const uint8_t *zb = static_cast<const uint8_t *>(z);
+  switch (src) {
+    case SRC_U8: pack_zeros_kernel<SRC_U8><<<blocks, 256, 0, st>>>(zb, zp, rows, N, rep, offset, err); break;
+    case SRC_AWQ: pack_zeros_kernel<SRC_AWQ><<<blocks, 256, 0, st>>>(zb, zp, rows, N, rep, offset, err); break;
+    case SRC_GPTQ: pack_zeros_kernel<SRC_GPTQ><<<blocks, 256, 0, st>>>(zb, zp, rows, N, rep, offset, err); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack_scales(const uint16_t *s, uint16_t *sp, int rows, int N, cudaStream_t st) {
+cudaError_t launch_pack_scales(const uint16_t *s, uint16_t *sp, int rows, int N, int rep, cudaStream_t st) {
   const size_t total = static_cast<size_t>(rows) * N;
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
-  pack_scales_kernel<<<blocks, 256, 0, st>>>(s, sp, rows, N);
+  pack_scales_kernel<<<blocks, 256, 0, st>>>(s, sp, rows, N, rep);
   return cudaGetLastError();
 }
 
