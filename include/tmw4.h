@@ -117,8 +117,8 @@ typedef struct tm_packed tm_packed;
  *   zeros:  tile-major [N/128][K/G][64] bytes, each byte two columns (even
  *     column in the low nibble); NULL for the symmetric format (zero 8). */
 typedef struct {
-  int32_t K, N, group; /* group: the one the kernels run with (64 or 128; a
-                          coarser source group is repeated, see tm_pack_w4) */
+  int32_t K, N, group; /* group: the one the kernels run with (32, 64 or 128;
+                          a coarser source group is repeated, see tm_pack_w4) */
   int32_t dtype;     /* tm_dtype */
   int32_t symmetric; /* 1: no stored zeros, zero point 8 */
   int32_t device;
@@ -136,11 +136,13 @@ typedef struct {
  *   scales device, [K/group][N] 16-bit values of type dtype
  *   zeros  device, [K/group][N] uint8 zero points 0..15, or NULL for the
  *          symmetric format (zero point 8)
- *   K % group == 0, group a positive multiple of 64 (per-channel weights:
- *   group = K), N % 128 == 0, K, N > 0; all pointers 16-byte aligned.
- *   Groups of 64 and 128 are kept; a coarser group is stored as groups of
- *   128 (of 64 if it is an odd multiple of 64) with its scale and zero
- *   repeated, which leaves every dequantized weight unchanged.
+ *   K % group == 0, K % 64 == 0, group 32 or a positive multiple of 64
+ *   (per-channel weights: group = K), N % 128 == 0, K, N > 0; all pointers
+ *   16-byte aligned.  Groups of 32, 64 and 128 are kept; a coarser group is
+ *   stored as groups of 128 (of 64 if it is an odd multiple of 64) with its
+ *   scale and zero repeated, which leaves every dequantized weight
+ *   unchanged.  Groups of 32 run on the TC kernel and the CUDA-core GEMV
+ *   only (the other kernels report TM_ERR_UNSUPPORTED for them).
  *   On TM_OK *out receives a new handle; the inputs may be reused once
  *   `stream` has passed this call.  The handle's storage is allocated with
  *   cudaMallocAsync on `stream`. */

@@ -91,12 +91,48 @@ def test_gptq_import(G, offset, dt):
     _check_gemms(W, q_o, s, z_o, G, dt, seed=31)
 
 
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_group_32(dt):
+    """Groups of 32: two scales per 64-K block.  The TC kernel (any M) and the
+    CUDA-core GEMV (M <= 8) run them; the kernels that scale fp32 sums per
+    block refuse them."""
+    K, N = 512, 256
+    qw, _ = synth.random_problem(8, 1, K, N, 32, dt)
+    W = packed_from_qw(qw)
+    assert W.group == 32
+    w = oracle.dequant_bits(qw.q, qw.scales, qw.zeros, 32, dt)
+    assert np.array_equal(bits_of(binding.dequant(W)), w)
+    for M in (1, 5, 16, 200):
+        a = synth.random_problem(40 + M, M, K, N, 32, dt)[1]
+        A = binding.acts_to_device(a, TORCH_DT[dt])
+        c_ref = oracle.gemm_ref(a, w, dt)
+        cfgs = [None, dict(kernel="tc", block_m=16, split_k=2), dict(kernel="tc", block_m=128, split_k=1)]
+        if M <= 8:
+            cfgs += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=4)]
+        for cfg in cfgs:
+            C = gemm_poisoned(A, W, config=cfg)
+            torch.cuda.synchronize()
+            assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, (M, cfg)
+        if M <= 16:
+            for cfg in (dict(kernel="decode_mma"), dict(kernel="tc_decode", block_m=16),
+                        dict(kernel="gemv", dq_warps=1)):
+                with pytest.raises(binding.TmError) as e:
+                    binding.gemm(A, W, config=cfg)
+                assert e.value.status == binding.TM_ERR_UNSUPPORTED, cfg
+    binding.poll_error()
+
+
+def packed_from_qw(qw):
+    p = binding.to_device(qw)
+    return binding.pack(p.q, p.scales, p.zeros, qw.group)
+
+
 def test_format_errors():
     K, N = 256, 128
     q = torch.zeros((K, N), dtype=torch.uint8, device="cuda")
-    s = torch.ones((K // 32, N), dtype=torch.float16, device="cuda")
+    s = torch.ones((K // 16, N), dtype=torch.float16, device="cuda")
     with pytest.raises(binding.TmError) as e:
-        binding.pack(q, s, None, 32)                  # groups finer than 64 are not supported
+        binding.pack(q, s, None, 16)                  # groups finer than 32 are not supported
     assert e.value.status == binding.TM_ERR_INVALID_ARG
     qw = torch.zeros((K // 8, N), dtype=torch.int32, device="cuda")
     s2 = torch.ones((K // 128, N), dtype=torch.float16, device="cuda")

@@ -266,6 +266,14 @@ static int gemv_rows_tmpl(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 :
 // Is cfg runnable for this shape?  (Fills defaults for zero fields.)
 static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::string *why) {
   const int KB = W->K / 64;
+  // Groups of 32 need a second scale inside each 64-K block: the kernels
+  // that scale the dequantized weight before the multiply (TC, CUDA-core
+  // GEMV) take them; those that scale fp32 sums per block do not.
+  if (W->group == 32 && (c->kernel == TM_KERNEL_DECODE_MMA || c->kernel == TM_KERNEL_TC_DECODE ||
+                         (c->kernel == TM_KERNEL_GEMV && c->dq_warps == 1))) {
+    if (why) *why = "this kernel needs groups of at least 64";
+    return false;
+  }
   if (c->kernel == TM_KERNEL_DECODE_MMA) {
     if (decode_mma_nt8(M) == 0) {
       if (why) *why = "DECODE_MMA handles M <= 16";
@@ -381,6 +389,11 @@ static tm_config default_config(const tm_packed *W, int M, int dev) {
   // rows the persistent stream-K grid of the register-MMA kernel; beyond,
   // the tcgen05 decode kernel up to 64 rows and the tcgen05 kernel after.
   const double wbytes = static_cast<double>(W->N) * W->K / 2;
+  if (W->group == 32 && M <= 8) {
+    c = tm_config{TM_KERNEL_GEMV, 0, 4, 0};
+    while (!normalize_config(W, M, &c, &why) && c.split_k < KB) c.split_k = std::min(KB, c.split_k * 2);
+    if (normalize_config(W, M, &c, &why)) return c;
+  }
   if (M <= 4 && wbytes <= 16e6) {
     c = tm_config{TM_KERNEL_DECODE_MMA, 0, 8, 1};
     if (normalize_config(W, M, &c, &why)) return c;
@@ -659,12 +672,12 @@ const char *tm_version(void) { return "tmw4 0.1 (sm_103a)"; }
 
 const char *tm_last_error(void) { return g_last_error.c_str(); }
 
-// The group the kernels run with for a source group G: 64 or 128.  A
+// The group the kernels run with for a source group G: 32, 64 or 128.  A
 // coarser group (any multiple of 64, per-channel G = K included) is packed
 // as 128 when it is a multiple of 128, else as 64, each of its scales and
 // zeros repeated over the finer groups it spans: the dequantized weight is
 // identical by construction.
-static int packed_group(int group) { return group % 128 == 0 ? 128 : 64; }
+static int packed_group(int group) { return group == 32 ? 32 : group % 128 == 0 ? 128 : 64; }
 
 // Packs codes in layout `src` (q: u8 [K][N], AWQ int32 [K][N/8] or GPTQ
 // int32 [K/8][N]), fp16/bf16 scales [K/G][N] and zeros (same layout family
@@ -677,8 +690,10 @@ static tm_status pack_common(int src, const void *q, const void *scales, const v
   if (q == nullptr || scales == nullptr) return fail(TM_ERR_INVALID_ARG, "codes and scales must not be NULL");
   if (dtype != TM_F16 && dtype != TM_BF16) return fail(TM_ERR_INVALID_ARG, "dtype must be TM_F16 or TM_BF16");
   if (K <= 0 || N <= 0) return fail(TM_ERR_INVALID_ARG, "K and N must be positive");
-  if (group <= 0 || group % 64 != 0) return fail(TM_ERR_INVALID_ARG, "group must be a positive multiple of 64");
-  if (K % group != 0) return fail(TM_ERR_INVALID_ARG, "K (%d) must be a multiple of group (%d)", K, group);
+  if (group != 32 && (group <= 0 || group % 64 != 0))
+    return fail(TM_ERR_INVALID_ARG, "group must be 32 or a positive multiple of 64");
+  if (K % group != 0 || K % 64 != 0)
+    return fail(TM_ERR_INVALID_ARG, "K (%d) must be a multiple of group (%d) and of 64", K, group);
   if (N % 128 != 0) return fail(TM_ERR_INVALID_ARG, "N (%d) must be a multiple of 128", N);
   if (!aligned16(q) || !aligned16(scales) || (zeros && !aligned16(zeros)))
     return fail(TM_ERR_INVALID_ARG, "codes, scales and zeros must be 16-byte aligned");

@@ -157,19 +157,24 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
   // scale and zero bytes are in flight while the current atom is
   // dequantized; nothing consumes a loaded value before its atom's turn, so
   // no load stalls the warp early
+  // sc/zb[h][col]: scale and zero byte of column nA (col 0) / nB (col 1) for
+  // the atom's 32-K half h (the same group unless G = 32)
   uint4 cur[4], nxt[4];
-  uint16_t sc_c[2], sc_n[2];
-  uint8_t zb_c[2], zb_n[2];
+  uint16_t sc_c[2][2], sc_n[2][2];
+  uint8_t zb_c[2][2], zb_n[2][2];
   const bool has_zeros = p.zeros != nullptr;
-  auto fetch = [&](int kb, uint4 (&c)[4], uint16_t (&sc)[2], uint8_t (&zb)[2]) {
+  auto fetch = [&](int kb, uint4 (&c)[4], uint16_t (&sc)[2][2], uint8_t (&zb)[2][2]) {
     const uint4 *atom = reinterpret_cast<const uint4 *>(p.qw + atom_offset(kb, na, KB));
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = ldg_stream(atom + lane + 32 * i);
-    const int g = (kb * ATOM_K) / p.group;
-    sc[0] = __ldg(p.scales + scale_index(g, nA, G_rows));
-    sc[1] = __ldg(p.scales + scale_index(g, nB, G_rows));
-    zb[0] = has_zeros ? __ldg(p.zeros + zero_byte(g, nA, G_rows)) : static_cast<uint8_t>(0x88u);
-    zb[1] = has_zeros ? __ldg(p.zeros + zero_byte(g, nB, G_rows)) : static_cast<uint8_t>(0x88u);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int g = (kb * ATOM_K + 32 * h) / p.group;
+      sc[h][0] = __ldg(p.scales + scale_index(g, nA, G_rows));
+      sc[h][1] = __ldg(p.scales + scale_index(g, nB, G_rows));
+      zb[h][0] = has_zeros ? __ldg(p.zeros + zero_byte(g, nA, G_rows)) : static_cast<uint8_t>(0x88u);
+      zb[h][1] = has_zeros ? __ldg(p.zeros + zero_byte(g, nB, G_rows)) : static_cast<uint8_t>(0x88u);
+    }
   };
   const int zsh = (lane & 1) * 4;   // nA and nB = nA + 32 have the same parity
   int kb = kb0 + warp;
@@ -194,12 +199,14 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
   for (; kb < kb1; kb += GEMV_WARPS) {
     const int kbn = kb + GEMV_WARPS;
     if (kbn < kb1) fetch(kbn, nxt, sc_n, zb_n);
-    uint32_t s2c[2], zmc[2];
+    uint32_t s2c[2][2], zmc[2][2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      s2c[i] = dup16(sc_c[i]);
-      zmc[i] = zero_magic2<BF16>((static_cast<uint32_t>(zb_c[i]) >> zsh) & 0xFu);
-    }
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        s2c[h][i] = dup16(sc_c[h][i]);
+        zmc[h][i] = zero_magic2<BF16>((static_cast<uint32_t>(zb_c[h][i]) >> zsh) & 0xFu);
+      }
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
       const int col = ci & 1, h = ci >> 1;
@@ -207,7 +214,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         uint32_t d[4];
-        dequant_word<BF16>(w[j], zmc[col], s2c[col], d);
+        dequant_word<BF16>(w[j], zmc[h][col], s2c[h][col], d);
         const int kloc = (kb - kb0) * ATOM_K + 32 * h + 8 * j;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
@@ -224,10 +231,12 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      sc_c[i] = sc_n[i];
-      zb_c[i] = zb_n[i];
-    }
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        sc_c[h][i] = sc_n[h][i];
+        zb_c[h][i] = zb_n[h][i];
+      }
   }
   // per-warp partials -> shared memory, then a fixed-order sum over warps
 #pragma unroll

@@ -54,7 +54,8 @@ __host__ __device__ constexpr int kbs_for(int block_m) {
 }
 __host__ __device__ constexpr int a_kb_bytes(int block_m) { return block_m * BLOCK_K * 2; }
 __host__ __device__ constexpr int stage_bytes(int block_m) {
-  return kbs_for(block_m) * (a_kb_bytes(block_m) + W_KB_BYTES + SC_GROUP_BYTES + ZP_GROUP_BYTES);
+  // (room for two groups per 64-K block: G = 32)
+  return kbs_for(block_m) * (a_kb_bytes(block_m) + W_KB_BYTES + 2 * SC_GROUP_BYTES + 2 * ZP_GROUP_BYTES);
 }
 // A copy takes ~1500 cycles to land under prefill load, so the ring must be
 // deep enough to cover it: 256-row tiles take the six stages that fit.
@@ -104,8 +105,8 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
   constexpr int A_KB = a_kb_bytes(BLOCK_M);
   constexpr int A_STAGE = KBS * A_KB;
   constexpr int W_STAGE = KBS * W_KB_BYTES;
-  constexpr int SC_STAGE = KBS * SC_GROUP_BYTES;   // room for KBS groups (G = 64)
-  constexpr int ZP_STAGE = KBS * ZP_GROUP_BYTES;
+  constexpr int SC_STAGE = 2 * KBS * SC_GROUP_BYTES;   // room for 2 KBS groups (G = 32)
+  constexpr int ZP_STAGE = 2 * KBS * ZP_GROUP_BYTES;
   constexpr int TMEM_COLS = tmem_cols(BLOCK_M);
   constexpr int A_COL0 = tmem_a_col0(BLOCK_M);
   constexpr int TS = tmem_a_stages(BLOCK_M);
@@ -302,12 +303,21 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         }
         tc_fence_after();
         if (quarter == 2 && lane == 0) TMW4_STAMP(2, i);
+        // groups of the block's two 32-K halves (the same group unless G = 32)
         const int gi = ((kbf + b) * BLOCK_K) / p.group - gf;
+        const int gi1 = ((kbf + b) * BLOCK_K + 32) / p.group - gf;
         const uint16_t sc =
             reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + gi * SC_GROUP_BYTES)[r];
+        const uint16_t sc1 =
+            reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + gi1 * SC_GROUP_BYTES)[r];
         const uint32_t z =
             p.zeros != nullptr
                 ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + gi * ZP_GROUP_BYTES + (r >> 1)]) >>
+                   ((r & 1) * 4)) & 0xFu
+                : 8u;
+        const uint32_t z1 =
+            p.zeros != nullptr
+                ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + gi1 * ZP_GROUP_BYTES + (r >> 1)]) >>
                    ((r & 1) * 4)) & 0xFu
                 : 8u;
         const uint8_t *src = wsrc + s * W_STAGE + b * W_KB_BYTES;
@@ -322,6 +332,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
           if (lane == 0) mbar_arrive(empty_bar + s);   // last read of this stage done
         }
         const uint32_t s2 = dup16(sc), zm2 = zero_magic2<BF16>(z);
+        const uint32_t s2b = dup16(sc1), zm2b = zero_magic2<BF16>(z1);
         uint32_t d0[16], d1[16];
         {
           const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
             dequant_word<BF16>(w0[q4], zm2, s2, o);
 #pragma unroll
             for (int q = 0; q < 4; ++q) d0[4 * q4 + q] = o[q];
-            dequant_word<BF16>(w1[q4], zm2, s2, o);
+            dequant_word<BF16>(w1[q4], zm2b, s2b, o);
 #pragma unroll
             for (int q = 0; q < 4; ++q) d1[4 * q4 + q] = o[q];
           }
