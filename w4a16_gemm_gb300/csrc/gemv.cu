@@ -167,13 +167,21 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
     const uint4 *atom = reinterpret_cast<const uint4 *>(p.qw + atom_offset(kb, na, KB));
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = ldg_stream(atom + lane + 32 * i);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int g = (kb * ATOM_K + 32 * h) / p.group;
-      sc[h][0] = __ldg(p.scales + scale_index(g, nA, G_rows));
-      sc[h][1] = __ldg(p.scales + scale_index(g, nB, G_rows));
-      zb[h][0] = has_zeros ? __ldg(p.zeros + zero_byte(g, nA, G_rows)) : static_cast<uint8_t>(0x88u);
-      zb[h][1] = has_zeros ? __ldg(p.zeros + zero_byte(g, nB, G_rows)) : static_cast<uint8_t>(0x88u);
+    const int g = (kb * ATOM_K) / p.group;
+    sc[0][0] = __ldg(p.scales + scale_index(g, nA, G_rows));
+    sc[0][1] = __ldg(p.scales + scale_index(g, nB, G_rows));
+    zb[0][0] = has_zeros ? __ldg(p.zeros + zero_byte(g, nA, G_rows)) : static_cast<uint8_t>(0x88u);
+    zb[0][1] = has_zeros ? __ldg(p.zeros + zero_byte(g, nB, G_rows)) : static_cast<uint8_t>(0x88u);
+    if (p.group == 32) {   // the second 32-K half has a group of its own
+      sc[1][0] = __ldg(p.scales + scale_index(g + 1, nA, G_rows));
+      sc[1][1] = __ldg(p.scales + scale_index(g + 1, nB, G_rows));
+      zb[1][0] = has_zeros ? __ldg(p.zeros + zero_byte(g + 1, nA, G_rows)) : static_cast<uint8_t>(0x88u);
+      zb[1][1] = has_zeros ? __ldg(p.zeros + zero_byte(g + 1, nB, G_rows)) : static_cast<uint8_t>(0x88u);
+    } else {
+      sc[1][0] = sc[0][0];
+      sc[1][1] = sc[0][1];
+      zb[1][0] = zb[0][0];
+      zb[1][1] = zb[0][1];
     }
   };
   const int zsh = (lane & 1) * 4;   // nA and nB = nA + 32 have the same parity

@@ -303,21 +303,12 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         }
         tc_fence_after();
         if (quarter == 2 && lane == 0) TMW4_STAMP(2, i);
-        // groups of the block's two 32-K halves (the same group unless G = 32)
         const int gi = ((kbf + b) * BLOCK_K) / p.group - gf;
-        const int gi1 = ((kbf + b) * BLOCK_K + 32) / p.group - gf;
         const uint16_t sc =
             reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + gi * SC_GROUP_BYTES)[r];
-        const uint16_t sc1 =
-            reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + gi1 * SC_GROUP_BYTES)[r];
         const uint32_t z =
             p.zeros != nullptr
                 ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + gi * ZP_GROUP_BYTES + (r >> 1)]) >>
-                   ((r & 1) * 4)) & 0xFu
-                : 8u;
-        const uint32_t z1 =
-            p.zeros != nullptr
-                ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + gi1 * ZP_GROUP_BYTES + (r >> 1)]) >>
                    ((r & 1) * 4)) & 0xFu
                 : 8u;
         const uint8_t *src = wsrc + s * W_STAGE + b * W_KB_BYTES;
@@ -332,7 +323,19 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
           if (lane == 0) mbar_arrive(empty_bar + s);   // last read of this stage done
         }
         const uint32_t s2 = dup16(sc), zm2 = zero_magic2<BF16>(z);
-        const uint32_t s2b = dup16(sc1), zm2b = zero_magic2<BF16>(z1);
+        // the block's second 32-K half has a group of its own only when G = 32
+        uint32_t s2b = s2, zm2b = zm2;
+        if (p.group == 32) {
+          const uint16_t sc1 =
+              reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + (gi + 1) * SC_GROUP_BYTES)[r];
+          const uint32_t z1 =
+              p.zeros != nullptr
+                  ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + (gi + 1) * ZP_GROUP_BYTES + (r >> 1)]) >>
+                     ((r & 1) * 4)) & 0xFu
+                  : 8u;
+          s2b = dup16(sc1);
+          zm2b = zero_magic2<BF16>(z1);
+        }
         uint32_t d0[16], d1[16];
         {
           const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
