@@ -59,7 +59,9 @@ typedef enum { TM_F16 = 0, TM_BF16 = 1 } tm_dtype;
 /* Kernel families (tm_config.kernel). */
 enum {
   TM_KERNEL_AUTO = 0,     /* pick from the tuned table, else the built-in rule */
-  TM_KERNEL_GEMV = 1,     /* CUDA-core split-K GEMV, M <= 8                    */
+  TM_KERNEL_GEMV = 1,     /* split-K GEMV: 64-column strips, eight warps over K;
+                              dq_warps 0: CUDA-core FMAs, M <= 8; dq_warps 1:
+                              register-operand tensor-core MMAs, M <= 16 */
   TM_KERNEL_TC = 2,       /* tcgen05/TMEM kernel, weights staged by TMA        */
   TM_KERNEL_TC_DECODE = 3, /* tcgen05/TMEM kernel for small M (block_m 16..64):
                               persistent stream-K grid, weights staged in shared
@@ -222,8 +224,13 @@ tm_status tm_gemm_w4a16_ex(const void *A, const tm_packed *W, void *C, int M, in
 tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, void *C, int M, int N, int K,
                                 void *stream);
 
-/* Dequant-only: W_out [K][N] (device, handle's dtype) = T(s*(q - z)),
- * bit-exact with a single round-to-nearest-even per element. */
+/* Dequant-only (TurboMind paper, pith.science review, Figure 6: the runtime
+ * conversion of the packed integers to floating point, then the scaling):
+ *   W_out  device, [K][N] of the handle's dtype, 16-byte aligned, caller-
+ *          allocated; W_out[k][n] = T(s[k/G][n] * (q[k][n] - z[k/G][n])),
+ *          bit-exact with a single round-to-nearest-even per element.
+ * Stream-ordered on `stream`; TM_ERR_INVALID_ARG for a bad handle or a
+ * misaligned / NULL W_out. */
 tm_status tm_dequant_w4(const tm_packed *W, void *W_out, void *stream);
 
 /* Releases a packed weight (stream-ordered cudaFreeAsync). NULL is OK. */
@@ -236,9 +243,11 @@ tm_status tm_packed_get(const tm_packed *W, tm_packed_info *info);
  * the environment override TM_VARIANT="kernel:block_m:split_k:dq_warps"
  * (kernel gemv, tc, tc_decode, decode_mma or its number) when it can run
  * this shape, else the tuned table's entry for M's row bucket, else the
- * built-in rule (measured crossovers: the register-MMA decode kernel for
- * M <= 16, the tcgen05 decode kernel up to 64 rows, the tcgen05 kernel
- * beyond). */
+ * built-in rule, set from crossovers measured on GB300: up to 4 rows and at
+ * most 16 MB of packed weight, the register-MMA decode kernel in clusters
+ * of 8 CTAs per tile; up to 8 rows its persistent stream-K grid; up to 64
+ * rows the tcgen05 decode kernel; beyond, the tcgen05 kernel (groups of 32:
+ * the CUDA-core GEMV up to 8 rows, else the tcgen05 kernel). */
 tm_status tm_select(const tm_packed *W, int M, tm_config *out);
 
 /* Variant selection by measured throughput (the pages give no selection
@@ -254,7 +263,8 @@ tm_status tm_select(const tm_packed *W, int M, tm_config *out);
  * the row bucket being the next power of two >= M.  If the environment
  * variable TM_TUNE_CACHE names a file, the table is saved there.  best_out
  * (host, may be NULL) receives nM configs.  Allocates temporary device
- * copies of the weight (at most 7) and frees them before returning.
+ * copies of the weight (at most 7 besides W) and frees them before
+ * returning.
  * Deviation from the plain tm_tune(Ms, W, stream) signature: best_out. */
 tm_status tm_tune(const int *Ms, int nM, const tm_packed *W, void *stream, tm_config *best_out);
 
