@@ -128,6 +128,8 @@ typedef struct {
   const void *scales;  /* device */
   const void *zeros;   /* device, NULL if symmetric */
   size_t qweight_bytes, scales_bytes, zeros_bytes;
+  int32_t bits;        /* bits per weight code: 4, or 8 (tm_pack_w8 / tm_pack_fp8) */
+  int32_t fp8;         /* 1: the 8-bit codes are FP8 E4M3 */
 } tm_packed_info;
 
 /* Offline repack (TurboMind paper, arXiv abstract: "offline weight
@@ -180,6 +182,28 @@ tm_status tm_pack_awq(const int32_t *qweight, const int32_t *qzeros, const void 
 tm_status tm_pack_gptq(const int32_t *qweight, const int32_t *qzeros, const void *scales, int zero_offset,
                        int K, int N, int group, tm_dtype dtype, void *stream, tm_packed **out);
 
+/* 8-bit weights on the same pipeline (TurboMind paper, arXiv abstract:
+ * "hybrid precision formats"; pith.science review, Figure 12 legend: FP8
+ * weights).  The pages print no format; read as the int4 method with 8-bit
+ * codes, one rounding per weight:
+ *   tm_pack_w8   W = T(s * (q - z)), q and z in 0..255; zeros device
+ *                [K/group][N] bytes, or NULL for the symmetric format (z = 128)
+ *   tm_pack_fp8  W = T(s * e4m3(q)): q are FP8 E4M3 ("fn": bias 7, no
+ *                infinities) bit patterns; no zeros.  The NaN codes 0x7F and
+ *                0xFF give NaN weights.
+ *   q       device, [K][N] uint8 codes
+ *   scales  device, [K/group][N] 16-bit values of type dtype
+ * Packed layout: 128-column tiles, 64-K blocks of 8192 bytes; inside a block
+ * 16-byte chunk kq * 128 + c holds the 16 consecutive K values 16 kq + 0..15
+ * of column c.  Zeros are tile-major [N/128][K/G][128] bytes.  Shapes, groups,
+ * alignment and ownership as for tm_pack_w4.  These weights run on the
+ * CUDA-core GEMV (M <= 8) and the TC kernel (any M); other kernels report
+ * TM_ERR_UNSUPPORTED for them. */
+tm_status tm_pack_w8(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N, int group,
+                     tm_dtype dtype, void *stream, tm_packed **out);
+tm_status tm_pack_fp8(const uint8_t *q, const void *scales, int K, int N, int group, tm_dtype dtype,
+                      void *stream, tm_packed **out);
+
 /* Online GEMM (TurboMind paper, arXiv abstract: the online half of the pipeline;
  * pith.science review, Figure 9: dequantization overlapped with the MMA).
  *   A  device, [M][K] values of the handle's dtype, 16-byte aligned
@@ -228,7 +252,8 @@ tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, void *C, int 
  * conversion of the packed integers to floating point, then the scaling):
  *   W_out  device, [K][N] of the handle's dtype, 16-byte aligned, caller-
  *          allocated; W_out[k][n] = T(s[k/G][n] * (q[k][n] - z[k/G][n])),
- *          bit-exact with a single round-to-nearest-even per element.
+ *          bit-exact with a single round-to-nearest-even per element (for
+ *          8-bit handles the 8-bit formula of tm_pack_w8 / tm_pack_fp8).
  * Stream-ordered on `stream`; TM_ERR_INVALID_ARG for a bad handle or a
  * misaligned / NULL W_out. */
 tm_status tm_dequant_w4(const tm_packed *W, void *W_out, void *stream);

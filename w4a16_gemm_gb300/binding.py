@@ -47,7 +47,7 @@ class TmPackedInfo(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("symmetric", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p),
                 ("qweight_bytes", ctypes.c_size_t), ("scales_bytes", ctypes.c_size_t),
-                ("zeros_bytes", ctypes.c_size_t)]
+                ("zeros_bytes", ctypes.c_size_t), ("bits", ctypes.c_int32), ("fp8", ctypes.c_int32)]
 
 
 _LIB = None
@@ -57,6 +57,8 @@ _VP, _I, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
 SIGNATURES = [
     ("tm_pack_w4", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
     ("tm_pack_awq", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
+    ("tm_pack_w8", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
+    ("tm_pack_fp8", _I, [_VP, _VP, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
     ("tm_pack_gptq", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, ctypes.POINTER(_VP)]),
     ("tm_gemm_w4a16", _I, [_VP, _VP, _VP, _I, _I, _I, _VP]),
     ("tm_gemm_w4a16_ex", _I, [_VP, _VP, _VP, _I, _I, _I, ctypes.POINTER(TmConfig), _VP]),
@@ -118,6 +120,7 @@ class PackedW4:
         self.K, self.N, self.group, self.dtype = K, N, group, dtype
         self.symmetric = symmetric
         self.device = device
+        self.bits, self.fp8 = 4, False
 
     def info(self) -> TmPackedInfo:
         inf = TmPackedInfo()
@@ -190,8 +193,46 @@ def pack(q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | None, grou
 
 def _packed(handle: int, K: int, N: int, dtype: torch.dtype, symmetric: bool, device) -> PackedW4:
     W = PackedW4(handle, K, N, 0, dtype, symmetric, device)
-    W.group = W.info().group        # the group the kernels run with
+    inf = W.info()
+    W.group = inf.group             # the group the kernels run with
+    W.bits, W.fp8 = inf.bits, bool(inf.fp8)
     return W
+
+
+def _codes_2d(q: torch.Tensor) -> torch.Tensor:
+    if q.dtype != torch.uint8 or q.dim() != 2 or not q.is_cuda:
+        raise ValueError("q must be a 2-D uint8 CUDA tensor")
+    return q.contiguous()
+
+
+def pack_w8(q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | None, group: int,
+            stream=None) -> PackedW4:
+    """tm_pack_w8: int8 codes q [K,N] uint8 (0..255), scales [K/G,N], zeros [K/G,N] uint8 or None."""
+    q = _codes_2d(q)
+    if scales.dtype not in _DT:
+        raise ValueError("scales must be float16 or bfloat16")
+    K, N = q.shape
+    scales = scales.contiguous()
+    zp = None if zeros is None else _codes_2d(zeros).data_ptr()
+    h = ctypes.c_void_p()
+    with torch.cuda.device(q.device):
+        _check(lib().tm_pack_w8(q.data_ptr(), scales.data_ptr(), zp, K, N, group, _DT[scales.dtype],
+                                _stream(stream), ctypes.byref(h)))
+    return _packed(h.value, K, N, scales.dtype, zeros is None, q.device)
+
+
+def pack_fp8(q: torch.Tensor, scales: torch.Tensor, group: int, stream=None) -> PackedW4:
+    """tm_pack_fp8: FP8 E4M3 codes q [K,N] uint8 (bit patterns), scales [K/G,N]."""
+    q = _codes_2d(q)
+    if scales.dtype not in _DT:
+        raise ValueError("scales must be float16 or bfloat16")
+    K, N = q.shape
+    scales = scales.contiguous()
+    h = ctypes.c_void_p()
+    with torch.cuda.device(q.device):
+        _check(lib().tm_pack_fp8(q.data_ptr(), scales.data_ptr(), K, N, group, _DT[scales.dtype],
+                                 _stream(stream), ctypes.byref(h)))
+    return _packed(h.value, K, N, scales.dtype, True, q.device)
 
 
 def _int32_2d(t: torch.Tensor, name: str) -> torch.Tensor:

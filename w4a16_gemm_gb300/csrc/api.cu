@@ -32,6 +32,8 @@ struct tm_packed {
   int K, N, group;
   tm_dtype dtype;
   int symmetric;
+  int bits;   // 4, or 8
+  int fp8;    // 8-bit codes are FP8 E4M3
   int device;
   uint8_t *qw;
   uint16_t *scales;
@@ -234,14 +236,16 @@ static int m_bucket(int M) {
   while (b < M && b < (1 << 30)) b <<= 1;
   return b;
 }
+// fmt: code format, 0 int4, 1 int8, 2 FP8
 struct TuneKey {
-  int N, K, group, dtype, sym, mb;
+  int N, K, group, dtype, sym, mb, fmt;
   bool operator<(const TuneKey &o) const {
-    return std::tie(N, K, group, dtype, sym, mb) < std::tie(o.N, o.K, o.group, o.dtype, o.sym, o.mb);
+    return std::tie(N, K, group, dtype, sym, mb, fmt) < std::tie(o.N, o.K, o.group, o.dtype, o.sym, o.mb, o.fmt);
   }
 };
+static int code_format(const tm_packed *W) { return W->bits == 8 ? (W->fp8 ? 2 : 1) : 0; }
 static TuneKey tune_key(const tm_packed *W, int M) {
-  return TuneKey{W->N, W->K, W->group, (int)W->dtype, W->symmetric, m_bucket(M)};
+  return TuneKey{W->N, W->K, W->group, (int)W->dtype, W->symmetric, m_bucket(M), code_format(W)};
 }
 struct TuneVal {
   tm_config cfg;
@@ -272,6 +276,11 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
   if (W->group == 32 && (c->kernel == TM_KERNEL_DECODE_MMA || c->kernel == TM_KERNEL_TC_DECODE ||
                          (c->kernel == TM_KERNEL_GEMV && c->dq_warps == 1))) {
     if (why) *why = "this kernel needs groups of at least 64";
+    return false;
+  }
+  // 8-bit codes run on the CUDA-core GEMV and the TC kernel
+  if (W->bits == 8 && !(c->kernel == TM_KERNEL_TC || (c->kernel == TM_KERNEL_GEMV && c->dq_warps == 0))) {
+    if (why) *why = "8-bit weights run on the CUDA-core GEMV and the TC kernel only";
     return false;
   }
   if (c->kernel == TM_KERNEL_DECODE_MMA) {
@@ -342,7 +351,7 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
       if (why) *why = "TC dq_warps must be 4, 8 or 16";
       return false;
     }
-    if (!tc_variant_ok(c->block_m, c->dq_warps)) {
+    if (!tc_variant_ok(c->block_m, c->dq_warps, W->bits)) {
       if (why) *why = "this block_m has too few pipeline stages for that many dequant warps";
       return false;
     }
@@ -389,7 +398,7 @@ static tm_config default_config(const tm_packed *W, int M, int dev) {
   // rows the persistent stream-K grid of the register-MMA kernel; beyond,
   // the tcgen05 decode kernel up to 64 rows and the tcgen05 kernel after.
   const double wbytes = static_cast<double>(W->N) * W->K / 2;
-  if (W->group == 32 && M <= 8) {
+  if ((W->group == 32 || W->bits == 8) && M <= 8) {
     c = tm_config{TM_KERNEL_GEMV, 0, 4, 0};
     while (!normalize_config(W, M, &c, &why) && c.split_k < KB) c.split_k = std::min(KB, c.split_k * 2);
     if (normalize_config(W, M, &c, &why)) return c;
@@ -594,6 +603,8 @@ static tm_status run_gemm(const void *A, const tm_packed *W, void *C, int M, con
   a.N = W->N;
   a.K = W->K;
   a.group = W->group;
+  a.wbits = W->bits;
+  a.fp8 = W->fp8;
   int dec_grid = 0;
   size_t ws_floats = 0, n_counters = 0;
   plan_work(W, M, cfg, &a, &dec_grid, &ws_floats, &n_counters);
@@ -713,6 +724,8 @@ static tm_status pack_common(int src, const void *q, const void *scales, const v
   W->group = G;
   W->dtype = dtype;
   W->symmetric = zeros == nullptr ? 1 : 0;
+  W->bits = 4;
+  W->fp8 = 0;
   W->device = dev;
   W->qw_bytes = static_cast<size_t>(K) * N / 2;
   W->scales_bytes = static_cast<size_t>(K / G) * N * 2;
@@ -755,6 +768,69 @@ tm_status tm_pack_gptq(const int32_t *qweight, const int32_t *qzeros, const void
                      "tm_pack_gptq");
 }
 
+// Packs 8-bit codes (u8 [K][N]): int8 with byte zeros [K/G][N] (NULL:
+// symmetric, zero 128), or FP8 E4M3 (fp8 = 1, no zeros).
+static tm_status pack8_common(const uint8_t *q, const void *scales, const uint8_t *zeros, int fp8, int K, int N,
+                              int group, tm_dtype dtype, void *stream, tm_packed **out, const char *what) {
+  if (out == nullptr) return fail(TM_ERR_INVALID_ARG, "out must not be NULL");
+  *out = nullptr;
+  if (q == nullptr || scales == nullptr) return fail(TM_ERR_INVALID_ARG, "codes and scales must not be NULL");
+  if (dtype != TM_F16 && dtype != TM_BF16) return fail(TM_ERR_INVALID_ARG, "dtype must be TM_F16 or TM_BF16");
+  if (K <= 0 || N <= 0) return fail(TM_ERR_INVALID_ARG, "K and N must be positive");
+  if (group != 32 && (group <= 0 || group % 64 != 0))
+    return fail(TM_ERR_INVALID_ARG, "group must be 32 or a positive multiple of 64");
+  if (K % group != 0 || K % 64 != 0)
+    return fail(TM_ERR_INVALID_ARG, "K (%d) must be a multiple of group (%d) and of 64", K, group);
+  if (N % 128 != 0) return fail(TM_ERR_INVALID_ARG, "N (%d) must be a multiple of 128", N);
+  if (!aligned16(q) || !aligned16(scales) || (zeros && !aligned16(zeros)))
+    return fail(TM_ERR_INVALID_ARG, "codes, scales and zeros must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = -1;
+  tm_status s = current_device(&dev);
+  if (s != TM_OK) return s;
+  const int G = packed_group(group), rep = group / G;
+  tm_packed *W = new tm_packed{};
+  W->magic = kPackedMagic;
+  W->K = K;
+  W->N = N;
+  W->group = G;
+  W->dtype = dtype;
+  W->symmetric = zeros == nullptr ? 1 : 0;
+  W->bits = 8;
+  W->fp8 = fp8;
+  W->device = dev;
+  W->qw_bytes = static_cast<size_t>(K) * N;
+  W->scales_bytes = static_cast<size_t>(K / G) * N * 2;
+  W->zeros_bytes = zeros ? static_cast<size_t>(K / G) * N : 0;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&W->qw), W->qw_bytes, st);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void **>(&W->scales), W->scales_bytes, st);
+  if (e == cudaSuccess && zeros) e = cudaMallocAsync(reinterpret_cast<void **>(&W->zeros), W->zeros_bytes, st);
+  if (e == cudaSuccess) e = launch_repack8(q, W->qw, K, N, st);
+  if (e == cudaSuccess)
+    e = launch_pack_scales(static_cast<const uint16_t *>(scales), W->scales, K / G, N, rep, st);
+  if (e == cudaSuccess && zeros) e = launch_pack_zeros8(zeros, W->zeros, K / G, N, rep, st);
+  if (e != cudaSuccess) {
+    if (W->qw) cudaFreeAsync(W->qw, st);
+    if (W->scales) cudaFreeAsync(W->scales, st);
+    if (W->zeros) cudaFreeAsync(W->zeros, st);
+    W->magic = 0;
+    delete W;
+    return fail_cuda(e, what);
+  }
+  *out = W;
+  return TM_OK;
+}
+
+tm_status tm_pack_w8(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N, int group,
+                     tm_dtype dtype, void *stream, tm_packed **out) {
+  return pack8_common(q, scales, zeros, 0, K, N, group, dtype, stream, out, "tm_pack_w8");
+}
+
+tm_status tm_pack_fp8(const uint8_t *q, const void *scales, int K, int N, int group, tm_dtype dtype,
+                      void *stream, tm_packed **out) {
+  return pack8_common(q, scales, nullptr, 1, K, N, group, dtype, stream, out, "tm_pack_fp8");
+}
+
 tm_status tm_packed_free(tm_packed *W, void *stream) {
   if (W == nullptr) return TM_OK;
   tm_status s = check_handle(W);
@@ -784,6 +860,8 @@ tm_status tm_packed_get(const tm_packed *W, tm_packed_info *info) {
   info->qweight_bytes = W->qw_bytes;
   info->scales_bytes = W->scales_bytes;
   info->zeros_bytes = W->zeros_bytes;
+  info->bits = W->bits;
+  info->fp8 = W->fp8;
   return TM_OK;
 }
 
@@ -792,6 +870,12 @@ tm_status tm_dequant_w4(const tm_packed *W, void *W_out, void *stream) {
   if (s != TM_OK) return s;
   if (W_out == nullptr || !aligned16(W_out))
     return fail(TM_ERR_INVALID_ARG, "W_out must be a 16-byte aligned device pointer");
+  if (W->bits == 8) {
+    cudaError_t e8 = launch_dequant8(W->qw, W->scales, W->symmetric ? nullptr : W->zeros, W->fp8 != 0,
+                                     static_cast<uint16_t *>(W_out), W->K, W->N, W->group, W->dtype == TM_BF16,
+                                     static_cast<cudaStream_t>(stream));
+    return e8 == cudaSuccess ? TM_OK : fail_cuda(e8, "tm_dequant_w4");
+  }
   cudaError_t e = launch_dequant(W->qw, W->scales, W->symmetric ? nullptr : W->zeros,
                                  static_cast<uint16_t *>(W_out), W->K, W->N, W->group,
                                  W->dtype == TM_BF16, static_cast<cudaStream_t>(stream));
@@ -918,6 +1002,7 @@ tm_status tm_tune_load(const char *path) {
         parse_int(line, "\"split_k\"", &v.cfg.split_k) &&
         parse_int(line, "\"dq_warps\"", &v.cfg.dq_warps)) {
       k.mb = m_bucket(M);
+      if (!parse_int(line, "\"fmt\"", &k.fmt)) k.fmt = 0;   // tables without it: int4
       v.M = M;
       g_tune[k] = v;
     }
@@ -935,10 +1020,10 @@ tm_status tm_tune_save(const char *path) {
     const TuneKey &k = kv.first;
     const TuneVal &v = kv.second;
     fprintf(f,
-            "{\"N\": %d, \"K\": %d, \"group\": %d, \"dtype\": %d, \"sym\": %d, \"M\": %d, "
+            "{\"N\": %d, \"K\": %d, \"group\": %d, \"dtype\": %d, \"sym\": %d, \"fmt\": %d, \"M\": %d, "
             "\"m_bucket\": %d, \"kernel\": %d, \"block_m\": %d, \"split_k\": %d, \"dq_warps\": %d, "
             "\"us\": %.3f}\n",
-            k.N, k.K, k.group, k.dtype, k.sym, v.M, k.mb, v.cfg.kernel, v.cfg.block_m, v.cfg.split_k,
+            k.N, k.K, k.group, k.dtype, k.sym, k.fmt, v.M, k.mb, v.cfg.kernel, v.cfg.block_m, v.cfg.split_k,
             v.cfg.dq_warps, v.us);
   }
   fclose(f);
@@ -1254,6 +1339,8 @@ extern "C" tm_status tm_gemm_w4a16_noalloc(const void *A, const tm_packed *W, vo
   a.N = W->N;
   a.K = W->K;
   a.group = W->group;
+  a.wbits = W->bits;
+  a.fp8 = W->fp8;
   int dec_grid = 0;
   size_t ws_floats = 0, tiles = 0;
   plan_work(W, M, cfg, &a, &dec_grid, &ws_floats, &tiles);

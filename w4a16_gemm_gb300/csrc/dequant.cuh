@@ -69,6 +69,77 @@ __device__ __forceinline__ uint32_t zero_magic2(uint32_t z) {
 
 __device__ __forceinline__ uint32_t dup16(uint32_t h) { return (h & 0xFFFFu) * 0x00010001u; }
 
+// 8-bit codes.  Four codes of one word (K order k..k+3, byte i = K k+i) become
+// two packed 16-bit pairs {w0,w1}, {w2,w3} with w = T(s * v), one rounding:
+//   int8 (v = q - z, q and z in 0..255):
+//     fp16: a byte permute places each code under the exponent magic 0x6400
+//           (1024 + q, exact for q <= 255); the subtract of 1024 + z is exact
+//           (|q - z| <= 255); the multiply by the scale is the one rounding.
+//     bf16: 7 mantissa bits cannot hold 128 + q for q >= 128, so each code
+//           goes through fp32: 2^23 + q (exact), minus 2^23 + z (exact), times
+//           s (exact: at most 17 significant bits), one rounding to bf16.
+//   FP8 E4M3 (v = e4m3(q)): exact conversion to fp16 (cvt.rn.f16x2.e4m3x2),
+//     then fp16: one multiply; bf16: widened to fp32 (exact), times s
+//     (exact: at most 12 significant bits), one rounding to bf16.
+// zm2 = (1024 + z) in both fp16 halves (int8, fp16), z8 = z (int8, bf16),
+// s2 = the scale in both halves, sf = the scale in fp32.
+template <bool BF16>
+__device__ __forceinline__ void dequant_word8(uint32_t w, bool fp8, uint32_t zm2, uint32_t z8, uint32_t s2,
+                                              float sf, uint32_t (&out)[2]) {
+  if (fp8) {
+    uint32_t h0, h1;   // fp16 pairs of bytes (0,1) and (2,3)
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+    if constexpr (BF16) {
+      const uint32_t h[2] = {h0, h1};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const __half2 v = *reinterpret_cast<const __half2 *>(&h[i]);
+        const float2 f = __half22float2(v);
+        const __nv_bfloat162 r = __floats2bfloat162_rn(f.x * sf, f.y * sf);
+        out[i] = *reinterpret_cast<const uint32_t *>(&r);
+      }
+    } else {
+      const __half2 s = *reinterpret_cast<const __half2 *>(&s2);
+      const __half2 r0 = __hmul2(*reinterpret_cast<const __half2 *>(&h0), s);
+      const __half2 r1 = __hmul2(*reinterpret_cast<const __half2 *>(&h1), s);
+      out[0] = *reinterpret_cast<const uint32_t *>(&r0);
+      out[1] = *reinterpret_cast<const uint32_t *>(&r1);
+    }
+    return;
+  }
+  if constexpr (BF16) {
+    const float zf = __uint_as_float(0x4B000000u | z8);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float a = (__uint_as_float(0x4B000000u | ((w >> (16 * i)) & 0xFFu)) - zf) * sf;
+      const float b = (__uint_as_float(0x4B000000u | ((w >> (16 * i + 8)) & 0xFFu)) - zf) * sf;
+      const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+      out[i] = *reinterpret_cast<const uint32_t *>(&r);
+    }
+  } else {
+    const __half2 z = *reinterpret_cast<const __half2 *>(&zm2);
+    const __half2 s = *reinterpret_cast<const __half2 *>(&s2);
+    const uint32_t x0 = __byte_perm(w, 0x6464u, 0x5140u);   // {0x64, byte1, 0x64, byte0} -> (1024+q0, 1024+q1)
+    const uint32_t x1 = __byte_perm(w, 0x6464u, 0x5342u);
+    const __half2 r0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&x0), z), s);
+    const __half2 r1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&x1), z), s);
+    out[0] = *reinterpret_cast<const uint32_t *>(&r0);
+    out[1] = *reinterpret_cast<const uint32_t *>(&r1);
+  }
+}
+
+// 8-bit zero point of column n in group g (tile-major bytes); 128 when there
+// is none (symmetric int8, and FP8, whose path ignores it).
+__device__ __forceinline__ uint32_t zero8_of(const uint8_t *zeros, int g, int n, int G_rows) {
+  if (zeros == nullptr) return 128u;
+  return zeros[(static_cast<size_t>(n >> 7) * G_rows + g) * TILE_N + (n & 127)];
+}
+
 // Zero point of column n in group g from the tile-major nibble array; 8 for
 // the symmetric format (zeros == nullptr).
 __device__ __forceinline__ uint32_t zero_of(const uint8_t *zeros, int g, int n, int G_rows) {

@@ -257,6 +257,137 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemmArgs p) {
 }
 
 
+// ----------------------------------------------------------- 8-bit weights
+// The same CTA structure for 8-bit codes (int8 with byte zeros, or FP8 E4M3;
+// GemmArgs::fp8): a strip's 64-K atom is half of an 8 KB tile block, lane l
+// again owns columns nA = 64 na + l and nB = nA + 32 and loads their 64 K as
+// 4 + 4 chunks of 16 consecutive K (512 contiguous bytes per warp
+// instruction); each word of 4 codes becomes two pairs w = T(s * v)
+// (dequant.cuh) and meets the activations in mixed-precision FMAs.
+template <bool BF16, int MT>
+__global__ void __launch_bounds__(256) gemv8_kernel(GemmArgs p) {
+  extern __shared__ float4 smem_f4[];
+  float *red = reinterpret_cast<float *>(smem_f4);          // [GEMV_WARPS][MT][64]
+  uint16_t *As = reinterpret_cast<uint16_t *>(red + GEMV_WARPS * MT * 64);  // [MT][ldA]
+  const int na = blockIdx.x, split = blockIdx.y;
+  const int KB = p.K / ATOM_K;
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(KB, kb0 + p.kb_per_split);
+  const int ldA = p.kb_per_split * ATOM_K;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int M = p.M;
+  const bool fp8 = p.fp8 != 0;
+
+  float acc[MT][2];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0.f;
+
+  const int nA = na * ATOM_N + lane, nB = nA + 32;
+  const int G_rows = p.K / p.group;
+  const bool has_zeros = p.zeros != nullptr;
+  // cur/nxt[2 kq + col]: chunk kq (16 K) of column nA (col 0) / nB (col 1);
+  // sc/zb[h][col]: scale and zero of the atom's 32-K half h
+  uint4 cur[8], nxt[8];
+  uint16_t sc_c[2][2], sc_n[2][2];
+  uint8_t zb_c[2][2], zb_n[2][2];
+  auto zero8 = [&](int g, int n) -> uint8_t {
+    return has_zeros ? __ldg(p.zeros + (static_cast<size_t>(n >> 7) * G_rows + g) * TILE_N + (n & 127))
+                     : static_cast<uint8_t>(128u);
+  };
+  auto fetch = [&](int kb, uint4 (&c)[8], uint16_t (&sc)[2][2], uint8_t (&zb)[2][2]) {
+    const uint8_t *blk = p.qw + (static_cast<size_t>(na >> 1) * KB + kb) * (2 * BLOCK_BYTES) + (na & 1) * ATOM_N * 16;
+#pragma unroll
+    for (int kq = 0; kq < 4; ++kq) {
+      const uint4 *row = reinterpret_cast<const uint4 *>(blk + kq * 2048);
+      c[2 * kq] = ldg_stream(row + lane);
+      c[2 * kq + 1] = ldg_stream(row + lane + 32);
+    }
+    const int g = (kb * ATOM_K) / p.group;
+    sc[0][0] = __ldg(p.scales + scale_index(g, nA, G_rows));
+    sc[0][1] = __ldg(p.scales + scale_index(g, nB, G_rows));
+    zb[0][0] = zero8(g, nA);
+    zb[0][1] = zero8(g, nB);
+    if (p.group == 32) {   // the second 32-K half has a group of its own
+      sc[1][0] = __ldg(p.scales + scale_index(g + 1, nA, G_rows));
+      sc[1][1] = __ldg(p.scales + scale_index(g + 1, nB, G_rows));
+      zb[1][0] = zero8(g + 1, nA);
+      zb[1][1] = zero8(g + 1, nB);
+    } else {
+      sc[1][0] = sc[0][0];
+      sc[1][1] = sc[0][1];
+      zb[1][0] = zb[0][0];
+      zb[1][1] = zb[0][1];
+    }
+  };
+  int kb = kb0 + warp;
+  if (kb < kb1) fetch(kb, cur, sc_c, zb_c);
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // activations of this K range -> shared memory, 16 bytes per copy (rows >= M are zero)
+  const int klen = (kb1 - kb0) * ATOM_K;
+  for (int idx = tid; idx < MT * (klen / 8); idx += blockDim.x) {
+    const int m = idx / (klen / 8), kk = (idx % (klen / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M)
+      v = *reinterpret_cast<const uint4 *>(p.A + static_cast<size_t>(m) * p.K + kb0 * ATOM_K + kk);
+    *reinterpret_cast<uint4 *>(As + m * ldA + kk) = v;
+  }
+  __syncwarp();   // a CTA barrier counts a warp as arrived once any lane reaches it
+  __syncthreads();
+
+  for (; kb < kb1; kb += GEMV_WARPS) {
+    const int kbn = kb + GEMV_WARPS;
+    if (kbn < kb1) fetch(kbn, nxt, sc_n, zb_n);
+    uint32_t s2c[2][2], zmc[2][2];
+    float sfc[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        s2c[h][i] = dup16(sc_c[h][i]);
+        zmc[h][i] = zero_magic2<false>(zb_c[h][i]);
+        sfc[h][i] = BF16 ? __uint_as_float(static_cast<uint32_t>(sc_c[h][i]) << 16)
+                         : __half2float(__ushort_as_half(sc_c[h][i]));
+      }
+#pragma unroll
+    for (int ci = 0; ci < 8; ++ci) {
+      const int kq = ci >> 1, col = ci & 1, h = kq >> 1;
+      const uint32_t w[4] = {cur[ci].x, cur[ci].y, cur[ci].z, cur[ci].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t d[2];
+        dequant_word8<BF16>(w[j], fp8, zmc[h][col], zb_c[h][col], s2c[h][col], sfc[h][col], d);
+        const int kloc = (kb - kb0) * ATOM_K + 16 * kq + 4 * j;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const uint2 av = *reinterpret_cast<const uint2 *>(As + m * ldA + kloc);
+          float s = acc[m][col];
+          s = fma_pair<BF16>(d[0], av.x, s);
+          s = fma_pair<BF16>(d[1], av.y, s);
+          acc[m][col] = s;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        sc_c[h][i] = sc_n[h][i];
+        zb_c[h][i] = zb_n[h][i];
+      }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    red[(warp * MT + m) * 64 + lane] = acc[m][0];
+    red[(warp * MT + m) * 64 + lane + 32] = acc[m][1];
+  }
+  __syncthreads();
+  gemv_epilogue<BF16, MT>(p, red, na, split, tid);
+}
+
 // ----------------------------------------------------------- tensor-core mode
 // The same CTA structure (one 64-column strip, one K range, eight warps
 // taking its 64-K atoms in turn, partials in warp then split order), with the
@@ -450,7 +581,25 @@ static cudaError_t launch_gemv_mma_t(const GemmArgs &a, cudaStream_t st) {
   return launch_kernel(gemv_mma_kernel<BF16, NT8>, grid, dim3(256), smem, st, a.pdl != 0, a);
 }
 
+template <bool BF16, int MT>
+static cudaError_t launch_gemv8_t(const GemmArgs &a, cudaStream_t st) {
+  const size_t smem = gemv_smem_bytes(MT, a.kb_per_split);   // at most 200 KB (checked by the caller)
+  cudaError_t e = smem_optin<gemv8_kernel<BF16, MT>>(200 * 1024);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.N / ATOM_N, a.splits);
+  return launch_kernel(gemv8_kernel<BF16, MT>, grid, dim3(256), smem, st, a.pdl != 0, a);
+}
+
 cudaError_t launch_gemv(const GemmArgs &a, bool bf16, int rows_tmpl, bool mma, cudaStream_t st) {
+  if (a.wbits == 8) {
+    switch (rows_tmpl) {
+      case 1: return bf16 ? launch_gemv8_t<true, 1>(a, st) : launch_gemv8_t<false, 1>(a, st);
+      case 2: return bf16 ? launch_gemv8_t<true, 2>(a, st) : launch_gemv8_t<false, 2>(a, st);
+      case 4: return bf16 ? launch_gemv8_t<true, 4>(a, st) : launch_gemv8_t<false, 4>(a, st);
+      case 8: return bf16 ? launch_gemv8_t<true, 8>(a, st) : launch_gemv8_t<false, 8>(a, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (mma) {
     switch (rows_tmpl) {
       case 8: return bf16 ? launch_gemv_mma_t<true, 1>(a, st) : launch_gemv_mma_t<false, 1>(a, st);

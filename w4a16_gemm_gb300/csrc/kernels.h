@@ -19,6 +19,12 @@ cudaError_t launch_pack_zeros(const void *z, uint8_t *zp, int rows, int N, int r
 cudaError_t launch_pack_scales(const uint16_t *s, uint16_t *sp, int rows, int N, int rep, cudaStream_t st);
 cudaError_t launch_dequant(const uint8_t *qw, const uint16_t *scales, const uint8_t *zeros,
                            uint16_t *out, int K, int N, int group, bool bf16, cudaStream_t st);
+// 8-bit weights (int8 codes with byte zeros, or FP8 E4M3 codes): repack of
+// u8 [K][N] codes, byte zeros, dequant-only (see pack.cu for the layout).
+cudaError_t launch_repack8(const uint8_t *q, uint8_t *qw, int K, int N, cudaStream_t st);
+cudaError_t launch_pack_zeros8(const uint8_t *z, uint8_t *zp, int rows, int N, int rep, cudaStream_t st);
+cudaError_t launch_dequant8(const uint8_t *qw, const uint16_t *scales, const uint8_t *zeros, bool fp8,
+                            uint16_t *out, int K, int N, int group, bool bf16, cudaStream_t st);
 
 // Shared arguments of the GEMM kernels.  ws/counters are the split-K
 // workspace (partials [splits][M][N] fp32 and one self-resetting arrival
@@ -33,6 +39,8 @@ struct GemmArgs {
   unsigned int *counters;
   unsigned int *err;
   int M, N, K, group;
+  int wbits;         // bits per weight code: 4, or 8 (int8 with byte zeros, or FP8)
+  int fp8;           // 8-bit codes are FP8 E4M3 (no zeros)
   int splits;
   int kb_per_split;  // 64-wide K blocks per split (a multiple of the TC stage's k-blocks)
   int act_map_3d;    // TC: the activation tensor map is 3-D (64 x M x K/64)
@@ -145,7 +153,7 @@ int tc_kblocks_per_stage(int block_m);
 // Pipeline geometry of the tcgen05 kernel for a legal block_m.
 void tc_pipeline(int block_m, int *stages, int *kbs, int *tmem_slots);
 // Whether (block_m, dq_warps) is a legal tcgen05 variant (see tc_gemm.cu).
-bool tc_variant_ok(int block_m, int dq_warps);
+bool tc_variant_ok(int block_m, int dq_warps, int wbits = 4);
 cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                       int dq_warps, cudaStream_t st);
 

@@ -155,6 +155,93 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
   }
 }
 
+// ------------------------------------------------------------ 8-bit weights
+// Packed 8-bit layout: 128-column tiles, 64-K blocks of 8192 bytes at
+// (nt * K/64 + kb) * 8192; inside a block, 16-byte chunk kq * 128 + c holds
+// the 16 consecutive K values 64 kb + 16 kq + (0..15) of column 128 nt + c.
+// One thread per chunk; a warp's threads take consecutive columns, so each
+// of the 16 rows it reads is 32 contiguous bytes.
+__global__ void __launch_bounds__(256) repack8_kernel(const uint8_t *__restrict__ q, uint8_t *__restrict__ qw,
+                                                      int K, int N) {
+  const size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= static_cast<size_t>(K) * N / 16) return;
+  const int KB = K / ATOM_K;
+  const size_t block = c >> 9;
+  const int inblk = static_cast<int>(c & 511), kq = inblk >> 7, col = inblk & 127;
+  const int nt = static_cast<int>(block / KB), kb = static_cast<int>(block % KB);
+  const int k0 = kb * ATOM_K + 16 * kq, n = nt * TILE_N + col;
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e) w[e >> 2] |= static_cast<uint32_t>(q[static_cast<size_t>(k0 + e) * N + n]) << (8 * (e & 3));
+  *reinterpret_cast<uint4 *>(qw + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 8-bit zeros [K/G][N] bytes -> tile-major [N/128][rows][128] bytes; packed
+// row g from source row g / rep.
+__global__ void pack_zeros8_kernel(const uint8_t *__restrict__ z, uint8_t *__restrict__ zp, int rows, int N,
+                                   int rep) {
+  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<size_t>(rows) * N) return;
+  const int g = static_cast<int>(i / N), n = static_cast<int>(i % N);
+  zp[(static_cast<size_t>(n >> 7) * rows + g) * TILE_N + (n & 127)] = z[static_cast<size_t>(g / rep) * N + n];
+}
+
+// Dequant-only for 8-bit weights; one thread per 16-byte chunk.
+template <bool BF16>
+__global__ void __launch_bounds__(256) dequant8_kernel(const uint8_t *__restrict__ qw,
+                                                       const uint16_t *__restrict__ scales,
+                                                       const uint8_t *__restrict__ zeros, int fp8,
+                                                       uint16_t *__restrict__ out, int K, int N, int group) {
+  const size_t c = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= static_cast<size_t>(K) * N / 16) return;
+  const int KB = K / ATOM_K, G_rows = K / group;
+  const size_t block = c >> 9;
+  const int inblk = static_cast<int>(c & 511), kq = inblk >> 7, col = inblk & 127;
+  const int nt = static_cast<int>(block / KB), kb = static_cast<int>(block % KB);
+  const int k0 = kb * ATOM_K + 16 * kq, n = nt * TILE_N + col;
+  const int g = k0 / group;
+  const uint16_t sc = scales[scale_index(g, n, G_rows)];
+  const uint32_t z = zero8_of(zeros, g, n, G_rows);
+  const uint32_t s2 = dup16(sc), zm2 = zero_magic2<false>(z);
+  const float sf = BF16 ? __uint_as_float(static_cast<uint32_t>(sc) << 16) : __half2float(__ushort_as_half(sc));
+  const uint4 v = *reinterpret_cast<const uint4 *>(qw + c * 16);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t d[2];
+    dequant_word8<BF16>(w[j], fp8 != 0, zm2, z, s2, sf, d);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const size_t k = static_cast<size_t>(k0 + 4 * j + 2 * i);
+      out[k * N + n] = static_cast<uint16_t>(d[i] & 0xFFFFu);
+      out[(k + 1) * N + n] = static_cast<uint16_t>(d[i] >> 16);
+    }
+  }
+}
+
+cudaError_t launch_repack8(const uint8_t *q, uint8_t *qw, int K, int N, cudaStream_t st) {
+  const size_t total = static_cast<size_t>(K) * N / 16;
+  repack8_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(q, qw, K, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_zeros8(const uint8_t *z, uint8_t *zp, int rows, int N, int rep, cudaStream_t st) {
+  const size_t total = static_cast<size_t>(rows) * N;
+  pack_zeros8_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(z, zp, rows, N, rep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant8(const uint8_t *qw, const uint16_t *scales, const uint8_t *zeros, bool fp8,
+                            uint16_t *out, int K, int N, int group, bool bf16, cudaStream_t st) {
+  const size_t total = static_cast<size_t>(K) * N / 16;
+  const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
+  if (bf16)
+    dequant8_kernel<true><<<blocks, 256, 0, st>>>(qw, scales, zeros, fp8 ? 1 : 0, out, K, N, group);
+  else
+    dequant8_kernel<false><<<blocks, 256, 0, st>>>(qw, scales, zeros, fp8 ? 1 : 0, out, K, N, group);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_repack(const void *q, uint8_t *qw, int K, int N, int src, unsigned int *err,
                           cudaStream_t st) {
   dim3 grid(N / ATOM_N, K / ATOM_K);

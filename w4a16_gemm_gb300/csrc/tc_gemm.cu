@@ -41,9 +41,10 @@ namespace {
 
 constexpr int BLOCK_N = 128;               // weight columns per CTA = MMA M
 constexpr int BLOCK_K = 64;                // K per k-block (one TMEM A slot)
-constexpr int W_KB_BYTES = BLOCK_N * BLOCK_K / 2;     // 4096: one tile block
+// bytes of one 64-K tile block and of one group row of zeros, for WB-bit codes
+__host__ __device__ constexpr int w_kb_bytes(int wb) { return BLOCK_N * BLOCK_K * wb / 8; }   // 4096 / 8192
+__host__ __device__ constexpr int zp_group_bytes(int wb) { return BLOCK_N * wb / 8; }          // 64 / 128
 constexpr int SC_GROUP_BYTES = BLOCK_N * 2;           // 256: one group row of scales
-constexpr int ZP_GROUP_BYTES = BLOCK_N / 2;           // 64: one group row of zeros
 constexpr int TMEM_A_COLS = BLOCK_K / 2;   // 32 columns of packed pairs per k-block
 
 // k-blocks per shared-memory stage: small tiles move more weight per stage so
@@ -53,14 +54,15 @@ __host__ __device__ constexpr int kbs_for(int block_m) {
   return block_m <= 16 ? 4 : block_m <= 64 ? 2 : 1;
 }
 __host__ __device__ constexpr int a_kb_bytes(int block_m) { return block_m * BLOCK_K * 2; }
-__host__ __device__ constexpr int stage_bytes(int block_m) {
+__host__ __device__ constexpr int stage_bytes(int block_m, int wb = 4) {
   // (room for two groups per 64-K block: G = 32)
-  return kbs_for(block_m) * (a_kb_bytes(block_m) + W_KB_BYTES + 2 * SC_GROUP_BYTES + 2 * ZP_GROUP_BYTES);
+  return kbs_for(block_m) * (a_kb_bytes(block_m) + w_kb_bytes(wb) + 2 * SC_GROUP_BYTES + 2 * zp_group_bytes(wb));
 }
 // A copy takes ~1500 cycles to land under prefill load, so the ring must be
 // deep enough to cover it: 256-row tiles take the six stages that fit.
-__host__ __device__ constexpr int stages_for(int block_m) {
-  return block_m <= 64 ? 4 : block_m <= 128 ? 8 : 6;
+__host__ __device__ constexpr int stages_for(int block_m, int wb = 4) {
+  // (8-bit codes double the weight bytes of a stage: four stages at 256 rows)
+  return block_m <= 64 ? 4 : block_m <= 128 ? 8 : wb == 4 ? 6 : 4;
 }
 // TMEM: D occupies columns [0, max(32, BLOCK_M)); the rest of a 256-column
 // (BLOCK_M <= 128) or 512-column allocation is a ring of k-block A slots.
@@ -82,13 +84,13 @@ __host__ __device__ constexpr int tmem_a_stages(int block_m) {
 //                           MMAs two uses back retired; MMAs retire in order)
 // A randomized model of this protocol (tests/test_pipeline_protocol.py)
 // checks both conditions.
-__host__ __device__ constexpr bool variant_ok(int block_m, int dq_wg) {
-  return stages_for(block_m) % dq_wg == 0 &&
+__host__ __device__ constexpr bool variant_ok(int block_m, int dq_wg, int wb = 4) {
+  return stages_for(block_m, wb) % dq_wg == 0 &&
          tmem_a_stages(block_m) >= (dq_wg - 1) * kbs_for(block_m) + 1;
 }
-__host__ __device__ constexpr size_t smem_bytes_for(int block_m) {
+__host__ __device__ constexpr size_t smem_bytes_for(int block_m, int wb = 4) {
   return 1024 /* alignment slack */ +
-         static_cast<size_t>(stages_for(block_m)) * stage_bytes(block_m) +
+         static_cast<size_t>(stages_for(block_m, wb)) * stage_bytes(block_m, wb) +
          512 /* barriers and flags */;
 }
 
@@ -97,10 +99,15 @@ __host__ __device__ constexpr size_t smem_bytes_for(int block_m) {
 
 // DQ_WG dequant warpgroups; warpgroup g dequantizes the shared-memory stages
 // j with j % DQ_WG == g, so DQ_WG stages are in flight in the ALUs at once.
-template <bool BF16, int BLOCK_M, int DQ_WG>
+// WB: bits per weight code, 4, or 8 (int8 with byte zeros, or FP8 E4M3 codes,
+// GemmArgs::fp8); an 8-bit tile block is 16-byte chunks of 16 consecutive K
+// of one column, chunk kq * 128 + c.
+template <bool BF16, int BLOCK_M, int DQ_WG, int WB>
 __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
-  constexpr int STAGES = stages_for(BLOCK_M);
+  constexpr int STAGES = stages_for(BLOCK_M, WB);
+  constexpr int W_KB_BYTES = w_kb_bytes(WB);
+  constexpr int ZP_GROUP_BYTES = zp_group_bytes(WB);
   constexpr int KBS = kbs_for(BLOCK_M);
   constexpr int A_KB = a_kb_bytes(BLOCK_M);
   constexpr int A_STAGE = KBS * A_KB;
@@ -114,7 +121,8 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
   static_assert(BLOCK_M % 16 == 0 && BLOCK_M >= 16 && BLOCK_M <= 256, "MMA N");
   static_assert(DQ_WG == 1 || DQ_WG == 2 || DQ_WG == 4, "dequant warpgroups");
   static_assert(TS >= 2, "TMEM A slots");
-  static_assert(variant_ok(BLOCK_M, DQ_WG), "parity waits need at most one phase of lead");
+  static_assert(variant_ok(BLOCK_M, DQ_WG, WB), "parity waits need at most one phase of lead");
+  static_assert(WB == 4 || WB == 8, "code width");
   static_assert(A_KB % 1024 == 0, "swizzle atoms");
 
   extern __shared__ uint8_t smem_raw[];
@@ -278,7 +286,9 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
     const int r = quarter * 32 + lane;        // weight column within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int atom = r >> 6, nl = r & 63;
-    const uint8_t *wsrc = sW + atom * ATOM_BYTES + nl * 16;
+    // this thread's codes in a stage: 4-bit, two chunks (K 0-31, 32-63) of
+    // its column in its atom; 8-bit, four chunks 2048 bytes apart
+    const uint8_t *wsrc = WB == 4 ? sW + atom * ATOM_BYTES + nl * 16 : sW + r * 16;
     bool ok = true;
     for (int j = wg; j < nstages && ok; j += DQ_WG) {
       const int s = j % STAGES;
@@ -304,51 +314,84 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         tc_fence_after();
         if (quarter == 2 && lane == 0) TMW4_STAMP(2, i);
         const int gi = ((kbf + b) * BLOCK_K) / p.group - gf;
-        const uint16_t sc =
-            reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + gi * SC_GROUP_BYTES)[r];
-        const uint32_t z =
-            p.zeros != nullptr
-                ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + gi * ZP_GROUP_BYTES + (r >> 1)]) >>
-                   ((r & 1) * 4)) & 0xFu
-                : 8u;
-        const uint8_t *src = wsrc + s * W_STAGE + b * W_KB_BYTES;
-        const uint4 v0 = *reinterpret_cast<const uint4 *>(src);
-        const uint4 v1 = *reinterpret_cast<const uint4 *>(src + 1024);
-#ifdef TMW4_TRACE
-        if (p.trace != nullptr && quarter == 2 && lane == 0 && ((v0.x ^ v1.y) == 0x9E3779B9u)) p.trace[8 * 256] = 1;
-        if (quarter == 2 && lane == 0) TMW4_STAMP(8, i);
-#endif
-        if (b == nb - 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty_bar + s);   // last read of this stage done
-        }
-        const uint32_t s2 = dup16(sc), zm2 = zero_magic2<BF16>(z);
-        // the block's second 32-K half has a group of its own only when G = 32
-        uint32_t s2b = s2, zm2b = zm2;
-        if (p.group == 32) {
-          const uint16_t sc1 =
-              reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + (gi + 1) * SC_GROUP_BYTES)[r];
-          const uint32_t z1 =
+        uint32_t d0[16], d1[16];
+        if constexpr (WB == 8) {
+          // 8-bit: scales and byte zeros of the block's two 32-K halves
+          const uint8_t *src = wsrc + s * W_STAGE + b * W_KB_BYTES;
+          uint4 v[4];
+#pragma unroll
+          for (int kq = 0; kq < 4; ++kq) v[kq] = *reinterpret_cast<const uint4 *>(src + kq * 2048);
+          if (b == nb - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar + s);   // last read of this stage done
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int gh = p.group == 32 ? gi + h : gi;
+            const uint16_t sc = reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + gh * SC_GROUP_BYTES)[r];
+            const uint32_t z = p.zeros != nullptr ? sZP[s * ZP_STAGE + gh * ZP_GROUP_BYTES + r] : 128u;
+            const uint32_t s2 = dup16(sc), zm2 = zero_magic2<false>(z);
+            const float sf = BF16 ? __uint_as_float(static_cast<uint32_t>(sc) << 16) : __half2float(__ushort_as_half(sc));
+            uint32_t *d = h == 0 ? d0 : d1;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint4 vv = v[2 * h + kk];
+              const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t o[2];
+                dequant_word8<BF16>(w[j], p.fp8 != 0, zm2, z, s2, sf, o);
+                d[8 * kk + 2 * j] = o[0];
+                d[8 * kk + 2 * j + 1] = o[1];
+              }
+            }
+          }
+        } else {
+          const uint16_t sc =
+              reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + gi * SC_GROUP_BYTES)[r];
+          const uint32_t z =
               p.zeros != nullptr
-                  ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + (gi + 1) * ZP_GROUP_BYTES + (r >> 1)]) >>
+                  ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + gi * ZP_GROUP_BYTES + (r >> 1)]) >>
                      ((r & 1) * 4)) & 0xFu
                   : 8u;
-          s2b = dup16(sc1);
-          zm2b = zero_magic2<BF16>(z1);
-        }
-        uint32_t d0[16], d1[16];
-        {
-          const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-          const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+          const uint8_t *src = wsrc + s * W_STAGE + b * W_KB_BYTES;
+          const uint4 v0 = *reinterpret_cast<const uint4 *>(src);
+          const uint4 v1 = *reinterpret_cast<const uint4 *>(src + 1024);
+#ifdef TMW4_TRACE
+          if (p.trace != nullptr && quarter == 2 && lane == 0 && ((v0.x ^ v1.y) == 0x9E3779B9u)) p.trace[8 * 256] = 1;
+          if (quarter == 2 && lane == 0) TMW4_STAMP(8, i);
+#endif
+          if (b == nb - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar + s);   // last read of this stage done
+          }
+          const uint32_t s2 = dup16(sc), zm2 = zero_magic2<BF16>(z);
+          // the block's second 32-K half has a group of its own only when G = 32
+          uint32_t s2b = s2, zm2b = zm2;
+          if (p.group == 32) {
+            const uint16_t sc1 =
+                reinterpret_cast<const uint16_t *>(sSC + s * SC_STAGE + (gi + 1) * SC_GROUP_BYTES)[r];
+            const uint32_t z1 =
+                p.zeros != nullptr
+                    ? (static_cast<uint32_t>(sZP[s * ZP_STAGE + (gi + 1) * ZP_GROUP_BYTES + (r >> 1)]) >>
+                       ((r & 1) * 4)) & 0xFu
+                    : 8u;
+            s2b = dup16(sc1);
+            zm2b = zero_magic2<BF16>(z1);
+          }
+          {
+            const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+            const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t o[4];
-            dequant_word<BF16>(w0[q4], zm2, s2, o);
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t o[4];
+              dequant_word<BF16>(w0[q4], zm2, s2, o);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) d0[4 * q4 + q] = o[q];
-            dequant_word<BF16>(w1[q4], zm2b, s2b, o);
+              for (int q = 0; q < 4; ++q) d0[4 * q4 + q] = o[q];
+              dequant_word<BF16>(w1[q4], zm2b, s2b, o);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) d1[4 * q4 + q] = o[q];
+              for (int q = 0; q < 4; ++q) d1[4 * q4 + q] = o[q];
+            }
           }
         }
 #ifdef TMW4_TRACE
@@ -411,52 +454,56 @@ void tc_pipeline(int block_m, int *stages, int *kbs, int *tmem_slots) {
   *kbs = kbs_for(block_m);
   *tmem_slots = tmem_a_stages(block_m);
 }
-bool tc_variant_ok(int block_m, int dq_warps) {
-  return (dq_warps == 4 || dq_warps == 8 || dq_warps == 16) && variant_ok(block_m, dq_warps / 4);
+bool tc_variant_ok(int block_m, int dq_warps, int wbits) {
+  return (dq_warps == 4 || dq_warps == 8 || dq_warps == 16) &&
+         (wbits == 8 ? variant_ok(block_m, dq_warps / 4, 8) : variant_ok(block_m, dq_warps / 4, 4));
 }
 
-template <bool BF16, int BLOCK_M, int DQ_WG>
+template <bool BF16, int BLOCK_M, int DQ_WG, int WB>
 static cudaError_t launch_tc_t(const GemmArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
-  auto kern = tc_gemm_kernel<BF16, BLOCK_M, DQ_WG>;
-  const size_t smem = smem_bytes_for(BLOCK_M);
-  cudaError_t e = smem_optin<tc_gemm_kernel<BF16, BLOCK_M, DQ_WG>>(static_cast<int>(smem));
+  auto kern = tc_gemm_kernel<BF16, BLOCK_M, DQ_WG, WB>;
+  const size_t smem = smem_bytes_for(BLOCK_M, WB);
+  cudaError_t e = smem_optin<tc_gemm_kernel<BF16, BLOCK_M, DQ_WG, WB>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(a.N / BLOCK_N, (a.M + BLOCK_M - 1) / BLOCK_M, a.splits);
   return launch_kernel(kern, grid, dim3(64 + 128 * DQ_WG), smem, st, a.pdl != 0, tmap, a);
 }
 
-template <bool BF16, int BLOCK_M>
+template <bool BF16, int BLOCK_M, int WB>
 static cudaError_t launch_tc_bm(const GemmArgs &a, const CUtensorMap &tmap, int dq_warps,
                                 cudaStream_t st) {
   switch (dq_warps) {
-    case 4: return launch_tc_t<BF16, BLOCK_M, 1>(a, tmap, st);
+    case 4: return launch_tc_t<BF16, BLOCK_M, 1, WB>(a, tmap, st);
     case 8:
-      if constexpr (variant_ok(BLOCK_M, 2)) return launch_tc_t<BF16, BLOCK_M, 2>(a, tmap, st);
+      if constexpr (variant_ok(BLOCK_M, 2, WB)) return launch_tc_t<BF16, BLOCK_M, 2, WB>(a, tmap, st);
       return cudaErrorInvalidValue;
     case 16:
-      if constexpr (variant_ok(BLOCK_M, 4)) return launch_tc_t<BF16, BLOCK_M, 4>(a, tmap, st);
+      if constexpr (variant_ok(BLOCK_M, 4, WB)) return launch_tc_t<BF16, BLOCK_M, 4, WB>(a, tmap, st);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <bool BF16>
+template <bool BF16, int WB>
 static cudaError_t launch_tc_dtype(const GemmArgs &a, const CUtensorMap &tmap, int block_m,
                                    int dq, cudaStream_t st) {
   switch (block_m) {
-    case 16: return launch_tc_bm<BF16, 16>(a, tmap, dq, st);
-    case 32: return launch_tc_bm<BF16, 32>(a, tmap, dq, st);
-    case 64: return launch_tc_bm<BF16, 64>(a, tmap, dq, st);
-    case 128: return launch_tc_bm<BF16, 128>(a, tmap, dq, st);
-    case 256: return launch_tc_bm<BF16, 256>(a, tmap, dq, st);
+    case 16: return launch_tc_bm<BF16, 16, WB>(a, tmap, dq, st);
+    case 32: return launch_tc_bm<BF16, 32, WB>(a, tmap, dq, st);
+    case 64: return launch_tc_bm<BF16, 64, WB>(a, tmap, dq, st);
+    case 128: return launch_tc_bm<BF16, 128, WB>(a, tmap, dq, st);
+    case 256: return launch_tc_bm<BF16, 256, WB>(a, tmap, dq, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_tc(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int block_m,
                       int dq_warps, cudaStream_t st) {
-  return bf16 ? launch_tc_dtype<true>(a, tmap_a, block_m, dq_warps, st)
-              : launch_tc_dtype<false>(a, tmap_a, block_m, dq_warps, st);
+  if (a.wbits == 8)
+    return bf16 ? launch_tc_dtype<true, 8>(a, tmap_a, block_m, dq_warps, st)
+                : launch_tc_dtype<false, 8>(a, tmap_a, block_m, dq_warps, st);
+  return bf16 ? launch_tc_dtype<true, 4>(a, tmap_a, block_m, dq_warps, st)
+              : launch_tc_dtype<false, 4>(a, tmap_a, block_m, dq_warps, st);
 }
 
 // ------------------------------------------------------ bounded-wait self test
