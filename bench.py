@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--reps", type=int, default=6, help="with --case: launches")
     ap.add_argument("--configs", type=str, default=",".join(CONFIG_WORKLOADS),
                     help="workloads of the per-problem block ('' to skip it)")
+    ap.add_argument("--formats", type=str, default="int8,fp8,w4_g32",
+                    help="non-default weight formats to time beside the configs ('' skips)")
     ap.add_argument("--config-cpu-seconds", type=float, default=1.0,
                     help="CPU time of the oracle sample per shape in the per-config block")
     return ap.parse_args()
@@ -251,14 +253,18 @@ def graph_time(launch, stream, launches: int, repeats: int) -> list[float]:
     return out
 
 
-def variant_name(v: dict, dtype: str = "f16") -> str:
+def variant_name(v: dict, dtype: str = "f16", wbits: int = 4) -> str:
     if v["kernel"] == "gemv":
+        if wbits == 8:
+            return f"gemv8_kernel<{dtype},{v['block_m']}>"
+        if v["dq_warps"] == 1:
+            return f"gemv_mma_kernel<{dtype},{v['block_m'] // 8}>"
         return f"gemv_kernel<{dtype},{v['block_m']}>"
     if v["kernel"] == "decode_mma":
         return f"decode_mma_kernel<{dtype},{v['block_m'] // 8}>"
     if v["kernel"] == "tc_decode":
         return f"tc_decode_kernel<{dtype},{v['block_m']},{v['dq_warps']}>"
-    return f"tc_gemm_kernel<{dtype},{v['block_m']},{v['dq_warps']}>"
+    return f"tc_gemm_kernel<{dtype},{v['block_m']},{v['dq_warps']}{',8' if wbits == 8 else ''}>"
 
 
 def oracle_problem_seconds(qw, a_bits, M: int, budget_s: float) -> tuple[float, str]:
@@ -357,6 +363,97 @@ def config_sweep(wl_name: str, dev, stream, peaks: dict, tune: bool, cpu_budget_
             "sample": ("extrapolated: " if extrap else "") +
                       "per problem, numpy dequant (RNE) of a column sample over all K and a float64 "
                       "matmul of a row sample, scaled linearly to the full problem"}
+    return out
+
+
+FORMAT_SHAPES = ((4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096))
+FORMAT_DECODE_MS = (1, 16)
+FORMAT_PREFILL = (4096, 4096, 2048)     # K, N, M (bf16)
+
+
+def format_weight_bytes(fmt: str, K: int, N: int) -> float:
+    """Algorithmic weight bytes of the non-default formats (group 128 unless
+    named): int8 = 8-bit code + 16-bit scale + 8-bit zero per group; fp8 =
+    8-bit code + 16-bit scale; w4_g32 = 4-bit code + 16-bit scale + 4-bit zero
+    per group of 32."""
+    if fmt == "int8":
+        return K * N * (1.0 + 3.0 / 128)
+    if fmt == "fp8":
+        return K * N * (1.0 + 2.0 / 128)
+    return K * N * (0.5 + 2.5 / 32)
+
+
+def _format_weight(fmt: str, K: int, N: int, dt, dev, gen):
+    """A seeded random weight of the format: uniform codes (FP8 codes with the
+    two NaN patterns replaced by 1.0), scales of either sign in [2e-4, 2e-3],
+    uniform zeros."""
+    import torch
+
+    from w4a16_gemm_gb300 import binding
+
+    G = 32 if fmt == "w4_g32" else 128
+    hi = 16 if fmt == "w4_g32" else 256
+    q = torch.randint(0, hi, (K, N), dtype=torch.uint8, device=dev, generator=gen)
+    s = torch.rand((K // G, N), device=dev, generator=gen) * 1.8e-3 + 2e-4
+    s = (s * (torch.randint(0, 2, s.shape, device=dev, generator=gen) * 2 - 1)).to(dt)
+    if fmt == "fp8":
+        q[(q == 0x7F) | (q == 0xFF)] = 0x38
+        return binding.pack_fp8(q, s, G)
+    z = torch.randint(0, hi, (K // G, N), dtype=torch.uint8, device=dev, generator=gen)
+    if fmt == "int8":
+        return binding.pack_w8(q, s, z, G)
+    return binding.pack(q, s, z, G)
+
+
+def formats_sweep(fmts: list, dev, stream, peaks: dict, tune: bool) -> dict:
+    """Times the non-default weight formats the way the configs are timed (graph
+    of GRAPH_LAUNCHES launches over rotated weight copies): the decode shapes at
+    M in FORMAT_DECODE_MS (fp16) and one prefill problem (bf16)."""
+    import math
+
+    import torch
+
+    from w4a16_gemm_gb300 import binding
+
+    L2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    gen = torch.Generator(device=dev)
+    out = {}
+    for fmt in fmts:
+        cases = [(K, N, FORMAT_DECODE_MS, torch.float16, "f16") for K, N in FORMAT_SHAPES]
+        cases.append((FORMAT_PREFILL[0], FORMAT_PREFILL[1], (FORMAT_PREFILL[2],), torch.bfloat16, "bf16"))
+        problems = []
+        for K, N, ms, dt, dname in cases:
+            gen.manual_seed(1000 + K * 7 + N)
+            wb = format_weight_bytes(fmt, K, N)
+            R = min(64, math.ceil(3 * L2 / wb) + 1)
+            Ws = [_format_weight(fmt, K, N, dt, dev, gen) for _ in range(R)]
+            if tune:
+                binding.tune(Ws[0], list(ms))
+            for M in ms:
+                A = torch.randn((M, K), device=dev, generator=gen).to(dt)
+                C = torch.empty((M, N), dtype=dt, device=dev)
+                v = binding.select(Ws[0], M)
+                ts = graph_time(lambda i: binding.gemm(A, Ws[i % R], out=C, stream=stream), stream,
+                                GRAPH_LAUNCHES, GRAPH_REPEATS)
+                binding.poll_error(stream)
+                t = statistics.median(ts)
+                t_hbm = (wb + 2.0 * M * K + 2.0 * M * N) / (peaks["hbm_gbs"] * 1e9)
+                t_tc = 2.0 * M * N * K / (peaks["bf16_tflops"] * 1e12)
+                problems.append({"K": K, "N": N, "M": M, "dtype": dname, "variant": v,
+                                 "kernel": variant_name(v, dname, 4 if fmt == "w4_g32" else 8), "us": round(t * 1e6, 3),
+                                 "us_min": round(min(ts) * 1e6, 3),
+                                 "tflops": round(2.0 * M * N * K / t / 1e12, 2),
+                                 "weight_gbs": round(wb / t / 1e9, 1),
+                                 "bound": "hbm" if M <= 16 else "tensor",
+                                 "frac": round(max(t_hbm, t_tc) / t, 4)})
+                del A, C
+            for w in Ws:
+                w.free()
+            del Ws
+            torch.cuda.synchronize()
+        out[fmt] = {"problems": problems,
+                    "weight_bytes": {"int8": "K*N*(1 + 3/128)", "fp8": "K*N*(1 + 2/128)",
+                                     "w4_g32": "K*N*(1/2 + 2.5/32)"}[fmt]}
     return out
 
 
@@ -509,6 +606,11 @@ def run_ours(args, rank: int, world: int):
         configs[name] = config_sweep(name, dev, stream, peaks, tune=not args.no_tune,
                                      cpu_budget_s=args.config_cpu_seconds if rank == 0 else 0.0)
 
+    formats = None
+    fmts = [x for x in args.formats.split(",") if x]
+    if fmts:
+        formats = formats_sweep(fmts, dev, stream, peaks, tune=not args.no_tune)
+
     # roofline of the dominant kernel of the headline step: the variant with the
     # most time per step, from the per-problem graph timings of the decode sweep
     roof = None
@@ -564,6 +666,7 @@ def run_ours(args, rank: int, world: int):
                  "unit": "us", "note": "offline repack (tm_pack_w4), timed once per shape"},
         "variants": {f"{shapes[si][0]}x{shapes[si][1]}xM{M}": variants[(si, M)] for si, M in problems},
         "configs": configs,
+        "formats": formats,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "tensor_tflops": peaks["bf16_tflops"], "source": peak_src},
     }
     return line

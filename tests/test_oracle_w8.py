@@ -1,10 +1,14 @@
 """Pins of the 8-bit weight oracle (oracle/w8.py)."""
 
+from fractions import Fraction
+
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from oracle import w8
+from tests.test_oracle_casts import round_exact
 
 
 def test_e4m3_against_torch_and_by_hand():
@@ -75,3 +79,65 @@ def test_pack_zeros8():
     z = np.arange(3 * 256, dtype=np.uint32).reshape(3, 256).astype(np.uint8)
     zp = w8.pack_zeros8_ref(z)
     assert zp[(1 * 3 + 2) * 128 + 5] == z[2, 128 + 5]
+
+
+def _e4m3_by_hand(c: int):
+    """E4M3 from its bit layout: 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+    exponent 0 is subnormal; S.1111.111 is NaN; no infinities."""
+    sign = -1 if c & 0x80 else 1
+    e, m = (c >> 3) & 0xF, c & 0x7
+    if e == 0xF and m == 0x7:
+        return None
+    if e == 0:
+        return sign * Fraction(m, 8) * Fraction(1, 2 ** 6)
+    return sign * (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+
+
+def _scales(fmt, n, seed):
+    rng = np.random.default_rng(seed)
+    hi = 0x7C00 if fmt == "f16" else 0x7F80
+    bits = rng.integers(0, hi, size=n).astype(np.uint16)
+    sign = rng.integers(0, 2, size=n).astype(np.uint16) << 15
+    return bits | sign
+
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+def test_int8_every_difference_vs_rational(fmt):
+    """Every q - z in [-255, 255] (each from a random valid (q, z)) times a
+    spread of scales, subnormal to large, either sign, against the exactly
+    rounded rational product."""
+    rng = np.random.default_rng(21)
+    d = np.arange(-255, 256)
+    z = np.array([rng.integers(max(0, -x), min(255, 255 - x) + 1) for x in d], dtype=np.int64)
+    q = (z + d).astype(np.uint8)
+    z = z.astype(np.uint8)
+    scales = _scales(fmt, 40, 22 if fmt == "f16" else 23)
+    S = scales.size
+    Q = np.repeat(q[:, None], S, axis=1)
+    Z = np.repeat(z[:, None], S, axis=1)              # group = 1: one zero per row
+    Sc = np.repeat(scales[None, :], d.size, axis=0)
+    with np.errstate(over="ignore"):
+        got = oracle.act_bits_to_f64(w8.dequant8_bits(Q, Sc, Z, 1, fmt), fmt)
+    sval = oracle.act_bits_to_f64(scales, fmt)
+    for i, dd in enumerate(d):
+        want = [round_exact(Fraction(float(sv)) * int(dd), fmt) for sv in sval]
+        assert np.array_equal(got[i], np.array(want)), dd
+
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+def test_fp8_every_code_vs_rational(fmt):
+    codes = np.array([c for c in range(256) if _e4m3_by_hand(c) is not None], dtype=np.uint8)
+    assert codes.size == 254
+    hand = w8.e4m3_to_f64(codes)
+    assert [Fraction(float(x)) for x in hand] == [_e4m3_by_hand(int(c)) for c in codes]
+    scales = _scales(fmt, 24, 24 if fmt == "f16" else 25)
+    S = scales.size
+    Q = np.repeat(codes[:, None], S, axis=1)
+    Sc = np.repeat(scales[None, :], codes.size, axis=0)
+    with np.errstate(over="ignore"):
+        got = oracle.act_bits_to_f64(w8.dequant8_bits(Q, Sc, None, 1, fmt, fp8=True), fmt)
+    sval = oracle.act_bits_to_f64(scales, fmt)
+    for i, c in enumerate(codes):
+        v = _e4m3_by_hand(int(c))
+        want = [round_exact(Fraction(float(sv)) * v, fmt) for sv in sval]
+        assert np.array_equal(got[i], np.array(want)), hex(c)
