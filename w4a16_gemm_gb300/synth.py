@@ -226,3 +226,96 @@ def random_problem(seed: int, M: int, K: int, N: int, group: int = 128, dtype: s
     qw = quantize_rtn(w, group, dtype, symmetric)
     a = _draw_acts(rng, M, K, act_dist, dtype)
     return qw, a
+
+
+# ------------------------------------------------------------ decode attention
+@dataclass
+class KVProblem:
+    """One decode-attention step over a low-bit KV cache (layouts as the
+    library takes them): q [B, Hq, D] 16-bit patterns; codes [B, Hkv, L_max,
+    D * bits / 8] bytes (4 bits: two elements per byte, low nibble first);
+    scales [B, Hkv, L_max] 16-bit patterns; zeros [B, Hkv, L_max] bytes;
+    lens [B] int32."""
+    q: np.ndarray
+    k_codes: np.ndarray
+    k_scale: np.ndarray
+    k_zero: np.ndarray
+    v_codes: np.ndarray
+    v_scale: np.ndarray
+    v_zero: np.ndarray
+    lens: np.ndarray
+    bits: int
+    dtype: str
+    sm_scale: float
+
+    @property
+    def B(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def Hq(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def D(self) -> int:
+        return self.q.shape[2]
+
+    @property
+    def Hkv(self) -> int:
+        return self.k_codes.shape[1]
+
+    @property
+    def L_max(self) -> int:
+        return self.k_codes.shape[2]
+
+
+def kv_problem(seed: int, B: int, Hq: int, Hkv: int, D: int, lens, L_max: int | None = None,
+               bits: int = 8, dtype: str = "f16") -> KVProblem:
+    """Seeded synthetic cache: N(0, 1) queries; uniform codes (4 bits: uniform
+    bytes, i.e. two uniform nibbles) and zeros; per-token scales uniform in
+    [0.004, 0.012] (8 bits) or [0.06, 0.2] (4 bits), so that K and V values
+    span about +-2; sm_scale = 1 / sqrt(D)."""
+    lens = np.asarray(lens, dtype=np.int32)
+    if L_max is None:
+        L_max = max(64, int(-(-int(lens.max(initial=0)) // 64) * 64))
+    rng = np.random.default_rng(np.random.SeedSequence([7000 + seed, B, Hq, Hkv, D, L_max, bits]))
+    q = to_16bit(rng.standard_normal((B, Hq, D), dtype=np.float32), dtype)
+    width = D if bits == 8 else D // 2
+    zhi = 256 if bits == 8 else 16
+    lo, hi = (0.004, 0.012) if bits == 8 else (0.06, 0.2)
+
+    def side():
+        codes = rng.integers(0, 256, size=(B, Hkv, L_max, width), dtype=np.uint8)
+        scale = to_16bit(rng.uniform(lo, hi, size=(B, Hkv, L_max)).astype(np.float32), dtype)
+        zero = rng.integers(0, zhi, size=(B, Hkv, L_max), dtype=np.uint8)
+        return codes, scale, zero
+
+    kc, ks, kz = side()
+    vc, vs, vz = side()
+    return KVProblem(q, kc, ks, kz, vc, vs, vz, lens, bits, dtype, float(1.0 / np.sqrt(D)))
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Decode attention at an 8B-class head layout (32 query heads, 8 KV heads,
+    head dim 128) for a list of (batch, context-length range) cases; lengths
+    are drawn uniformly from the range per sequence."""
+    bits: int
+    dtype: str = "f16"
+    Hq: int = 32
+    Hkv: int = 8
+    D: int = 128
+    cases: tuple = ((1, (8192, 8192)), (16, (1024, 8192)), (64, (512, 4096)), (256, (256, 2048)))
+
+
+ATTN_WORKLOADS = {
+    "attn_8b_kv8": AttnWorkload(bits=8),
+    "attn_8b_kv4": AttnWorkload(bits=4),
+}
+
+
+def attn_lens(name: str, case_idx: int) -> np.ndarray:
+    wl = ATTN_WORKLOADS[name]
+    B, (lo, hi) = wl.cases[case_idx]
+    rng = np.random.default_rng(np.random.SeedSequence([7100, wl.bits, case_idx]))
+    return rng.integers(lo, hi + 1, size=B).astype(np.int32)
