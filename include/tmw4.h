@@ -322,6 +322,50 @@ tm_status tm_tc_decode_pipeline(int block_m, int dq_warps, int *weight_stages,
 tm_status tm_decode_plan(int M, int N, int K, int block_m, int sm_count, int *grid,
                          long long *tiles, int *partial_slots);
 
+/* Decode attention over a low-bit KV cache: one query token per sequence
+ * against its cached keys and values (TurboMind paper, pith.science review,
+ * Figure 4: the attention pipeline dequantizes the low-bit cache by
+ * integer-to-float conversion and scaling, then computes Q K^T and P V;
+ * Figure 10: the cache is consumed in 64-token tiles).  For sequence b and
+ * query head hq, with KV head h = hq / (Hq / Hkv) and t < lens[b]:
+ *   K[t][d] = T(k_scale[t] * (kq[t][d] - k_zero[t])), V likewise
+ *   O[b][hq] = sum_t softmax_t(sm_scale * Q[b][hq] . K[t]) V[t]
+ * (per-token, per-KV-head scale and integer zero; one round-to-nearest-even
+ * per cached element, as for the weights).  A sequence with lens[b] == 0
+ * gets O = 0.
+ *   q        device, [B][Hq][128] of dtype
+ *   k_cache, v_cache  device, [B][Hkv][L_max][128 * kv_bits / 8] bytes;
+ *            8 bits: one code 0..255 per byte; 4 bits: element d in byte
+ *            d / 2, the low nibble holding even d
+ *   k_scale, v_scale  device, [B][Hkv][L_max] of dtype
+ *   k_zero, v_zero    device, [B][Hkv][L_max] bytes (codes; <= 15 for 4 bits)
+ *   lens     device, [B] int32 (values outside [0, L_max] are clamped)
+ *   o        device, [B][Hq][128] of dtype, written
+ *   head_dim must be 128; Hq a multiple of Hkv with at most 16 query heads
+ *   per KV head; L_max a positive multiple of 64; B * Hkv * L_max < 2^31;
+ *   every pointer 16-byte aligned.  Cache rows at t >= lens[b] are never
+ *   used (they may hold anything, NaN scales included).
+ *   chunk_tiles: 64-token tiles per unit of work (0 = chosen from the
+ *   shapes; tm_attn_decode_plan reports the choice).  Sequences longer
+ *   than one unit are split over CTAs and merged through a library-owned
+ *   per-(device, stream) workspace (grown outside stream capture, like the
+ *   GEMM's split-K scratch).
+ * The caller owns every buffer.  Stream-ordered on `stream`, launched with
+ * programmatic dependent launch like the GEMMs (every read of the inputs
+ * waits for the previous kernel).  Device-side conditions (a bounded wait
+ * that gave up) are reported by tm_poll_error.  TM_ERR_INVALID_ARG /
+ * TM_ERR_UNSUPPORTED for arguments outside the above. */
+tm_status tm_attn_decode(const void *q, const uint8_t *k_cache, const void *k_scale, const uint8_t *k_zero,
+                         const uint8_t *v_cache, const void *v_scale, const uint8_t *v_zero, const int32_t *lens,
+                         void *o, int B, int Hq, int Hkv, int head_dim, int L_max, int kv_bits, tm_dtype dtype,
+                         float sm_scale, int chunk_tiles, void *stream);
+
+/* The automatic chunk_tiles of tm_attn_decode and its grid (CTAs) for the
+ * shape on the current device, host-side (planned for every sequence at
+ * L_max).  TM_ERR_INVALID_ARG for shapes tm_attn_decode refuses. */
+tm_status tm_attn_decode_plan(int B, int Hq, int Hkv, int L_max, int kv_bits, tm_dtype dtype, int *chunk_tiles,
+                              int *grid);
+
 /* Loads/saves the tuned table (JSON lines) from/to a host path. */
 tm_status tm_tune_load(const char *path);
 tm_status tm_tune_save(const char *path);

@@ -76,6 +76,8 @@ SIGNATURES = [
     ("tm_tc_decode_pipeline", _I, [_I, _I] + [ctypes.POINTER(_I)] * 4),
     ("tm_decode_plan", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_LL),
                             ctypes.POINTER(_I)]),
+    ("tm_attn_decode", _I, [_VP] * 9 + [_I] * 7 + [ctypes.c_float, _I, _VP]),
+    ("tm_attn_decode_plan", _I, [_I] * 6 + [ctypes.POINTER(_I)] * 2),
     ("tm_last_error", ctypes.c_char_p, []),
     ("tm_version", ctypes.c_char_p, []),
 ]
@@ -360,6 +362,45 @@ def decode_plan(M: int, N: int, K: int, block_m: int, sm_count: int) -> dict:
     _check(lib().tm_decode_plan(int(M), int(N), int(K), int(block_m), int(sm_count),
                                 ctypes.byref(g), ctypes.byref(t), ctypes.byref(p)))
     return {"grid": g.value, "tiles": t.value, "partial_slots": p.value}
+
+
+def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, k_scale: torch.Tensor, k_zero: torch.Tensor,
+                v_cache: torch.Tensor, v_scale: torch.Tensor, v_zero: torch.Tensor, lens: torch.Tensor,
+                kv_bits: int, sm_scale: float, out: torch.Tensor | None = None, chunk_tiles: int = 0,
+                stream=None) -> torch.Tensor:
+    """tm_attn_decode: q [B, Hq, 128]; caches [B, Hkv, L_max, 128 * kv_bits / 8] uint8; scales
+    [B, Hkv, L_max] of q's dtype; zeros [B, Hkv, L_max] uint8; lens [B] int32 (device)."""
+    if q.dim() != 3 or q.dtype not in _DT or not q.is_cuda:
+        raise ValueError("q must be a 3-D float16/bfloat16 CUDA tensor")
+    B, Hq, D = q.shape
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must be 4-D and of the same shape")
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    for t in (k_cache, v_cache, k_zero, v_zero):
+        if t.dtype != torch.uint8:
+            raise ValueError("caches and zeros must be uint8")
+    for t in (k_scale, v_scale):
+        if t.dtype != q.dtype:
+            raise ValueError("scales must have q's dtype")
+    if lens.dtype != torch.int32:
+        raise ValueError("lens must be int32")
+    q = q.contiguous()
+    if out is None:
+        out = torch.empty_like(q)
+    st = _stream(stream)
+    with torch.cuda.device(q.device):
+        _check(lib().tm_attn_decode(q.data_ptr(), k_cache.data_ptr(), k_scale.data_ptr(), k_zero.data_ptr(),
+                                    v_cache.data_ptr(), v_scale.data_ptr(), v_zero.data_ptr(), lens.data_ptr(),
+                                    out.data_ptr(), B, Hq, Hkv, D, L_max, int(kv_bits), _DT[q.dtype],
+                                    float(sm_scale), int(chunk_tiles), st))
+    return out
+
+
+def attn_decode_plan(B: int, Hq: int, Hkv: int, L_max: int, kv_bits: int, dtype=torch.float16) -> dict:
+    """tm_attn_decode_plan: the automatic chunk_tiles and the grid."""
+    ct, grid = ctypes.c_int(), ctypes.c_int()
+    _check(lib().tm_attn_decode_plan(B, Hq, Hkv, L_max, kv_bits, _DT[dtype], ctypes.byref(ct), ctypes.byref(grid)))
+    return {"chunk_tiles": ct.value, "grid": grid.value}
 
 
 def version() -> str:

@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -971,6 +972,137 @@ tm_status tm_selftest_wait_timeout(long long limit_ns, void *stream) {
   cudaError_t e = launch_wait_selftest(err, static_cast<unsigned long long>(limit_ns),
                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "tm_selftest_wait_timeout");
+  return TM_OK;
+}
+
+// ------------------------------------------------------ decode attention
+// 64-token tiles per unit of work, from the worst case (every sequence at
+// L_max): the smallest per-CTA tile count when U units are spread over the
+// resident grid, counting half a tile of merge work per unit.
+static int attn_chunk_tiles(int B, int Hkv, int tiles, int cap) {
+  int best = 1;
+  double best_cost = 1e300;
+  for (int ct = 1;; ct *= 2) {
+    const long long n_ch = (tiles + ct - 1) / ct;
+    const long long U = static_cast<long long>(B) * Hkv * n_ch;
+    const long long rounds = (U + cap - 1) / cap;
+    const double cost = static_cast<double>(rounds) * (std::min(ct, tiles) + 0.5);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = std::min(ct, tiles);
+    }
+    if (ct >= tiles) break;
+  }
+  return best;
+}
+
+static tm_status encode_kv_map(const uint8_t *cache, long long rows, int row_bytes, CUtensorMap *map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  tm_status s = get_encoder(&enc);
+  if (s != TM_OK) return s;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes), 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(cache), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TM_ERR_CUDA, "cuTensorMapEncodeTiled (KV cache) failed (%d)", (int)r);
+  return TM_OK;
+}
+
+tm_status tm_attn_decode(const void *q, const uint8_t *k_cache, const void *k_scale, const uint8_t *k_zero,
+                         const uint8_t *v_cache, const void *v_scale, const uint8_t *v_zero, const int32_t *lens,
+                         void *o, int B, int Hq, int Hkv, int head_dim, int L_max, int kv_bits, tm_dtype dtype,
+                         float sm_scale, int chunk_tiles, void *stream) {
+  if (B < 0 || Hq < 1 || Hkv < 1) return fail(TM_ERR_INVALID_ARG, "B >= 0, Hq >= 1 and Hkv >= 1 required");
+  if (Hq % Hkv != 0) return fail(TM_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (Hq / Hkv > 16) return fail(TM_ERR_UNSUPPORTED, "at most 16 query heads per KV head");
+  if (head_dim != 128) return fail(TM_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (kv_bits != 4 && kv_bits != 8) return fail(TM_ERR_INVALID_ARG, "kv_bits must be 4 or 8");
+  if (dtype != TM_F16 && dtype != TM_BF16) return fail(TM_ERR_INVALID_ARG, "dtype must be TM_F16 or TM_BF16");
+  if (L_max < 64 || L_max % 64 != 0) return fail(TM_ERR_INVALID_ARG, "L_max must be a positive multiple of 64");
+  if (chunk_tiles < 0) return fail(TM_ERR_INVALID_ARG, "chunk_tiles must be >= 0 (0 = automatic)");
+  if (!std::isfinite(sm_scale)) return fail(TM_ERR_INVALID_ARG, "sm_scale must be finite");
+  const long long rows = static_cast<long long>(B) * Hkv * L_max;
+  if (rows > 0x7FFFFFFFLL) return fail(TM_ERR_UNSUPPORTED, "B * Hkv * L_max must be below 2^31");
+  if (B == 0) return TM_OK;
+  const void *ptrs[] = {q, k_cache, k_scale, k_zero, v_cache, v_scale, v_zero, o};
+  for (const void *ptr : ptrs)
+    if (ptr == nullptr || !aligned16(ptr))
+      return fail(TM_ERR_INVALID_ARG, "q, caches, scales, zeros and o must be non-NULL and 16-byte aligned");
+  if (lens == nullptr) return fail(TM_ERR_INVALID_ARG, "lens must not be NULL");
+  int dev = -1;
+  tm_status s = current_device(&dev);
+  if (s != TM_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == TM_BF16;
+  const int gq = Hq / Hkv;
+  const int occ = attn_decode_ctas_per_sm(bf16, kv_bits, gq);
+  if (occ < 1) return fail(TM_ERR_CUDA, "decode attention kernel cannot be resident");
+  const int cap = sm_count(dev) * occ;
+  const int tiles = L_max / 64;
+  const int ct = chunk_tiles > 0 ? std::min(chunk_tiles, tiles) : attn_chunk_tiles(B, Hkv, tiles, cap);
+  const int n_ch = (tiles + ct - 1) / ct;
+  unsigned int *err = nullptr;
+  s = error_word(dev, &err);
+  if (s != TM_OK) return s;
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t *>(q);
+  a.k_scale = static_cast<const uint16_t *>(k_scale);
+  a.v_scale = static_cast<const uint16_t *>(v_scale);
+  a.k_zero = k_zero;
+  a.v_zero = v_zero;
+  a.lens = lens;
+  a.o = static_cast<uint16_t *>(o);
+  a.err = err;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.L_max = L_max;
+  a.chunk_tiles = ct;
+  a.n_chunks_max = n_ch;
+  a.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+  a.limit_ns = wait_limit_ns();
+  a.pdl = pdl_enabled() ? 1 : 0;
+  if (n_ch > 1) {
+    Workspace *ws = nullptr;
+    const size_t floats = static_cast<size_t>(B) * Hkv * n_ch * gq * (128 + 2);
+    s = get_workspace(dev, st, sizeof(float) * floats, static_cast<size_t>(B) * Hkv, &ws);
+    if (s != TM_OK) return s;
+    a.ws = ws->ws;
+    a.counters = ws->counters;
+  }
+  CUtensorMap kmap, vmap;
+  const int row_bytes = 128 * kv_bits / 8;
+  s = encode_kv_map(k_cache, rows, row_bytes, &kmap);
+  if (s != TM_OK) return s;
+  s = encode_kv_map(v_cache, rows, row_bytes, &vmap);
+  if (s != TM_OK) return s;
+  const long long U = static_cast<long long>(B) * Hkv * n_ch;
+  const int grid = static_cast<int>(std::min<long long>(U, cap));
+  cudaError_t e = launch_attn_decode(kmap, vmap, a, bf16, kv_bits, grid, st);
+  if (e != cudaSuccess) return fail_cuda(e, "tm_attn_decode launch");
+  return TM_OK;
+}
+
+tm_status tm_attn_decode_plan(int B, int Hq, int Hkv, int L_max, int kv_bits, tm_dtype dtype, int *chunk_tiles,
+                              int *grid) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > 16 || L_max < 64 || L_max % 64 != 0 ||
+      (kv_bits != 4 && kv_bits != 8))
+    return fail(TM_ERR_INVALID_ARG, "invalid decode attention shape");
+  int dev = -1;
+  tm_status s = current_device(&dev);
+  if (s != TM_OK) return s;
+  const int occ = attn_decode_ctas_per_sm(dtype == TM_BF16, kv_bits, Hq / Hkv);
+  if (occ < 1) return fail(TM_ERR_CUDA, "decode attention kernel cannot be resident");
+  const int cap = sm_count(dev) * occ;
+  const int tiles = L_max / 64;
+  const int ct = attn_chunk_tiles(B, Hkv, tiles, cap);
+  const long long U = static_cast<long long>(B) * Hkv * ((tiles + ct - 1) / ct);
+  if (chunk_tiles) *chunk_tiles = ct;
+  if (grid) *grid = static_cast<int>(std::min<long long>(U, cap));
   return TM_OK;
 }
 

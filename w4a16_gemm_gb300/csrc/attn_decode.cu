@@ -1,0 +1,640 @@
+// attn_decode.cu -- decode attention (one query token per sequence) over a
+// low-bit KV cache: the attention pipeline of the TurboMind paper
+// (pith.science review, Figure 4: the low-bit cache is loaded, converted to
+// 16-bit values by integer-to-float conversion and scaling, and multiplied
+// in Q K^T and P V on tensor cores; Figure 10: the cache is consumed in
+// 64-token tiles whose loads overlap the two products).
+//
+//   K[t, d] = T(ks[t] * (kq[t, d] - kz[t])),  V likewise   (per token, KV head)
+//   O[hq]   = softmax_t(sm_scale * Q[hq] . K[t]) V,  t < len,  h = hq / GQ
+//
+// Blackwell form:
+//   - A persistent grid walks units (sequence b, KV head h, chunk c of
+//     chunk_tiles 64-token tiles).  One producer lane streams each tile's K
+//     and V rows with TMA tensor copies (128-byte swizzle for 8-bit rows,
+//     64-byte for 4-bit rows, so the transposing reads below hit distinct
+//     banks) and the tile's scales and zeros with bulk copies into a ring.
+//   - Four consumer warps take 16 tokens of each tile.  S^T = Q K^T runs on
+//     mma.sync m16n8k16 with the query heads as the 16 rows (GQ <= 16) and
+//     the dequantized keys as the B operand; the head dimension is summed in
+//     a permuted order (any order gives the same sum) chosen so that each
+//     thread's B fragments come from contiguous bytes of one key row.  The
+//     fp32 scores feed an online softmax (exp2, running max and sum per
+//     head); P, rounded to 16 bits, is the A operand of O += P V, whose B
+//     fragments pair two tokens of one value column: the byte permute that
+//     builds them is the "transpose V" step of Figure 4, done in registers.
+//   - At a unit's end the four warps merge through shared memory; a unit
+//     that covers its whole sequence writes O, otherwise it leaves (m, l, O)
+//     in a workspace slot and the last chunk to arrive (one acq_rel atomic)
+//     merges the chunks in order.  Every wait is bounded.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "mma_frag.cuh"
+#include "ptx.cuh"
+#include "tc_epilogue.cuh"
+
+namespace tmw4 {
+namespace {
+
+constexpr int AD_D = 128;     // head dimension
+constexpr int AD_TT = 64;     // tokens per tile (one ring stage)
+constexpr int AD_CW = 4;      // consumer warps; warp w takes tokens 16w..16w+15 of a tile
+constexpr int AD_THREADS = 32 * (AD_CW + 1);
+constexpr int AD_CSTRIDE = AD_D + 4;   // floats per row of the merge area
+
+template <int BITS>
+struct AdGeom {
+  static constexpr int ROW = AD_D * BITS / 8;                  // bytes per cached token row
+  static constexpr int KV = AD_TT * ROW;                       // one K (or V) tile
+  static constexpr int PRM = AD_TT * 2 * 2 + AD_TT * 2;        // ks, vs (16-bit), kz, vz (bytes)
+  static constexpr int TX = 2 * KV + PRM;                      // bytes landing per stage
+  static constexpr int STAGE = ((TX + 1023) / 1024) * 1024;
+  static constexpr int NS = BITS == 8 ? 3 : 5;                 // ring stages
+  static constexpr int RING = NS * STAGE;
+};
+
+struct AdUnit {
+  int b, h, c, t0, ntile, nch, len;
+};
+
+// Unit u of the walk: chunk-major over (chunk, sequence, KV head), so that a
+// stride of the persistent grid covers many sequences.  false: the chunk
+// lies past the sequence (nothing to do).  A sequence of length 0 keeps its
+// chunk 0 (with no tiles), which writes the zero output.
+__device__ __forceinline__ bool ad_unit(const AttnArgs &p, long long u, AdUnit &x) {
+  const long long bh = static_cast<long long>(p.B) * p.Hkv;
+  x.c = static_cast<int>(u / bh);
+  const int r = static_cast<int>(u % bh);
+  x.b = r / p.Hkv;
+  x.h = r % p.Hkv;
+  int len = __ldg(p.lens + x.b);
+  len = len < 0 ? 0 : (len > p.L_max ? p.L_max : len);
+  x.len = len;
+  const int ctok = p.chunk_tiles * AD_TT;
+  x.nch = len == 0 ? 1 : (len + ctok - 1) / ctok;
+  if (x.c >= x.nch) return false;
+  x.t0 = x.c * ctok;
+  x.ntile = len == 0 ? 0 : min(p.chunk_tiles, (len - x.t0 + AD_TT - 1) / AD_TT);
+  return true;
+}
+
+// 16-bit pairs from 8-bit codes: x holds (1024 + qa, 1024 + qb) (fp16 magic)
+// or the two codes in its low bytes (bf16).  Result T(s * (q - z)) per half,
+// one rounding each: fp16 subtracts exactly under the magic and multiplies
+// once; bf16 goes through fp32 (2^23 magic, exact subtract and product).
+template <bool BF16>
+__device__ __forceinline__ uint32_t kv8_pair(uint32_t qa, uint32_t qb, uint32_t zm, float za, float zb,
+                                             uint32_t s2, float sa, float sb) {
+  if constexpr (BF16) {
+    const float a = (__uint_as_float(0x4B000000u | qa) - za) * sa;
+    const float b = (__uint_as_float(0x4B000000u | qb) - zb) * sb;
+    const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&r);
+  } else {
+    const uint32_t x = (qa | (qb << 16)) | 0x64006400u;
+    const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&x),
+                                      *reinterpret_cast<const __half2 *>(&zm)),
+                              *reinterpret_cast<const __half2 *>(&s2));
+    (void)za; (void)zb; (void)sa; (void)sb;
+    return *reinterpret_cast<const uint32_t *>(&v);
+  }
+}
+
+// 16-bit pairs from 4-bit codes already in the low nibble of each half
+// (x = (qa | qb << 16), both <= 15): the exponent magic (fp16 1024 + q,
+// bf16 128 + q) is exact in either type, so is the subtract of (magic + z),
+// and the multiply by the scale is the one rounding.
+template <bool BF16>
+__device__ __forceinline__ uint32_t kv4_pair(uint32_t x, uint32_t zm, uint32_t s2) {
+  uint32_t r;
+  if constexpr (BF16) {
+    x |= 0x43004300u;
+    asm("{\n\t.reg .b32 d;\n\t"
+        "sub.rn.bf16x2 d, %1, %2;\n\t"
+        "mul.rn.bf16x2 %0, d, %3;\n\t}"
+        : "=r"(r)
+        : "r"(x), "r"(zm), "r"(s2));
+  } else {
+    x |= 0x64006400u;
+    asm("{\n\t.reg .b32 d;\n\t"
+        "sub.rn.f16x2 d, %1, %2;\n\t"
+        "mul.rn.f16x2 %0, d, %3;\n\t}"
+        : "=r"(r)
+        : "r"(x), "r"(zm), "r"(s2));
+  }
+  return r;
+}
+
+// mma_16816 when rows 8..15 of A are zero (at most 8 query heads): those
+// rows' accumulators are neither read nor kept, so they take no registers.
+template <bool BF16>
+__device__ __forceinline__ void mma_16816_lo(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  float x2, x3;
+  if constexpr (BF16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %5}, {%7, %8}, {%9, %10, %11, %11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(x2), "=f"(x3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %5}, {%7, %8}, {%9, %10, %11, %11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(x2), "=f"(x3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f));
+  }
+  (void)x2;
+  (void)x3;
+}
+
+template <bool BF16, bool HI>
+__device__ __forceinline__ void mma_q(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                      uint32_t b0, uint32_t b1) {
+  if constexpr (HI) {
+    mma_16816<BF16>(d, a0, a1, a2, a3, b0, b1);
+  } else {
+    (void)a1;
+    (void)a3;
+    mma_16816_lo<BF16>(d, a0, a2, b0, b1);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&r);
+  } else {
+    const __half2 r = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&r);
+  }
+}
+
+// (magic + za, magic + zb) as a 16-bit pair: exact integers in either type.
+template <bool BF16, int BITS>
+__device__ __forceinline__ uint32_t zero_pair(uint32_t za, uint32_t zb) {
+  if constexpr (BF16 && BITS == 4) {
+    return (0x4300u + za) | ((0x4300u + zb) << 16);   // 128 + z, z <= 15: mantissa bits
+  } else {
+    return (0x6400u + za) | ((0x6400u + zb) << 16);   // 1024 + z, z <= 255
+  }
+}
+
+template <bool BF16, int BITS, bool HI>
+__global__ void __launch_bounds__(AD_THREADS)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                       const AttnArgs p) {
+  using Gm = AdGeom<BITS>;
+  constexpr int NS = Gm::NS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *ring = align_smem_1024(smem_raw);
+  const int GQ = p.Hq / p.Hkv;
+  float *cO = reinterpret_cast<float *>(ring + Gm::RING);               // [CW][GQ][CSTRIDE]
+  float *cM = cO + AD_CW * GQ * AD_CSTRIDE;                             // [CW][GQ]
+  float *cL = cM + AD_CW * GQ;                                          // [CW][GQ]
+  uint64_t *full = reinterpret_cast<uint64_t *>(cL + AD_CW * GQ + 2);   // 536 GQ + 2 floats in: 8-byte aligned
+  uint64_t *empty = full + NS;
+  volatile int *flags = reinterpret_cast<volatile int *>(empty + NS);   // abort, last arriver, exit
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < NS) {
+    mbar_init(full + threadIdx.x, 1);
+    mbar_init(empty + threadIdx.x, AD_CW);
+  }
+  if (threadIdx.x == 0) {
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  // the lengths, queries and cache may come from the previous kernel
+  pdl_wait();
+
+  const long long U = static_cast<long long>(p.n_chunks_max) * p.B * p.Hkv;
+
+  if (warp == AD_CW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+      int i = 0;
+      bool ok = true;
+      for (long long u = blockIdx.x; u < U && ok; u += gridDim.x) {
+        AdUnit x;
+        if (!ad_unit(p, u, x)) continue;
+        const long long row = (static_cast<long long>(x.b) * p.Hkv + x.h) * p.L_max + x.t0;
+        for (int tt = 0; tt < x.ntile; ++tt, ++i) {
+          const int s = i % NS;
+          if (i >= NS &&
+              !mbar_wait_bounded(empty + s, ((i / NS) & 1) ^ 1u, p.limit_ns, reinterpret_cast<volatile int *>(flags),
+                                 p.err, SITE_PRODUCER_EMPTY, i)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = ring + s * Gm::STAGE;
+          const long long r = row + static_cast<long long>(tt) * AD_TT;
+          mbar_arrive_expect_tx(full + s, Gm::TX);
+          tma_load_2d(st, &kmap, 0, static_cast<int32_t>(r), full + s);
+          tma_load_2d(st + Gm::KV, &vmap, 0, static_cast<int32_t>(r), full + s);
+          tma_bulk_g2s(st + 2 * Gm::KV, p.k_scale + r, AD_TT * 2, full + s);
+          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 2, p.v_scale + r, AD_TT * 2, full + s);
+          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 4, p.k_zero + r, AD_TT, full + s);
+          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 5, p.v_zero + r, AD_TT, full + s);
+        }
+      }
+      // every copy issued must land before the CTA exits
+      for (int j = max(0, i - NS); j < i; ++j)
+        mbar_wait_bounded(full + j % NS, (j / NS) & 1, p.limit_ns, nullptr, p.err, SITE_DRAIN_TMA, j);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, t = lane & 3;
+  const int ctid = threadIdx.x;   // 0..127
+  const float NEG_INF = -__int_as_float(0x7F800000);
+  int i = 0;
+  for (long long u = blockIdx.x; u < U; u += gridDim.x) {
+    AdUnit x;
+    if (!ad_unit(p, u, x)) continue;
+    const long long bh = static_cast<long long>(x.b) * p.Hkv + x.h;
+    const size_t orow0 = (static_cast<size_t>(x.b) * p.Hq + static_cast<size_t>(x.h) * GQ);
+    if (x.ntile == 0) {
+      // empty sequence: zero output
+      for (int e = ctid; e < GQ * AD_D; e += 32 * AD_CW) p.o[orow0 * AD_D + e] = 0;
+      continue;
+    }
+
+    // Q fragments.  Thread t's head-dimension range is [32t, 32t + 32); the
+    // order inside it matches the B fragments built from the key rows below.
+    uint32_t qa[8][2], qb[8][2];
+    {
+      uint32_t h0[16], h1[16];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int head = g + 8 * r;
+        uint32_t *hv = r == 0 ? h0 : h1;
+        if ((r == 0 || HI) && head < GQ) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (orow0 + head) * AD_D + 32 * t);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = src[k];
+            hv[4 * k] = v.x; hv[4 * k + 1] = v.y; hv[4 * k + 2] = v.z; hv[4 * k + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) hv[k] = 0;
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        if constexpr (BITS == 8) {
+          // step s: elements 4s, 4s+1 | 4s+2, 4s+3
+          qa[s][0] = h0[2 * s]; qa[s][1] = h0[2 * s + 1];
+          qb[s][0] = h1[2 * s]; qb[s][1] = h1[2 * s + 1];
+        } else {
+          // step 2m + r: elements (8m + 2r, 8m + 2r + 4) | (8m + 2r + 1, 8m + 2r + 5)
+          const int m = s >> 1, r = s & 1;
+          const uint32_t lo0 = h0[4 * m + r], hi0 = h0[4 * m + 2 + r];
+          const uint32_t lo1 = h1[4 * m + r], hi1 = h1[4 * m + 2 + r];
+          qa[s][0] = __byte_perm(lo0, hi0, 0x5410); qa[s][1] = __byte_perm(lo0, hi0, 0x7632);
+          qb[s][0] = __byte_perm(lo1, hi1, 0x5410); qb[s][1] = __byte_perm(lo1, hi1, 0x7632);
+        }
+      }
+    }
+
+    float m_run[2] = {NEG_INF, NEG_INF}, l_run[2] = {0.f, 0.f};
+    float o[16][4];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
+
+    bool ok = true;
+    for (int tt = 0; tt < x.ntile; ++tt, ++i) {
+      const int s = i % NS;
+      if (!mbar_wait_all(full + s, (i / NS) & 1, p.limit_ns, reinterpret_cast<volatile int *>(flags), p.err,
+                         SITE_DQ_FULL, i)) {
+        ok = false;
+        ++i;
+        break;
+      }
+      const uint8_t *st = ring + s * Gm::STAGE;
+      const uint8_t *sK = st, *sV = st + Gm::KV;
+      const uint16_t *sks = reinterpret_cast<const uint16_t *>(st + 2 * Gm::KV);
+      const uint16_t *svs = sks + AD_TT;
+      const uint8_t *skz = st + 2 * Gm::KV + AD_TT * 4;
+      const uint8_t *svz = skz + AD_TT;
+      const int tb = 16 * warp;
+      const int tok0 = x.t0 + tt * AD_TT + tb;   // sequence position of this warp's first token
+
+      // ---- S^T = Q K^T over this warp's 16 tokens (two n8 tiles)
+      float sc[2][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
+      {
+        uint32_t kw[2][8];
+        uint32_t kzm[2], ks2[2];
+        float kzf[2], ksf[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int r = tb + 8 * j + g;
+          const uint32_t z = skz[r], sbits = sks[r];
+          kzm[j] = zero_pair<BF16, BITS>(z, z);
+          ks2[j] = sbits | (sbits << 16);
+          kzf[j] = __uint_as_float(0x4B000000u | z);
+          ksf[j] = bits16_to_f32<BF16>(sbits);
+          if constexpr (BITS == 8) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint4 v = *reinterpret_cast<const uint4 *>(sK + r * 128 + (((2 * t + c) ^ (r & 7)) << 4));
+              kw[j][4 * c] = v.x; kw[j][4 * c + 1] = v.y; kw[j][4 * c + 2] = v.z; kw[j][4 * c + 3] = v.w;
+            }
+          } else {
+            const uint4 v = *reinterpret_cast<const uint4 *>(sK + r * 64 + ((t ^ ((r >> 1) & 3)) << 4));
+            kw[j][0] = v.x; kw[j][1] = v.y; kw[j][2] = v.z; kw[j][3] = v.w;
+          }
+        }
+#pragma unroll
+        for (int s8 = 0; s8 < 8; ++s8) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            uint32_t b0, b1;
+            if constexpr (BITS == 8) {
+              const uint32_t w = kw[j][s8];
+              b0 = kv8_pair<BF16>(w & 0xFFu, (w >> 8) & 0xFFu, kzm[j], kzf[j], kzf[j], ks2[j], ksf[j], ksf[j]);
+              b1 = kv8_pair<BF16>((w >> 16) & 0xFFu, w >> 24, kzm[j], kzf[j], kzf[j], ks2[j], ksf[j], ksf[j]);
+            } else {
+              const uint32_t w = kw[j][s8 >> 1] >> (8 * (s8 & 1));
+              b0 = kv4_pair<BF16>(w & 0x000F000Fu, kzm[j], ks2[j]);
+              b1 = kv4_pair<BF16>((w >> 4) & 0x000F000Fu, kzm[j], ks2[j]);
+            }
+            mma_q<BF16, HI>(sc[j], qa[s8][0], qb[s8][0], qa[s8][1], qb[s8][1], b0, b1);
+          }
+        }
+      }
+
+      // ---- mask, online softmax (rows g and g + 8 of this thread)
+      float pmax[2] = {NEG_INF, NEG_INF};
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool valid = tok0 + 8 * j + 2 * t + (e & 1) < x.len;
+          sc[j][e] = valid ? sc[j][e] * p.sm_scale_log2 : NEG_INF;
+          pmax[e >> 1] = fmaxf(pmax[e >> 1], sc[j][e]);
+        }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        pmax[r] = fmaxf(pmax[r], __shfl_xor_sync(0xFFFFFFFFu, pmax[r], 1));
+        pmax[r] = fmaxf(pmax[r], __shfl_xor_sync(0xFFFFFFFFu, pmax[r], 2));
+      }
+      float corr[2], muse[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float mnew = fmaxf(m_run[r], pmax[r]);
+        muse[r] = mnew == NEG_INF ? 0.f : mnew;
+        corr[r] = exp2f(m_run[r] - muse[r]);
+        m_run[r] = mnew;
+      }
+      float psum[2] = {0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sc[j][e] = exp2f(sc[j][e] - muse[e >> 1]);
+          psum[e >> 1] += sc[j][e];
+        }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * corr[r] + psum[r];
+      if (__any_sync(0xFFFFFFFFu, corr[0] != 1.f || (HI && corr[1] != 1.f))) {
+#pragma unroll
+        for (int jn = 0; jn < 16; ++jn) {
+          o[jn][0] *= corr[0]; o[jn][1] *= corr[0];
+          if constexpr (HI) {
+            o[jn][2] *= corr[1]; o[jn][3] *= corr[1];
+          }
+        }
+      }
+      const uint32_t pa0 = pack2<BF16>(sc[0][0], sc[0][1]);
+      const uint32_t pa2 = pack2<BF16>(sc[1][0], sc[1][1]);
+      const uint32_t pa1 = HI ? pack2<BF16>(sc[0][2], sc[0][3]) : 0u;
+      const uint32_t pa3 = HI ? pack2<BF16>(sc[1][2], sc[1][3]) : 0u;
+
+      // ---- O += P V: B fragments pair tokens (2t, 2t+1) and (2t+8, 2t+9) of
+      // value column d = 16 g + jn
+      {
+        uint32_t vzm[2], vs2[2];
+        float vzf[4], vsf[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = tb + 2 * t + (q & 1) + 8 * (q >> 1);
+          const bool valid = tok0 + 2 * t + (q & 1) + 8 * (q >> 1) < x.len;
+          vzf[q] = __uint_as_float(0x4B000000u | svz[r]);
+          // a token past the length gets scale 0: its value row is exactly 0
+          // whatever the (unwritten) cache holds there
+          const uint32_t sbits = valid ? svs[r] : 0u;
+          vsf[q] = bits16_to_f32<BF16>(sbits);
+          if ((q & 1) == 0) {
+            vzm[q >> 1] = svz[r];
+            vs2[q >> 1] = sbits;
+          } else {
+            vzm[q >> 1] = zero_pair<BF16, BITS>(vzm[q >> 1], svz[r]);
+            vs2[q >> 1] |= sbits << 16;
+          }
+        }
+        if constexpr (BITS == 8) {
+          uint4 vr[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = tb + 2 * t + (q & 1) + 8 * (q >> 1);
+            vr[q] = *reinterpret_cast<const uint4 *>(sV + r * 128 + ((g ^ (r & 7)) << 4));
+          }
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            const uint32_t a0 = (&vr[0].x)[wi], a1 = (&vr[1].x)[wi];
+            const uint32_t c0 = (&vr[2].x)[wi], c1 = (&vr[3].x)[wi];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t b0 = kv8_pair<BF16>((a0 >> (8 * e)) & 0xFFu, (a1 >> (8 * e)) & 0xFFu, vzm[0], vzf[0],
+                                                 vzf[1], vs2[0], vsf[0], vsf[1]);
+              const uint32_t b1 = kv8_pair<BF16>((c0 >> (8 * e)) & 0xFFu, (c1 >> (8 * e)) & 0xFFu, vzm[1], vzf[2],
+                                                 vzf[3], vs2[1], vsf[2], vsf[3]);
+              mma_q<BF16, HI>(o[4 * wi + e], pa0, pa1, pa2, pa3, b0, b1);
+            }
+          }
+        } else {
+          uint2 vr[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = tb + 2 * t + (q & 1) + 8 * (q >> 1);
+            vr[q] = *reinterpret_cast<const uint2 *>(sV + r * 64 + ((((g >> 1) ^ ((r >> 1) & 3)) << 4) | ((g & 1) << 3)));
+          }
+#pragma unroll
+          for (int wi = 0; wi < 2; ++wi) {
+            const uint32_t a0 = (&vr[0].x)[wi], a1 = (&vr[1].x)[wi];
+            const uint32_t c0 = (&vr[2].x)[wi], c1 = (&vr[3].x)[wi];
+            // byte k of a word holds value columns 2k (low nibble) and 2k + 1
+            // (high nibble).  xs = (a0.b_k, a0.b_k+1, a1.b_k, a1.b_k+1): its
+            // nibble at bit `sh` of each half is the (token 2t, token 2t + 1)
+            // pair of one column
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+              const uint32_t xs = __byte_perm(a0, a1, which ? 0x7632 : 0x5410);
+              const uint32_t ys = __byte_perm(c0, c1, which ? 0x7632 : 0x5410);
+#pragma unroll
+              for (int sh = 0; sh < 16; sh += 4) {
+                const uint32_t b0 = kv4_pair<BF16>((xs >> sh) & 0x000F000Fu, vzm[0], vs2[0]);
+                const uint32_t b1 = kv4_pair<BF16>((ys >> sh) & 0x000F000Fu, vzm[1], vs2[1]);
+                mma_q<BF16, HI>(o[8 * wi + 4 * which + sh / 4], pa0, pa1, pa2, pa3, b0, b1);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+
+    // ---- merge the four warps
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      l_run[r] += __shfl_xor_sync(0xFFFFFFFFu, l_run[r], 1);
+      l_run[r] += __shfl_xor_sync(0xFFFFFFFFu, l_run[r], 2);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int head = g + 8 * r;
+      if ((r == 0 || HI) && head < GQ) {
+        float *row = cO + (warp * GQ + head) * AD_CSTRIDE;
+        // fragment order: column n of n-tile jn is value column 16 n + jn
+#pragma unroll
+        for (int jn = 0; jn < 16; ++jn)
+          *reinterpret_cast<float2 *>(row + jn * 8 + 2 * t) = make_float2(o[jn][2 * r], o[jn][2 * r + 1]);
+        if (t == 0) {
+          cM[warp * GQ + head] = m_run[r];
+          cL[warp * GQ + head] = l_run[r];
+        }
+      }
+    }
+    named_bar_sync(1, 32 * AD_CW);
+    const int d = ctid;                              // this thread's value column
+    const int fo = (d & 15) * 8 + (d >> 4);          // its place in fragment order
+    const bool whole = x.nch == 1;
+    float *wsO = p.ws + (static_cast<size_t>(bh) * p.n_chunks_max + x.c) * GQ * (AD_D + 2);
+    for (int head = 0; head < GQ; ++head) {
+      float mx = NEG_INF;
+#pragma unroll
+      for (int w = 0; w < AD_CW; ++w) mx = fmaxf(mx, cM[w * GQ + head]);
+      float acc = 0.f, l = 0.f;
+#pragma unroll
+      for (int w = 0; w < AD_CW; ++w) {
+        const float f = exp2f(cM[w * GQ + head] - mx);
+        acc += f * cO[(w * GQ + head) * AD_CSTRIDE + fo];
+        l += f * cL[w * GQ + head];
+      }
+      if (whole) {
+        reinterpret_cast<uint16_t *>(p.o)[(orow0 + head) * AD_D + d] = f32_to_bits16<BF16>(acc / l);
+      } else {
+        float *slot = wsO + head * (AD_D + 2);
+        slot[d] = acc;
+        if (d == 0) {
+          slot[AD_D] = mx;
+          slot[AD_D + 1] = l;
+        }
+      }
+    }
+    if (!whole) {
+      // publish, count; the last chunk of (b, h) to arrive merges in order
+      __threadfence();
+      named_bar_sync(1, 32 * AD_CW);
+      if (ctid == 0) {
+        const unsigned old = atomic_add_acq_rel_gpu(p.counters + bh, 1u);
+        const bool last = old == static_cast<unsigned>(x.nch - 1);
+        if (last) p.counters[bh] = 0;   // self-resetting for the next launch
+        flags[1] = last ? 1 : 0;
+      }
+      named_bar_sync(1, 32 * AD_CW);
+      if (flags[1]) {
+        const float *base = p.ws + static_cast<size_t>(bh) * p.n_chunks_max * GQ * (AD_D + 2);
+        for (int head = 0; head < GQ; ++head) {
+          float mx = NEG_INF;
+          for (int c = 0; c < x.nch; ++c) mx = fmaxf(mx, __ldcg(base + (c * GQ + head) * (AD_D + 2) + AD_D));
+          float acc = 0.f, l = 0.f;
+          for (int c = 0; c < x.nch; ++c) {
+            const float *slot = base + (c * GQ + head) * (AD_D + 2);
+            const float f = exp2f(__ldcg(slot + AD_D) - mx);
+            acc += f * __ldcg(slot + d);
+            l += f * __ldcg(slot + AD_D + 1);
+          }
+          reinterpret_cast<uint16_t *>(p.o)[(orow0 + head) * AD_D + d] = f32_to_bits16<BF16>(acc / l);
+        }
+      }
+    }
+    // the merge area is rewritten by the next unit; the exit decision is
+    // taken from one copy of the abort flag so that every consumer warp
+    // leaves together (the named barriers above need all four)
+    if (ctid == 0) flags[2] = flags[0];
+    named_bar_sync(1, 32 * AD_CW);
+    (void)ok;
+    if (flags[2]) break;
+  }
+}
+
+}  // namespace
+
+size_t attn_decode_smem_bytes(int bits, int gq) {
+  const int ring = bits == 8 ? AdGeom<8>::RING : AdGeom<4>::RING;
+  const size_t merge = sizeof(float) * (static_cast<size_t>(AD_CW) * gq * AD_CSTRIDE + 2 * AD_CW * gq + 2);
+  const int ns = bits == 8 ? AdGeom<8>::NS : AdGeom<4>::NS;
+  return 1024 + ring + merge + 16 * ns + 16;
+}
+
+template <bool BF16, int BITS, bool HI>
+static cudaError_t launch_ad_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnArgs &a, int grid,
+                               cudaStream_t st) {
+  auto kern = attn_decode_kernel<BF16, BITS, HI>;
+  const size_t smem = attn_decode_smem_bytes(BITS, a.Hq / a.Hkv);
+  cudaError_t e = smem_optin<attn_decode_kernel<BF16, BITS, HI>>(static_cast<int>(attn_decode_smem_bytes(BITS, 16)));
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, dim3(grid), dim3(AD_THREADS), smem, st, a.pdl != 0, km, vm, a);
+}
+
+template <bool BF16, int BITS, bool HI>
+static int ad_occ_t(int gq) {
+  int n = 0;
+  if (smem_optin<attn_decode_kernel<BF16, BITS, HI>>(static_cast<int>(attn_decode_smem_bytes(BITS, 16))) !=
+      cudaSuccess)
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<BF16, BITS, HI>, AD_THREADS,
+                                                    attn_decode_smem_bytes(BITS, gq)) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+int attn_decode_ctas_per_sm(bool bf16, int bits, int gq) {
+  const bool hi = gq > 8;
+#define AD_OCC(B, W, H) \
+  if (bf16 == B && bits == W && hi == H) return ad_occ_t<B, W, H>(gq);
+  AD_OCC(false, 8, false) AD_OCC(false, 8, true) AD_OCC(false, 4, false) AD_OCC(false, 4, true)
+  AD_OCC(true, 8, false) AD_OCC(true, 8, true) AD_OCC(true, 4, false) AD_OCC(true, 4, true)
+#undef AD_OCC
+  return 0;
+}
+
+cudaError_t launch_attn_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a, bool bf16,
+                               int bits, int grid, cudaStream_t st) {
+  const bool hi = a.Hq / a.Hkv > 8;
+#define AD_LAUNCH(B, W, H) \
+  if (bf16 == B && bits == W && hi == H) return launch_ad_t<B, W, H>(kmap, vmap, a, grid, st);
+  AD_LAUNCH(false, 8, false) AD_LAUNCH(false, 8, true) AD_LAUNCH(false, 4, false) AD_LAUNCH(false, 4, true)
+  AD_LAUNCH(true, 8, false) AD_LAUNCH(true, 8, true) AD_LAUNCH(true, 4, false) AD_LAUNCH(true, 4, true)
+#undef AD_LAUNCH
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tmw4

@@ -56,6 +56,35 @@ struct GemmArgs {
   long long *trace;
 };
 
+// Decode attention over a low-bit KV cache (attn_decode.cu).  q, o
+// [B][Hq][128]; cache rows [B][Hkv][L_max][128 * bits / 8] (K and V, through
+// the tensor maps); scales [B][Hkv][L_max] 16-bit; zeros [B][Hkv][L_max]
+// bytes; lens [B] (device).  ws holds one (O[128], m, l) fp32 slot per
+// (sequence, KV head, chunk, query head of the group); counters one
+// self-resetting arrival count per (sequence, KV head).
+struct AttnArgs {
+  const uint16_t *q;
+  const uint16_t *k_scale;
+  const uint16_t *v_scale;
+  const uint8_t *k_zero;
+  const uint8_t *v_zero;
+  const int *lens;
+  uint16_t *o;
+  float *ws;
+  unsigned int *counters;
+  unsigned int *err;
+  int B, Hq, Hkv, L_max;
+  int chunk_tiles;    // 64-token tiles per unit of work
+  int n_chunks_max;   // ceil(L_max / (64 * chunk_tiles))
+  float sm_scale_log2;
+  unsigned long long limit_ns;
+  int pdl;
+};
+size_t attn_decode_smem_bytes(int bits, int gq);
+int attn_decode_ctas_per_sm(bool bf16, int bits, int gq);
+cudaError_t launch_attn_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a, bool bf16,
+                               int bits, int grid, cudaStream_t st);
+
 // Launch kern<<<grid, block, smem, st>>>(args...), with programmatic stream
 // serialization when pdl is set (see GemmArgs::pdl).
 template <typename... KArgs, typename... Args>
