@@ -68,6 +68,10 @@ def parse():
                     help="workloads of the per-problem block ('' to skip it)")
     ap.add_argument("--formats", type=str, default="int8,fp8,w4_g32",
                     help="non-default weight formats to time beside the configs ('' skips)")
+    ap.add_argument("--attn-case", type=str, default=None,
+                    help="one decode-attention case name:case[:chunk_tiles], repeated --reps times")
+    ap.add_argument("--attention", type=str, default=",".join(("attn_8b_kv8", "attn_8b_kv4")),
+                    help="decode-attention workloads to time beside the configs ('' skips)")
     ap.add_argument("--config-cpu-seconds", type=float, default=1.0,
                     help="CPU time of the oracle sample per shape in the per-config block")
     return ap.parse_args()
@@ -457,6 +461,164 @@ def formats_sweep(fmts: list, dev, stream, peaks: dict, tune: bool) -> dict:
     return out
 
 
+ATTN_NAMES = ("attn_8b_kv8", "attn_8b_kv4")
+
+
+def attn_kv_bytes(lens, Hkv: int, D: int, bits: int) -> float:
+    """Algorithmic cache bytes of one decode-attention step: per cached token
+    and KV head, K and V codes (D * bits / 8 bytes each) with a 16-bit scale
+    and an 8-bit zero each."""
+    return float(sum(int(n) for n in lens)) * Hkv * (2 * D * bits / 8 + 2 * 3)
+
+
+def attention_sweep(names: list, dev, stream, peaks: dict, cpu_budget_s: float) -> dict:
+    """Times decode attention over the low-bit KV cache for every (batch,
+    length mix) case of each workload, graph of GRAPH_LAUNCHES launches over
+    rotated cache copies (> 3x L2 when one copy is smaller), median of
+    GRAPH_REPEATS replays; HBM roofline on the algorithmic bytes (cache +
+    Q + O).  The cache is drawn on the device (uniform codes and zeros,
+    per-token scales uniform in the workload's range); the CPU oracle is
+    timed on one sequence of each case."""
+    import torch
+
+    from w4a16_gemm_gb300 import binding, synth
+
+    L2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for name in names:
+        wl = synth.ATTN_WORKLOADS[name]
+        cases = []
+        for ci, (B, _) in enumerate(wl.cases):
+            c = attn_case_inputs(name, ci, dev, L2)
+            copies, q, o, lens, lens_np, R = c["copies"], c["q"], c["o"], c["lens"], c["lens_np"], c["R"]
+            L_max, kvb, alloc, sm = c["L_max"], c["kv_bytes"], c["alloc"], c["sm_scale"]
+            plan = binding.attn_decode_plan(B, wl.Hq, wl.Hkv, L_max, wl.bits, q.dtype)
+            ts = graph_time(lambda i: binding.attn_decode(q, lens=lens, kv_bits=wl.bits, sm_scale=sm, out=o,
+                                                          stream=stream, **copies[i % R]),
+                            stream, GRAPH_LAUNCHES, GRAPH_REPEATS)
+            binding.poll_error(stream)
+            t = statistics.median(ts)
+            tot = kvb + 2.0 * 2 * B * wl.Hq * wl.D
+            rec = {"B": B, "lens": f"{int(lens_np.min())}..{int(lens_np.max())} (sum {int(lens_np.sum())})",
+                   "L_max": L_max, "us": round(t * 1e6, 3), "us_min": round(min(ts) * 1e6, 3),
+                   "kv_gbs": round(kvb / t / 1e9, 1), "bytes": round(tot),
+                   "frac_hbm": round(tot / t / 1e9 / peaks["hbm_gbs"], 4),
+                   "chunk_tiles": plan["chunk_tiles"], "grid": plan["grid"], "copies": R,
+                   "device_bytes_per_copy": alloc}
+            if cpu_budget_s > 0:
+                rec["cpu_oracle_s_one_seq"] = round(_attn_oracle_one(copies[0], q, lens_np, wl, sm), 4)
+            cases.append(rec)
+            del c, copies, q, o, lens
+            torch.cuda.synchronize()
+        t_all = sum(c["us"] for c in cases) * 1e-6
+        b_all = sum(c["bytes"] for c in cases)
+        out[name] = {"cases": cases, "kernel": f"attn_decode_kernel<{wl.dtype},{wl.bits}>",
+                     "layout": f"Hq={wl.Hq} Hkv={wl.Hkv} D={wl.D}, {wl.bits}-bit KV, {wl.dtype}",
+                     "gbs_over_cases": round(b_all / t_all / 1e9, 1),
+                     "frac_hbm_over_cases": round(b_all / t_all / 1e9 / peaks["hbm_gbs"], 4)}
+    return out
+
+
+def attn_case_inputs(name: str, ci: int, dev, L2: int, copies: int | None = None) -> dict:
+    """Device inputs of case ci of an attention workload: the cache drawn on
+    the device (uniform codes and zeros, per-token scales uniform in the
+    workload's range), in enough rotated copies that the copies together
+    exceed 3x L2 (unless `copies` is given), N(0, 1) queries, the seeded
+    length mix."""
+    import math
+
+    import torch
+
+    from w4a16_gemm_gb300 import synth
+
+    wl = synth.ATTN_WORKLOADS[name]
+    B = wl.cases[ci][0]
+    dt = torch.float16 if wl.dtype == "f16" else torch.bfloat16
+    width = wl.D * wl.bits // 8
+    zhi = 256 if wl.bits == 8 else 16
+    lo, hi = (0.004, 0.012) if wl.bits == 8 else (0.06, 0.2)
+    lens_np = synth.attn_lens(name, ci)
+    L_max = int(-(-int(lens_np.max()) // 64) * 64)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(9000 + 10 * ci + wl.bits)
+    kvb = attn_kv_bytes(lens_np, wl.Hkv, wl.D, wl.bits)
+    R = copies or (min(64, math.ceil(3 * L2 / kvb) + 1) if kvb < 3 * L2 else 1)
+
+    def cache():
+        shp = (B, wl.Hkv, L_max)
+        return dict(
+            k_cache=torch.randint(0, 256, shp + (width,), dtype=torch.uint8, device=dev, generator=gen),
+            v_cache=torch.randint(0, 256, shp + (width,), dtype=torch.uint8, device=dev, generator=gen),
+            k_scale=(torch.rand(shp, device=dev, generator=gen) * (hi - lo) + lo).to(dt),
+            v_scale=(torch.rand(shp, device=dev, generator=gen) * (hi - lo) + lo).to(dt),
+            k_zero=torch.randint(0, zhi, shp, dtype=torch.uint8, device=dev, generator=gen),
+            v_zero=torch.randint(0, zhi, shp, dtype=torch.uint8, device=dev, generator=gen))
+
+    q = torch.randn((B, wl.Hq, wl.D), device=dev, generator=gen).to(dt)
+    return {"copies": [cache() for _ in range(R)], "q": q, "o": torch.empty_like(q),
+            "lens": torch.from_numpy(lens_np).to(dev), "lens_np": lens_np, "R": R, "L_max": L_max,
+            "kv_bytes": kvb, "alloc": B * wl.Hkv * L_max * (2 * width + 6), "sm_scale": 1.0 / math.sqrt(wl.D)}
+
+
+def run_attn_case(args) -> dict:
+    """One decode-attention case, repeated eagerly over rotated cache copies
+    (a small case for ncu captures): --attn-case name:case[:chunk_tiles]."""
+    import torch
+
+    from w4a16_gemm_gb300 import binding, build, synth
+
+    build.build()
+    parts = args.attn_case.split(":")
+    name, ci = parts[0], int(parts[1])
+    ct = int(parts[2]) if len(parts) > 2 else 0
+    wl = synth.ATTN_WORKLOADS[name]
+    L2 = torch.cuda.get_device_properties(0).L2_cache_size
+    c = attn_case_inputs(name, ci, torch.device("cuda"), L2, copies=2)
+
+    def launch(i):
+        binding.attn_decode(c["q"], lens=c["lens"], kv_bits=wl.bits, sm_scale=c["sm_scale"], out=c["o"],
+                            chunk_tiles=ct, **c["copies"][i % 2])
+
+    for i in range(2):
+        launch(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.reps):
+        launch(i)
+    e1.record()
+    torch.cuda.synchronize()
+    binding.poll_error()
+    us = e0.elapsed_time(e1) * 1e3 / args.reps
+    return {"metric": "decode attention KV GB/s (single case)", "value": round(c["kv_bytes"] / us / 1e3, 1),
+            "unit": "GB/s", "case": {"workload": name, "case": ci, "B": int(len(c["lens_np"])),
+                                     "L_max": c["L_max"], "chunk_tiles": ct},
+            "us_per_launch": round(us, 2), "kv_bytes": c["kv_bytes"],
+            "note": "eager launches, 2 rotated cache copies; for profiling, not the headline"}
+
+
+def _attn_oracle_one(c, q, lens_np, wl, sm) -> float:
+    """Seconds of the CPU oracle for the first sequence of a case."""
+    import numpy as np
+
+    from oracle import attention
+
+    n = int(lens_np[0])
+    h = lambda t: t[:1, :, :n].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    u = lambda t: t[:1, :, :n].contiguous().cpu().numpy()
+    qb = q[:1].contiguous().view(torch_int16()).cpu().numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    attention.attn_decode_ref(qb, u(c["k_cache"]), h(c["k_scale"]), u(c["k_zero"]), u(c["v_cache"]),
+                              h(c["v_scale"]), u(c["v_zero"]), lens_np[:1], wl.bits, wl.dtype, sm)
+    return time.perf_counter() - t0
+
+
+def torch_int16():
+    import torch
+
+    return torch.int16
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank: int, world: int):
     import numpy as np
@@ -611,6 +773,12 @@ def run_ours(args, rank: int, world: int):
     if fmts:
         formats = formats_sweep(fmts, dev, stream, peaks, tune=not args.no_tune)
 
+    attention = None
+    anames = [x for x in args.attention.split(",") if x]
+    if anames:
+        attention = attention_sweep(anames, dev, stream, peaks,
+                                    cpu_budget_s=args.config_cpu_seconds if rank == 0 else 0.0)
+
     # roofline of the dominant kernel of the headline step: the variant with the
     # most time per step, from the per-problem graph timings of the decode sweep
     roof = None
@@ -667,6 +835,7 @@ def run_ours(args, rank: int, world: int):
         "variants": {f"{shapes[si][0]}x{shapes[si][1]}xM{M}": variants[(si, M)] for si, M in problems},
         "configs": configs,
         "formats": formats,
+        "attention": attention,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "tensor_tflops": peaks["bf16_tflops"], "source": peak_src},
     }
     return line
@@ -792,6 +961,9 @@ def run_case(args) -> dict:
 
 def main():
     args = parse()
+    if args.attn_case:
+        print(json.dumps(run_attn_case(args)), flush=True)
+        return
     if args.case:
         print(json.dumps(run_case(args)), flush=True)
         return

@@ -977,8 +977,9 @@ tm_status tm_selftest_wait_timeout(long long limit_ns, void *stream) {
 
 // ------------------------------------------------------ decode attention
 // 64-token tiles per unit of work, from the worst case (every sequence at
-// L_max): the smallest per-CTA tile count when U units are spread over the
-// resident grid, counting half a tile of merge work per unit.
+// L_max): the smallest per-CTA time when U units are spread over the
+// resident grid, in tiles, counting half a tile of merge work per unit and,
+// for the last chunk to arrive, a sixteenth of a tile per chunk it merges.
 static int attn_chunk_tiles(int B, int Hkv, int tiles, int cap) {
   int best = 1;
   double best_cost = 1e300;
@@ -986,7 +987,8 @@ static int attn_chunk_tiles(int B, int Hkv, int tiles, int cap) {
     const long long n_ch = (tiles + ct - 1) / ct;
     const long long U = static_cast<long long>(B) * Hkv * n_ch;
     const long long rounds = (U + cap - 1) / cap;
-    const double cost = static_cast<double>(rounds) * (std::min(ct, tiles) + 0.5);
+    const double cost = static_cast<double>(rounds) * (std::min(ct, tiles) + 0.5) +
+                        (n_ch > 1 ? static_cast<double>(n_ch) / 16.0 : 0.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = std::min(ct, tiles);
@@ -1068,7 +1070,7 @@ tm_status tm_attn_decode(const void *q, const uint8_t *k_cache, const void *k_sc
   a.pdl = pdl_enabled() ? 1 : 0;
   if (n_ch > 1) {
     Workspace *ws = nullptr;
-    const size_t floats = static_cast<size_t>(B) * Hkv * n_ch * gq * (128 + 2);
+    const size_t floats = static_cast<size_t>(B) * Hkv * n_ch * gq * (128 + 4);
     s = get_workspace(dev, st, sizeof(float) * floats, static_cast<size_t>(B) * Hkv, &ws);
     if (s != TM_OK) return s;
     a.ws = ws->ws;

@@ -43,6 +43,12 @@ constexpr int AD_TT = 64;     // tokens per tile (one ring stage)
 constexpr int AD_CW = 4;      // consumer warps; warp w takes tokens 16w..16w+15 of a tile
 constexpr int AD_THREADS = 32 * (AD_CW + 1);
 constexpr int AD_CSTRIDE = AD_D + 4;   // floats per row of the merge area
+// CTAs per SM the register allocation targets with at most 8 query heads per
+// KV head (a build option: -DTMW4_AD_MINB=n)
+#ifndef TMW4_AD_MINB
+#define TMW4_AD_MINB 2
+#endif
+constexpr int AD_SLOT = AD_D + 4;      // floats per workspace slot: O[128], m, l, pad (16-byte rows)
 
 template <int BITS>
 struct AdGeom {
@@ -80,51 +86,80 @@ __device__ __forceinline__ bool ad_unit(const AttnArgs &p, long long u, AdUnit &
   return true;
 }
 
-// 16-bit pairs from 8-bit codes: x holds (1024 + qa, 1024 + qb) (fp16 magic)
-// or the two codes in its low bytes (bf16).  Result T(s * (q - z)) per half,
-// one rounding each: fp16 subtracts exactly under the magic and multiplies
-// once; bf16 goes through fp32 (2^23 magic, exact subtract and product).
 template <bool BF16>
-__device__ __forceinline__ uint32_t kv8_pair(uint32_t qa, uint32_t qb, uint32_t zm, float za, float zb,
-                                             uint32_t s2, float sa, float sb) {
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
   if constexpr (BF16) {
-    const float a = (__uint_as_float(0x4B000000u | qa) - za) * sa;
-    const float b = (__uint_as_float(0x4B000000u | qb) - zb) * sb;
     const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&r);
   } else {
-    const uint32_t x = (qa | (qb << 16)) | 0x64006400u;
-    const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&x),
-                                      *reinterpret_cast<const __half2 *>(&zm)),
-                              *reinterpret_cast<const __half2 *>(&s2));
-    (void)za; (void)zb; (void)sa; (void)sb;
-    return *reinterpret_cast<const uint32_t *>(&v);
+    const __half2 r = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&r);
   }
 }
 
-// 16-bit pairs from 4-bit codes already in the low nibble of each half
-// (x = (qa | qb << 16), both <= 15): the exponent magic (fp16 1024 + q,
-// bf16 128 + q) is exact in either type, so is the subtract of (magic + z),
-// and the multiply by the scale is the one rounding.
-template <bool BF16>
-__device__ __forceinline__ uint32_t kv4_pair(uint32_t x, uint32_t zm, uint32_t s2) {
+// Cached codes become exact (q - z) values in 16 bits; the per-token scales
+// are applied to fp32 quantities instead: to the scores (S = s_t * sum_d
+// Q_d (q - z)) and to the probabilities that multiply the values
+// (P'_t = P_t * s_t, rounded once to 16 bits for the MMA).  With P = 1 (a
+// single token) the output is RNE(s * (q - z)) exactly, as in the
+// definition; otherwise it differs from dequantizing first only by rounding
+// (it skips the rounding of each s * (q - z) to 16 bits).
+//   fp16 codes: the byte under the exponent magic 0x6400 is 1024 + q
+//   exactly; minus (1024 + z) is exact.  bf16 8-bit codes: 2^23 + q in fp32,
+//   minus 2^23 + z, converted exactly (|q - z| <= 255 fits 8 bits).  4-bit
+//   codes: codes_minus_zero.
+constexpr uint32_t kMagic16 = 0x64646464u;
+
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t x, uint32_t zm) {
   uint32_t r;
-  if constexpr (BF16) {
-    x |= 0x43004300u;
-    asm("{\n\t.reg .b32 d;\n\t"
-        "sub.rn.bf16x2 d, %1, %2;\n\t"
-        "mul.rn.bf16x2 %0, d, %3;\n\t}"
-        : "=r"(r)
-        : "r"(x), "r"(zm), "r"(s2));
-  } else {
-    x |= 0x64006400u;
-    asm("{\n\t.reg .b32 d;\n\t"
-        "sub.rn.f16x2 d, %1, %2;\n\t"
-        "mul.rn.f16x2 %0, d, %3;\n\t}"
-        : "=r"(r)
-        : "r"(x), "r"(zm), "r"(s2));
-  }
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(zm));
   return r;
+}
+
+// fp32 value of byte e of w, exactly: 2^23 + byte
+__device__ __forceinline__ float byte_f32(uint32_t w, int e) {
+  return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | e));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One key word (four codes of one token): (q - z) pairs (e0, e1), (e2, e3).
+template <bool BF16>
+__device__ __forceinline__ void k8_diff(uint32_t w, uint32_t zm, float zf, uint32_t &p01, uint32_t &p23) {
+  if constexpr (BF16) {
+    (void)zm;
+    p01 = pack2<true>(byte_f32(w, 0) - zf, byte_f32(w, 1) - zf);
+    p23 = pack2<true>(byte_f32(w, 2) - zf, byte_f32(w, 3) - zf);
+  } else {
+    (void)zf;
+    p01 = sub_f16x2(__byte_perm(w, kMagic16, 0x4140), zm);
+    p23 = sub_f16x2(__byte_perm(w, kMagic16, 0x4342), zm);
+  }
+}
+
+// Two value words of tokens a and b (same four columns): p[e] = (column e
+// of a, column e of b) as (q - z), each with its own token's zero.
+template <bool BF16>
+__device__ __forceinline__ void v8_diff(uint32_t a, uint32_t b, uint32_t zm, float za, float zb,
+                                        uint32_t (&p)[4]) {
+  if constexpr (BF16) {
+    (void)zm;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[e] = pack2<true>(byte_f32(a, e) - za, byte_f32(b, e) - zb);
+  } else {
+    (void)za;
+    (void)zb;
+    const uint32_t t01 = __byte_perm(a, b, 0x5140);   // a.b0, b.b0, a.b1, b.b1
+    const uint32_t t23 = __byte_perm(a, b, 0x7362);   // a.b2, b.b2, a.b3, b.b3
+    p[0] = sub_f16x2(__byte_perm(t01, kMagic16, 0x4140), zm);
+    p[1] = sub_f16x2(__byte_perm(t01, kMagic16, 0x4342), zm);
+    p[2] = sub_f16x2(__byte_perm(t23, kMagic16, 0x4140), zm);
+    p[3] = sub_f16x2(__byte_perm(t23, kMagic16, 0x4342), zm);
+  }
 }
 
 // mma_16816 when rows 8..15 of A are zero (at most 8 query heads): those
@@ -159,15 +194,10 @@ __device__ __forceinline__ void mma_q(float (&d)[4], uint32_t a0, uint32_t a1, u
   }
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  if constexpr (BF16) {
-    const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&r);
-  } else {
-    const __half2 r = __floats2half2_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&r);
-  }
+// -(64 + za), -(64 + zb) as an fp16 pair (4-bit codes, fp16 only): exact.
+__device__ __forceinline__ uint32_t z16_pair(uint32_t za, uint32_t zb) {
+  const __half2 h = __floats2half2_rn(-(64.f + static_cast<float>(za)), -(64.f + static_cast<float>(zb)));
+  return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 // (magic + za, magic + zb) as a 16-bit pair: exact integers in either type.
@@ -181,7 +211,7 @@ __device__ __forceinline__ uint32_t zero_pair(uint32_t za, uint32_t zb) {
 }
 
 template <bool BF16, int BITS, bool HI>
-__global__ void __launch_bounds__(AD_THREADS)
+__global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
     attn_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                        const AttnArgs p) {
   using Gm = AdGeom<BITS>;
@@ -228,8 +258,8 @@ __global__ void __launch_bounds__(AD_THREADS)
         for (int tt = 0; tt < x.ntile; ++tt, ++i) {
           const int s = i % NS;
           if (i >= NS &&
-              !mbar_wait_bounded(empty + s, ((i / NS) & 1) ^ 1u, p.limit_ns, reinterpret_cast<volatile int *>(flags),
-                                 p.err, SITE_PRODUCER_EMPTY, i)) {
+              !mbar_wait_backoff(empty + s, ((i / NS) & 1) ^ 1u, p.limit_ns, reinterpret_cast<volatile int *>(flags),
+                                 p.err, SITE_PRODUCER_EMPTY, i, 256)) {
             ok = false;
             break;
           }
@@ -315,8 +345,14 @@ __global__ void __launch_bounds__(AD_THREADS)
     bool ok = true;
     for (int tt = 0; tt < x.ntile; ++tt, ++i) {
       const int s = i % NS;
-      if (!mbar_wait_all(full + s, (i / NS) & 1, p.limit_ns, reinterpret_cast<volatile int *>(flags), p.err,
-                         SITE_DQ_FULL, i)) {
+      bool got = mbar_try_wait(full + s, (i / NS) & 1);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        if (!got)
+          got = mbar_wait_backoff(full + s, (i / NS) & 1, p.limit_ns, reinterpret_cast<volatile int *>(flags), p.err,
+                                  SITE_DQ_FULL, i, 128);
+        got = __all_sync(0xFFFFFFFFu, got);
+      }
+      if (!got) {
         ok = false;
         ++i;
         break;
@@ -330,7 +366,12 @@ __global__ void __launch_bounds__(AD_THREADS)
       const int tb = 16 * warp;
       const int tok0 = x.t0 + tt * AD_TT + tb;   // sequence position of this warp's first token
 
-      // ---- S^T = Q K^T over this warp's 16 tokens (two n8 tiles)
+      // every token of this warp's slice is inside the sequence (all but
+      // the last tile of a unit): no masking
+      const bool full = tok0 + 16 <= x.len;
+
+      // ---- S^T = Q K^T over this warp's 16 tokens (two n8 tiles), on exact
+      // (q - z); B-fragment column g of n-tile j is token tb + 8j + g
       float sc[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -338,16 +379,15 @@ __global__ void __launch_bounds__(AD_THREADS)
         for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
       {
         uint32_t kw[2][8];
-        uint32_t kzm[2], ks2[2];
-        float kzf[2], ksf[2];
+        uint32_t kzm[2], kz16[2];
+        float kzf[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int r = tb + 8 * j + g;
-          const uint32_t z = skz[r], sbits = sks[r];
+          const uint32_t z = skz[r];
           kzm[j] = zero_pair<BF16, BITS>(z, z);
-          ks2[j] = sbits | (sbits << 16);
+          kz16[j] = (BITS == 4 && !BF16) ? z16_pair(z, z) : 0u;
           kzf[j] = __uint_as_float(0x4B000000u | z);
-          ksf[j] = bits16_to_f32<BF16>(sbits);
           if constexpr (BITS == 8) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -359,59 +399,89 @@ __global__ void __launch_bounds__(AD_THREADS)
             kw[j][0] = v.x; kw[j][1] = v.y; kw[j][2] = v.z; kw[j][3] = v.w;
           }
         }
+        if constexpr (BITS == 8) {
 #pragma unroll
-        for (int s8 = 0; s8 < 8; ++s8) {
+          for (int s8 = 0; s8 < 8; ++s8)
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            uint32_t b0, b1;
-            if constexpr (BITS == 8) {
-              const uint32_t w = kw[j][s8];
-              b0 = kv8_pair<BF16>(w & 0xFFu, (w >> 8) & 0xFFu, kzm[j], kzf[j], kzf[j], ks2[j], ksf[j], ksf[j]);
-              b1 = kv8_pair<BF16>((w >> 16) & 0xFFu, w >> 24, kzm[j], kzf[j], kzf[j], ks2[j], ksf[j], ksf[j]);
-            } else {
-              const uint32_t w = kw[j][s8 >> 1] >> (8 * (s8 & 1));
-              b0 = kv4_pair<BF16>(w & 0x000F000Fu, kzm[j], ks2[j]);
-              b1 = kv4_pair<BF16>((w >> 4) & 0x000F000Fu, kzm[j], ks2[j]);
+            for (int j = 0; j < 2; ++j) {
+              uint32_t b0, b1;
+              k8_diff<BF16>(kw[j][s8], kzm[j], kzf[j], b0, b1);
+              mma_q<BF16, HI>(sc[j], qa[s8][0], qb[s8][0], qa[s8][1], qb[s8][1], b0, b1);
             }
-            mma_q<BF16, HI>(sc[j], qa[s8][0], qb[s8][0], qa[s8][1], qb[s8][1], b0, b1);
-          }
+        } else {
+          // word m: pairs (8m, 8m+4), (8m+1, 8m+5) feed step 2m; (8m+2, 8m+6),
+          // (8m+3, 8m+7) step 2m + 1
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              uint32_t pr[4];
+              codes_minus_zero<BF16>(kw[j][m], kzm[j], kz16[j], pr);
+              mma_q<BF16, HI>(sc[j], qa[2 * m][0], qb[2 * m][0], qa[2 * m][1], qb[2 * m][1], pr[0], pr[1]);
+              mma_q<BF16, HI>(sc[j], qa[2 * m + 1][0], qb[2 * m + 1][0], qa[2 * m + 1][1], qb[2 * m + 1][1], pr[2],
+                              pr[3]);
+            }
         }
       }
 
-      // ---- mask, online softmax (rows g and g + 8 of this thread)
+      // ---- scale, mask, online softmax.  Score column e of n-tile j is token
+      // tb + 8j + 2t + (e & 1): its key and value scales are read as pairs.
+      constexpr int NR = HI ? 2 : 1;   // rows g (and g + 8 with more than 8 heads)
+      float kcs[2][2], vsc[2][2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t kp = *reinterpret_cast<const uint32_t *>(sks + tb + 8 * j + 2 * t);
+        const uint32_t vp = *reinterpret_cast<const uint32_t *>(svs + tb + 8 * j + 2 * t);
+        kcs[j][0] = bits16_to_f32<BF16>(kp & 0xFFFFu) * p.sm_scale_log2;
+        kcs[j][1] = bits16_to_f32<BF16>(kp >> 16) * p.sm_scale_log2;
+        vsc[j][0] = bits16_to_f32<BF16>(vp & 0xFFFFu);
+        vsc[j][1] = bits16_to_f32<BF16>(vp >> 16);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2 * NR; ++e) sc[j][e] *= kcs[j][e & 1];
+      if (!full) {
+        // a token past the length: score -inf and value scale 0, so that
+        // whatever the (unwritten) cache holds there contributes exactly 0
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool valid = tok0 + 8 * j + 2 * t + e < x.len;
+            if (!valid) {
+              sc[j][e] = NEG_INF;
+              if (HI) sc[j][e + 2] = NEG_INF;
+              vsc[j][e] = 0.f;
+            }
+          }
+      }
       float pmax[2] = {NEG_INF, NEG_INF};
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const bool valid = tok0 + 8 * j + 2 * t + (e & 1) < x.len;
-          sc[j][e] = valid ? sc[j][e] * p.sm_scale_log2 : NEG_INF;
-          pmax[e >> 1] = fmaxf(pmax[e >> 1], sc[j][e]);
-        }
+        for (int e = 0; e < 2 * NR; ++e) pmax[e >> 1] = fmaxf(pmax[e >> 1], sc[j][e]);
+      float corr[2] = {1.f, 1.f}, muse[2] = {0.f, 0.f};
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
+      for (int r = 0; r < NR; ++r) {
         pmax[r] = fmaxf(pmax[r], __shfl_xor_sync(0xFFFFFFFFu, pmax[r], 1));
         pmax[r] = fmaxf(pmax[r], __shfl_xor_sync(0xFFFFFFFFu, pmax[r], 2));
-      }
-      float corr[2], muse[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
         const float mnew = fmaxf(m_run[r], pmax[r]);
         muse[r] = mnew == NEG_INF ? 0.f : mnew;
-        corr[r] = exp2f(m_run[r] - muse[r]);
+        corr[r] = ex2(m_run[r] - muse[r]);
         m_run[r] = mnew;
       }
       float psum[2] = {0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sc[j][e] = exp2f(sc[j][e] - muse[e >> 1]);
+        for (int e = 0; e < 2 * NR; ++e) {
+          sc[j][e] = ex2(sc[j][e] - muse[e >> 1]);
           psum[e >> 1] += sc[j][e];
         }
 #pragma unroll
-      for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * corr[r] + psum[r];
-      if (__any_sync(0xFFFFFFFFu, corr[0] != 1.f || (HI && corr[1] != 1.f))) {
+      for (int r = 0; r < NR; ++r) l_run[r] = l_run[r] * corr[r] + psum[r];
+      if (__any_sync(0xFFFFFFFFu, corr[0] != 1.f || corr[1] != 1.f)) {
 #pragma unroll
         for (int jn = 0; jn < 16; ++jn) {
           o[jn][0] *= corr[0]; o[jn][1] *= corr[0];
@@ -420,32 +490,25 @@ __global__ void __launch_bounds__(AD_THREADS)
           }
         }
       }
-      const uint32_t pa0 = pack2<BF16>(sc[0][0], sc[0][1]);
-      const uint32_t pa2 = pack2<BF16>(sc[1][0], sc[1][1]);
-      const uint32_t pa1 = HI ? pack2<BF16>(sc[0][2], sc[0][3]) : 0u;
-      const uint32_t pa3 = HI ? pack2<BF16>(sc[1][2], sc[1][3]) : 0u;
+      // A fragments of P V: P'_t = P_t * s_t (value scale)
+      const uint32_t pa0 = pack2<BF16>(sc[0][0] * vsc[0][0], sc[0][1] * vsc[0][1]);
+      const uint32_t pa2 = pack2<BF16>(sc[1][0] * vsc[1][0], sc[1][1] * vsc[1][1]);
+      const uint32_t pa1 = HI ? pack2<BF16>(sc[0][2] * vsc[0][0], sc[0][3] * vsc[0][1]) : 0u;
+      const uint32_t pa3 = HI ? pack2<BF16>(sc[1][2] * vsc[1][0], sc[1][3] * vsc[1][1]) : 0u;
 
-      // ---- O += P V: B fragments pair tokens (2t, 2t+1) and (2t+8, 2t+9) of
-      // value column d = 16 g + jn
+      // ---- O += P' (q - z): B fragments pair tokens (2t, 2t+1) and
+      // (2t+8, 2t+9) of value column d = 16 g + jn
       {
-        uint32_t vzm[2], vs2[2];
-        float vzf[4], vsf[4];
+        uint32_t vzm[2], vz16[2];
+        float vzf[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = tb + 2 * t + (q & 1) + 8 * (q >> 1);
-          const bool valid = tok0 + 2 * t + (q & 1) + 8 * (q >> 1) < x.len;
-          vzf[q] = __uint_as_float(0x4B000000u | svz[r]);
-          // a token past the length gets scale 0: its value row is exactly 0
-          // whatever the (unwritten) cache holds there
-          const uint32_t sbits = valid ? svs[r] : 0u;
-          vsf[q] = bits16_to_f32<BF16>(sbits);
-          if ((q & 1) == 0) {
-            vzm[q >> 1] = svz[r];
-            vs2[q >> 1] = sbits;
-          } else {
-            vzm[q >> 1] = zero_pair<BF16, BITS>(vzm[q >> 1], svz[r]);
-            vs2[q >> 1] |= sbits << 16;
-          }
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t zz = *reinterpret_cast<const uint16_t *>(svz + tb + 8 * h2 + 2 * t);
+          const uint32_t za = zz & 0xFFu, zb = zz >> 8;
+          vzm[h2] = zero_pair<BF16, BITS>(za, zb);
+          vz16[h2] = (BITS == 4 && !BF16) ? z16_pair(za, zb) : 0u;
+          vzf[2 * h2] = __uint_as_float(0x4B000000u | za);
+          vzf[2 * h2 + 1] = __uint_as_float(0x4B000000u | zb);
         }
         if constexpr (BITS == 8) {
           uint4 vr[4];
@@ -456,16 +519,11 @@ __global__ void __launch_bounds__(AD_THREADS)
           }
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {
-            const uint32_t a0 = (&vr[0].x)[wi], a1 = (&vr[1].x)[wi];
-            const uint32_t c0 = (&vr[2].x)[wi], c1 = (&vr[3].x)[wi];
+            uint32_t b0[4], b1[4];
+            v8_diff<BF16>((&vr[0].x)[wi], (&vr[1].x)[wi], vzm[0], vzf[0], vzf[1], b0);
+            v8_diff<BF16>((&vr[2].x)[wi], (&vr[3].x)[wi], vzm[1], vzf[2], vzf[3], b1);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t b0 = kv8_pair<BF16>((a0 >> (8 * e)) & 0xFFu, (a1 >> (8 * e)) & 0xFFu, vzm[0], vzf[0],
-                                                 vzf[1], vs2[0], vsf[0], vsf[1]);
-              const uint32_t b1 = kv8_pair<BF16>((c0 >> (8 * e)) & 0xFFu, (c1 >> (8 * e)) & 0xFFu, vzm[1], vzf[2],
-                                                 vzf[3], vs2[1], vsf[2], vsf[3]);
-              mma_q<BF16, HI>(o[4 * wi + e], pa0, pa1, pa2, pa3, b0, b1);
-            }
+            for (int e = 0; e < 4; ++e) mma_q<BF16, HI>(o[4 * wi + e], pa0, pa1, pa2, pa3, b0[e], b1[e]);
           }
         } else {
           uint2 vr[4];
@@ -476,22 +534,17 @@ __global__ void __launch_bounds__(AD_THREADS)
           }
 #pragma unroll
           for (int wi = 0; wi < 2; ++wi) {
-            const uint32_t a0 = (&vr[0].x)[wi], a1 = (&vr[1].x)[wi];
-            const uint32_t c0 = (&vr[2].x)[wi], c1 = (&vr[3].x)[wi];
-            // byte k of a word holds value columns 2k (low nibble) and 2k + 1
-            // (high nibble).  xs = (a0.b_k, a0.b_k+1, a1.b_k, a1.b_k+1): its
-            // nibble at bit `sh` of each half is the (token 2t, token 2t + 1)
-            // pair of one column
+            // halves from the two tokens: (a.b0, a.b1 | b.b0, b.b1) holds
+            // columns 0..3 of both, (a.b2, a.b3 | b.b2, b.b3) columns 4..7
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-              const uint32_t xs = __byte_perm(a0, a1, which ? 0x7632 : 0x5410);
-              const uint32_t ys = __byte_perm(c0, c1, which ? 0x7632 : 0x5410);
+              const uint32_t sel = which ? 0x7632 : 0x5410;
+              uint32_t b0[4], b1[4];
+              codes_minus_zero<BF16>(__byte_perm((&vr[0].x)[wi], (&vr[1].x)[wi], sel), vzm[0], vz16[0], b0);
+              codes_minus_zero<BF16>(__byte_perm((&vr[2].x)[wi], (&vr[3].x)[wi], sel), vzm[1], vz16[1], b1);
 #pragma unroll
-              for (int sh = 0; sh < 16; sh += 4) {
-                const uint32_t b0 = kv4_pair<BF16>((xs >> sh) & 0x000F000Fu, vzm[0], vs2[0]);
-                const uint32_t b1 = kv4_pair<BF16>((ys >> sh) & 0x000F000Fu, vzm[1], vs2[1]);
-                mma_q<BF16, HI>(o[8 * wi + 4 * which + sh / 4], pa0, pa1, pa2, pa3, b0, b1);
-              }
+              for (int e = 0; e < 4; ++e)
+                mma_q<BF16, HI>(o[8 * wi + 4 * which + e], pa0, pa1, pa2, pa3, b0[e], b1[e]);
             }
           }
         }
@@ -525,7 +578,7 @@ __global__ void __launch_bounds__(AD_THREADS)
     const int d = ctid;                              // this thread's value column
     const int fo = (d & 15) * 8 + (d >> 4);          // its place in fragment order
     const bool whole = x.nch == 1;
-    float *wsO = p.ws + (static_cast<size_t>(bh) * p.n_chunks_max + x.c) * GQ * (AD_D + 2);
+    float *wsO = p.ws + (static_cast<size_t>(bh) * p.n_chunks_max + x.c) * GQ * AD_SLOT;
     for (int head = 0; head < GQ; ++head) {
       float mx = NEG_INF;
 #pragma unroll
@@ -540,7 +593,7 @@ __global__ void __launch_bounds__(AD_THREADS)
       if (whole) {
         reinterpret_cast<uint16_t *>(p.o)[(orow0 + head) * AD_D + d] = f32_to_bits16<BF16>(acc / l);
       } else {
-        float *slot = wsO + head * (AD_D + 2);
+        float *slot = wsO + head * AD_SLOT;
         slot[d] = acc;
         if (d == 0) {
           slot[AD_D] = mx;
@@ -560,18 +613,28 @@ __global__ void __launch_bounds__(AD_THREADS)
       }
       named_bar_sync(1, 32 * AD_CW);
       if (flags[1]) {
-        const float *base = p.ws + static_cast<size_t>(bh) * p.n_chunks_max * GQ * (AD_D + 2);
-        for (int head = 0; head < GQ; ++head) {
+        // warp w merges heads w, w + 4, ...: lane l owns value columns
+        // 4l..4l+3; the chunks are read with 16-byte loads, eight in flight
+        const float *base = p.ws + static_cast<size_t>(bh) * p.n_chunks_max * GQ * AD_SLOT;
+        for (int head = warp; head < GQ; head += AD_CW) {
           float mx = NEG_INF;
-          for (int c = 0; c < x.nch; ++c) mx = fmaxf(mx, __ldcg(base + (c * GQ + head) * (AD_D + 2) + AD_D));
-          float acc = 0.f, l = 0.f;
+#pragma unroll 8
+          for (int c = 0; c < x.nch; ++c) mx = fmaxf(mx, __ldcg(base + (c * GQ + head) * AD_SLOT + AD_D));
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          float l = 0.f;
+#pragma unroll 8
           for (int c = 0; c < x.nch; ++c) {
-            const float *slot = base + (c * GQ + head) * (AD_D + 2);
+            const float *slot = base + (c * GQ + head) * AD_SLOT;
             const float f = exp2f(__ldcg(slot + AD_D) - mx);
-            acc += f * __ldcg(slot + d);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(slot) + lane);
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
             l += f * __ldcg(slot + AD_D + 1);
           }
-          reinterpret_cast<uint16_t *>(p.o)[(orow0 + head) * AD_D + d] = f32_to_bits16<BF16>(acc / l);
+          const uint32_t lo = pack2<BF16>(acc.x / l, acc.y / l), hi = pack2<BF16>(acc.z / l, acc.w / l);
+          *reinterpret_cast<uint2 *>(p.o + (orow0 + head) * AD_D + 4 * lane) = make_uint2(lo, hi);
         }
       }
     }

@@ -59,7 +59,7 @@ struct GemmArgs {
 // Decode attention over a low-bit KV cache (attn_decode.cu).  q, o
 // [B][Hq][128]; cache rows [B][Hkv][L_max][128 * bits / 8] (K and V, through
 // the tensor maps); scales [B][Hkv][L_max] 16-bit; zeros [B][Hkv][L_max]
-// bytes; lens [B] (device).  ws holds one (O[128], m, l) fp32 slot per
+// bytes; lens [B] (device).  ws holds one 132-float slot (O[128], m, l) per
 // (sequence, KV head, chunk, query head of the group); counters one
 // self-resetting arrival count per (sequence, KV head).
 struct AttnArgs {

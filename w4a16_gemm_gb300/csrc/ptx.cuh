@@ -128,6 +128,39 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
+// Bounded wait that backs off with __nanosleep between polls (32 ns,
+// doubling up to max_sleep_ns), so that a waiting warp takes no issue slots
+// from the warps it shares a scheduler with.  For a producer whose ring is
+// full, or a consumer whose data is late; the other arguments and the
+// result are those of mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                                  volatile int *abort, unsigned int *err_word, unsigned site,
+                                                  unsigned step, unsigned max_sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  unsigned ns = 32;
+  while (true) {
+    __nanosleep(ns);
+    ns = ns * 2 < max_sleep_ns ? ns * 2 : max_sleep_ns;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (abort != nullptr) *abort = 1;
+      if (err_word != nullptr) {
+        atomicOr(err_word, TM_DEVERR_TIMEOUT);
+        if (atomicCAS(err_word + 1, 0u, 1u) == 0u) {
+          err_word[2] = site;
+          err_word[3] = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+          err_word[4] = threadIdx.x;
+          err_word[5] = step;
+          err_word[6] = parity;
+        }
+      }
+      return false;
+    }
+  }
+}
+
 // Warp-wide bounded wait: lane 0 waits (sleeping in hardware), the warp
 // agrees on the outcome, then every lane takes its own acquire with one
 // non-blocking test of the (now completed) phase.  Must be called by all 32
