@@ -976,26 +976,18 @@ tm_status tm_selftest_wait_timeout(long long limit_ns, void *stream) {
 }
 
 // ------------------------------------------------------ decode attention
-// 64-token tiles per unit of work, from the worst case (every sequence at
-// L_max): the smallest per-CTA time when U units are spread over the
-// resident grid, in tiles, counting half a tile of merge work per unit and,
-// for the last chunk to arrive, a sixteenth of a tile per chunk it merges.
+// 64-token tiles per unit of work (units are handed out dynamically, and
+// every unit of a split sequence costs a merge through global memory).
+// Measured on GB300 over batch 1..256 at the 8B-class layout: whole
+// sequences once there are at least 4 (sequence, KV head) pairs per
+// resident CTA; otherwise chunks of 16 tiles, or smaller (down to 4) when
+// that would leave resident CTAs idle.  Planned for every sequence at L_max.
 static int attn_chunk_tiles(int B, int Hkv, int tiles, int cap) {
-  int best = 1;
-  double best_cost = 1e300;
-  for (int ct = 1;; ct *= 2) {
-    const long long n_ch = (tiles + ct - 1) / ct;
-    const long long U = static_cast<long long>(B) * Hkv * n_ch;
-    const long long rounds = (U + cap - 1) / cap;
-    const double cost = static_cast<double>(rounds) * (std::min(ct, tiles) + 0.5) +
-                        (n_ch > 1 ? static_cast<double>(n_ch) / 16.0 : 0.0);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = std::min(ct, tiles);
-    }
-    if (ct >= tiles) break;
-  }
-  return best;
+  const long long pairs = static_cast<long long>(B) * Hkv;
+  if (pairs >= 4LL * cap) return tiles;
+  int ct = 16;
+  while (ct > 4 && pairs * ((tiles + ct - 1) / ct) < cap) ct /= 2;
+  return std::min(ct, tiles);
 }
 
 static tm_status encode_kv_map(const uint8_t *cache, long long rows, int row_bytes, CUtensorMap *map) {
@@ -1021,6 +1013,7 @@ tm_status tm_attn_decode(const void *q, const uint8_t *k_cache, const void *k_sc
   if (B < 0 || Hq < 1 || Hkv < 1) return fail(TM_ERR_INVALID_ARG, "B >= 0, Hq >= 1 and Hkv >= 1 required");
   if (Hq % Hkv != 0) return fail(TM_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
   if (Hq / Hkv > 16) return fail(TM_ERR_UNSUPPORTED, "at most 16 query heads per KV head");
+  if (B > kAttnMaxBatch) return fail(TM_ERR_UNSUPPORTED, "at most %d sequences per call", kAttnMaxBatch);
   if (head_dim != 128) return fail(TM_ERR_UNSUPPORTED, "head_dim must be 128");
   if (kv_bits != 4 && kv_bits != 8) return fail(TM_ERR_INVALID_ARG, "kv_bits must be 4 or 8");
   if (dtype != TM_F16 && dtype != TM_BF16) return fail(TM_ERR_INVALID_ARG, "dtype must be TM_F16 or TM_BF16");
@@ -1041,7 +1034,7 @@ tm_status tm_attn_decode(const void *q, const uint8_t *k_cache, const void *k_sc
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = dtype == TM_BF16;
   const int gq = Hq / Hkv;
-  const int occ = attn_decode_ctas_per_sm(bf16, kv_bits, gq);
+  const int occ = attn_decode_ctas_per_sm(bf16, kv_bits, gq, B);
   if (occ < 1) return fail(TM_ERR_CUDA, "decode attention kernel cannot be resident");
   const int cap = sm_count(dev) * occ;
   const int tiles = L_max / 64;
@@ -1068,10 +1061,12 @@ tm_status tm_attn_decode(const void *q, const uint8_t *k_cache, const void *k_sc
   a.sm_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
   a.limit_ns = wait_limit_ns();
   a.pdl = pdl_enabled() ? 1 : 0;
-  if (n_ch > 1) {
+  {
+    // partial slots when sequences are split; one arrival counter per
+    // (sequence, KV head) plus the two work-ticket counters
     Workspace *ws = nullptr;
-    const size_t floats = static_cast<size_t>(B) * Hkv * n_ch * gq * (128 + 4);
-    s = get_workspace(dev, st, sizeof(float) * floats, static_cast<size_t>(B) * Hkv, &ws);
+    const size_t floats = n_ch > 1 ? static_cast<size_t>(B) * Hkv * n_ch * gq * (128 + 4) : 0;
+    s = get_workspace(dev, st, sizeof(float) * floats, static_cast<size_t>(B) * Hkv + 2, &ws);
     if (s != TM_OK) return s;
     a.ws = ws->ws;
     a.counters = ws->counters;
@@ -1091,13 +1086,14 @@ tm_status tm_attn_decode(const void *q, const uint8_t *k_cache, const void *k_sc
 
 tm_status tm_attn_decode_plan(int B, int Hq, int Hkv, int L_max, int kv_bits, tm_dtype dtype, int *chunk_tiles,
                               int *grid) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > 16 || L_max < 64 || L_max % 64 != 0 ||
+  if (B < 1 || B > kAttnMaxBatch || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > 16 || L_max < 64 ||
+      L_max % 64 != 0 ||
       (kv_bits != 4 && kv_bits != 8))
     return fail(TM_ERR_INVALID_ARG, "invalid decode attention shape");
   int dev = -1;
   tm_status s = current_device(&dev);
   if (s != TM_OK) return s;
-  const int occ = attn_decode_ctas_per_sm(dtype == TM_BF16, kv_bits, Hq / Hkv);
+  const int occ = attn_decode_ctas_per_sm(dtype == TM_BF16, kv_bits, Hq / Hkv, B);
   if (occ < 1) return fail(TM_ERR_CUDA, "decode attention kernel cannot be resident");
   const int cap = sm_count(dev) * occ;
   const int tiles = L_max / 64;

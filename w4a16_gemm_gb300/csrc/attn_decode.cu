@@ -56,35 +56,21 @@ struct AdGeom {
   static constexpr int KV = AD_TT * ROW;                       // one K (or V) tile
   static constexpr int PRM = AD_TT * 2 * 2 + AD_TT * 2;        // ks, vs (16-bit), kz, vz (bytes)
   static constexpr int TX = 2 * KV + PRM;                      // bytes landing per stage
-  static constexpr int STAGE = ((TX + 1023) / 1024) * 1024;
+  static constexpr int META = 2 * KV + 512 - 128;              // 8 ints: the stage's unit and tile
+  static constexpr int QOFF = 2 * KV + 512;                    // a unit's queries (first tile only)
+  static constexpr int QMAX = 16 * AD_D * 2;                   // at most 16 query heads
+  static constexpr int STAGE = ((QOFF + QMAX + 1023) / 1024) * 1024;
   static constexpr int NS = BITS == 8 ? 3 : 5;                 // ring stages
   static constexpr int RING = NS * STAGE;
 };
 
-struct AdUnit {
-  int b, h, c, t0, ntile, nch, len;
+// What a ring stage holds (written by the producer before it arms the
+// stage's barrier, read by the consumers after it completes).
+struct AdMeta {
+  int b, h, c, tt;     // sequence, KV head, chunk, tile within the chunk
+  int ntile, nch;      // tiles of this unit (0: empty sequence), chunks of the sequence
+  int len, end;        // sequence length; end = 1: no more units
 };
-
-// Unit u of the walk: chunk-major over (chunk, sequence, KV head), so that a
-// stride of the persistent grid covers many sequences.  false: the chunk
-// lies past the sequence (nothing to do).  A sequence of length 0 keeps its
-// chunk 0 (with no tiles), which writes the zero output.
-__device__ __forceinline__ bool ad_unit(const AttnArgs &p, long long u, AdUnit &x) {
-  const long long bh = static_cast<long long>(p.B) * p.Hkv;
-  x.c = static_cast<int>(u / bh);
-  const int r = static_cast<int>(u % bh);
-  x.b = r / p.Hkv;
-  x.h = r % p.Hkv;
-  int len = __ldg(p.lens + x.b);
-  len = len < 0 ? 0 : (len > p.L_max ? p.L_max : len);
-  x.len = len;
-  const int ctok = p.chunk_tiles * AD_TT;
-  x.nch = len == 0 ? 1 : (len + ctok - 1) / ctok;
-  if (x.c >= x.nch) return false;
-  x.t0 = x.c * ctok;
-  x.ntile = len == 0 ? 0 : min(p.chunk_tiles, (len - x.t0 + AD_TT - 1) / AD_TT);
-  return true;
-}
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -224,7 +210,11 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
   float *cL = cM + AD_CW * GQ;                                          // [CW][GQ]
   uint64_t *full = reinterpret_cast<uint64_t *>(cL + AD_CW * GQ + 2);   // 536 GQ + 2 floats in: 8-byte aligned
   uint64_t *empty = full + NS;
-  volatile int *flags = reinterpret_cast<volatile int *>(empty + NS);   // abort, last arriver, exit
+  uint64_t *cbar = empty + NS;                                          // the consumer warps' barrier
+  volatile int *flags = reinterpret_cast<volatile int *>(cbar + 1);     // abort, last arriver
+  int *wsum = const_cast<int *>(flags) + 2;                             // [AD_CW + 1] warp totals
+  int *pref = wsum + AD_CW + 2;                                         // [B + 1] first unit of each sequence
+  int *slen = pref + p.B + 1;                                           // [B] clamped lengths
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < NS) {
@@ -232,82 +222,175 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
     mbar_init(empty + threadIdx.x, AD_CW);
   }
   if (threadIdx.x == 0) {
+    mbar_init(cbar, AD_CW);
     flags[0] = 0;
     flags[1] = 0;
-    flags[2] = 0;
     fence_mbar_init();
   }
   __syncthreads();
   pdl_launch_dependents();
-  // the lengths, queries and cache may come from the previous kernel
+  // the lengths, queries, cache and work tickets may come from the previous kernel
   pdl_wait();
+  volatile int *abort_flag = flags;
+  const int ctok = p.chunk_tiles * AD_TT;
+  unsigned int *ticket = p.counters + static_cast<size_t>(p.B) * p.Hkv;   // next unit; then CTAs finished
 
-  const long long U = static_cast<long long>(p.n_chunks_max) * p.B * p.Hkv;
+  // Units in sequence-major order (sequence b, then chunk, then KV head):
+  // sequence b's first unit pref[b], by a block-wide scan of its unit
+  // count Hkv * chunks(b) (a sequence of length 0 keeps one chunk, which
+  // writes its zero output).
+  {
+    const int per = (p.B + AD_THREADS - 1) / AD_THREADS;
+    const int b0 = min(p.B, static_cast<int>(threadIdx.x) * per), b1 = min(p.B, b0 + per);
+    auto units_of = [&](int len) { return p.Hkv * (len == 0 ? 1 : (len + ctok - 1) / ctok); };
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) {
+      int len = __ldg(p.lens + b);
+      len = len < 0 ? 0 : (len > p.L_max ? p.L_max : len);
+      slen[b] = len;
+      sum += units_of(len);
+    }
+    int x = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += wsum[w];
+    int run = base + x - sum;
+    for (int b = b0; b < b1; ++b) {
+      pref[b] = run;
+      run += units_of(slen[b]);
+    }
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int w = 0; w <= AD_CW; ++w) tot += wsum[w];
+      pref[p.B] = tot;
+    }
+    __syncthreads();
+  }
 
   if (warp == AD_CW) {
     // ------------------------------------------------------------ producer
+    // Units are handed out by a ticket counter, so that every CTA takes the
+    // next unit as soon as it has issued its last one.
     if (lane == 0) {
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
+      const int total = pref[p.B];
       int i = 0;
       bool ok = true;
-      for (long long u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        AdUnit x;
-        if (!ad_unit(p, u, x)) continue;
-        const long long row = (static_cast<long long>(x.b) * p.Hkv + x.h) * p.L_max + x.t0;
-        for (int tt = 0; tt < x.ntile; ++tt, ++i) {
-          const int s = i % NS;
-          if (i >= NS &&
-              !mbar_wait_backoff(empty + s, ((i / NS) & 1) ^ 1u, p.limit_ns, reinterpret_cast<volatile int *>(flags),
-                                 p.err, SITE_PRODUCER_EMPTY, i, 256)) {
+      unsigned int next = atomicAdd(ticket, 1u);
+      auto stage_free = [&](int idx) {
+        return idx < NS || mbar_wait_idle(empty + idx % NS, ((idx / NS) & 1) ^ 1u, p.limit_ns, abort_flag, p.err,
+                                          SITE_PRODUCER_EMPTY, idx, 256);
+      };
+      while (ok) {
+        if (next >= static_cast<unsigned>(total)) break;
+        const int u = static_cast<int>(next);
+        // the sequence of unit u: the last b with pref[b] <= u
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (pref[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        const int cb = lo, len_b = slen[cb];
+        const int nch_b = len_b == 0 ? 1 : (len_b + ctok - 1) / ctok;
+        const int r = u - pref[cb];
+        const int c = r / p.Hkv, h = r % p.Hkv;
+        const int t0 = c * ctok;
+        const int ntile = len_b == 0 ? 0 : min(p.chunk_tiles, (len_b - t0 + AD_TT - 1) / AD_TT);
+        const long long row = (static_cast<long long>(cb) * p.Hkv + h) * p.L_max + t0;
+        for (int tt = 0; tt < max(ntile, 1); ++tt, ++i) {
+          if (!stage_free(i)) {
             ok = false;
             break;
           }
+          const int s = i % NS;
           uint8_t *st = ring + s * Gm::STAGE;
-          const long long r = row + static_cast<long long>(tt) * AD_TT;
-          mbar_arrive_expect_tx(full + s, Gm::TX);
-          tma_load_2d(st, &kmap, 0, static_cast<int32_t>(r), full + s);
-          tma_load_2d(st + Gm::KV, &vmap, 0, static_cast<int32_t>(r), full + s);
-          tma_bulk_g2s(st + 2 * Gm::KV, p.k_scale + r, AD_TT * 2, full + s);
-          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 2, p.v_scale + r, AD_TT * 2, full + s);
-          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 4, p.k_zero + r, AD_TT, full + s);
-          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 5, p.v_zero + r, AD_TT, full + s);
+          AdMeta *m = reinterpret_cast<AdMeta *>(st + Gm::META);
+          m->b = cb; m->h = h; m->c = c; m->tt = tt;
+          m->ntile = ntile; m->nch = nch_b; m->len = len_b; m->end = 0;
+          if (ntile == 0) {
+            mbar_arrive(full + s);   // no data: the consumers write the zero output
+            continue;
+          }
+          const long long rr = row + static_cast<long long>(tt) * AD_TT;
+          const int qbytes = tt == 0 ? GQ * AD_D * 2 : 0;
+          mbar_arrive_expect_tx(full + s, Gm::TX + qbytes);
+          tma_load_2d(st, &kmap, 0, static_cast<int32_t>(rr), full + s);
+          tma_load_2d(st + Gm::KV, &vmap, 0, static_cast<int32_t>(rr), full + s);
+          tma_bulk_g2s(st + 2 * Gm::KV, p.k_scale + rr, AD_TT * 2, full + s);
+          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 2, p.v_scale + rr, AD_TT * 2, full + s);
+          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 4, p.k_zero + rr, AD_TT, full + s);
+          tma_bulk_g2s(st + 2 * Gm::KV + AD_TT * 5, p.v_zero + rr, AD_TT, full + s);
+          if (qbytes)
+            tma_bulk_g2s(st + Gm::QOFF, p.q + (static_cast<size_t>(cb) * p.Hq + static_cast<size_t>(h) * GQ) * AD_D,
+                         qbytes, full + s);
         }
+        // the next ticket once this unit is issued (not earlier: a CTA that
+        // held a second ticket while others had none would run two units)
+        next = atomicAdd(ticket, 1u);
+      }
+      // the end marker
+      if (ok && stage_free(i)) {
+        const int s = i % NS;
+        reinterpret_cast<AdMeta *>(ring + s * Gm::STAGE + Gm::META)->end = 1;
+        mbar_arrive(full + s);
+        ++i;
       }
       // every copy issued must land before the CTA exits
       for (int j = max(0, i - NS); j < i; ++j)
         mbar_wait_bounded(full + j % NS, (j / NS) & 1, p.limit_ns, nullptr, p.err, SITE_DRAIN_TMA, j);
     }
-    return;
-  }
-
+  } else {
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
   const int ctid = threadIdx.x;   // 0..127
   const float NEG_INF = -__int_as_float(0x7F800000);
-  int i = 0;
-  for (long long u = blockIdx.x; u < U; u += gridDim.x) {
-    AdUnit x;
-    if (!ad_unit(p, u, x)) continue;
+  uint32_t cphase = 0;
+  // barrier of the four consumer warps (an mbarrier, so that its wait is
+  // bounded like every other)
+  auto cbar_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cbar);
+    const bool okb = mbar_wait_all_idle(cbar, cphase, p.limit_ns, abort_flag, p.err, SITE_DQ_AEMPTY, 0, 64);
+    cphase ^= 1u;
+    return okb;
+  };
+  uint32_t qa[8][2], qb[8][2];
+  float m_run[2], l_run[2];
+  float o[16][4];
+  for (int i = 0;; ++i) {
+    const int s = i % NS;
+    if (!mbar_wait_all_idle(full + s, (i / NS) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL, i, 128)) break;
+    const uint8_t *st = ring + s * Gm::STAGE;
+    const AdMeta x = *reinterpret_cast<const AdMeta *>(st + Gm::META);
+    if (x.end) break;
     const long long bh = static_cast<long long>(x.b) * p.Hkv + x.h;
     const size_t orow0 = (static_cast<size_t>(x.b) * p.Hq + static_cast<size_t>(x.h) * GQ);
     if (x.ntile == 0) {
       // empty sequence: zero output
       for (int e = ctid; e < GQ * AD_D; e += 32 * AD_CW) p.o[orow0 * AD_D + e] = 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
       continue;
     }
-
-    // Q fragments.  Thread t's head-dimension range is [32t, 32t + 32); the
-    // order inside it matches the B fragments built from the key rows below.
-    uint32_t qa[8][2], qb[8][2];
-    {
+    if (x.tt == 0) {
+      // a new unit: Q fragments from the stage (thread t's head-dimension
+      // range is [32t, 32t + 32); the order inside it matches the B
+      // fragments built from the key rows below), fresh softmax state
+      const uint16_t *sq = reinterpret_cast<const uint16_t *>(st + Gm::QOFF);
       uint32_t h0[16], h1[16];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int head = g + 8 * r;
         uint32_t *hv = r == 0 ? h0 : h1;
         if ((r == 0 || HI) && head < GQ) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (orow0 + head) * AD_D + 32 * t);
+          const uint4 *src = reinterpret_cast<const uint4 *>(sq + head * AD_D + 32 * t);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint4 v = src[k];
@@ -319,52 +402,35 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
         }
       }
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
+      for (int k = 0; k < 8; ++k) {
         if constexpr (BITS == 8) {
-          // step s: elements 4s, 4s+1 | 4s+2, 4s+3
-          qa[s][0] = h0[2 * s]; qa[s][1] = h0[2 * s + 1];
-          qb[s][0] = h1[2 * s]; qb[s][1] = h1[2 * s + 1];
+          // step k: elements 4k, 4k+1 | 4k+2, 4k+3
+          qa[k][0] = h0[2 * k]; qa[k][1] = h0[2 * k + 1];
+          qb[k][0] = h1[2 * k]; qb[k][1] = h1[2 * k + 1];
         } else {
           // step 2m + r: elements (8m + 2r, 8m + 2r + 4) | (8m + 2r + 1, 8m + 2r + 5)
-          const int m = s >> 1, r = s & 1;
+          const int m = k >> 1, r = k & 1;
           const uint32_t lo0 = h0[4 * m + r], hi0 = h0[4 * m + 2 + r];
           const uint32_t lo1 = h1[4 * m + r], hi1 = h1[4 * m + 2 + r];
-          qa[s][0] = __byte_perm(lo0, hi0, 0x5410); qa[s][1] = __byte_perm(lo0, hi0, 0x7632);
-          qb[s][0] = __byte_perm(lo1, hi1, 0x5410); qb[s][1] = __byte_perm(lo1, hi1, 0x7632);
+          qa[k][0] = __byte_perm(lo0, hi0, 0x5410); qa[k][1] = __byte_perm(lo0, hi0, 0x7632);
+          qb[k][0] = __byte_perm(lo1, hi1, 0x5410); qb[k][1] = __byte_perm(lo1, hi1, 0x7632);
         }
       }
+      m_run[0] = m_run[1] = NEG_INF;
+      l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
     }
-
-    float m_run[2] = {NEG_INF, NEG_INF}, l_run[2] = {0.f, 0.f};
-    float o[16][4];
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
-
-    bool ok = true;
-    for (int tt = 0; tt < x.ntile; ++tt, ++i) {
-      const int s = i % NS;
-      bool got = mbar_try_wait(full + s, (i / NS) & 1);
-      if (!__all_sync(0xFFFFFFFFu, got)) {
-        if (!got)
-          got = mbar_wait_backoff(full + s, (i / NS) & 1, p.limit_ns, reinterpret_cast<volatile int *>(flags), p.err,
-                                  SITE_DQ_FULL, i, 128);
-        got = __all_sync(0xFFFFFFFFu, got);
-      }
-      if (!got) {
-        ok = false;
-        ++i;
-        break;
-      }
-      const uint8_t *st = ring + s * Gm::STAGE;
+    {
       const uint8_t *sK = st, *sV = st + Gm::KV;
       const uint16_t *sks = reinterpret_cast<const uint16_t *>(st + 2 * Gm::KV);
       const uint16_t *svs = sks + AD_TT;
       const uint8_t *skz = st + 2 * Gm::KV + AD_TT * 4;
       const uint8_t *svz = skz + AD_TT;
       const int tb = 16 * warp;
-      const int tok0 = x.t0 + tt * AD_TT + tb;   // sequence position of this warp's first token
+      const int tok0 = x.c * ctok + x.tt * AD_TT + tb;   // sequence position of this warp's first token
 
       // every token of this warp's slice is inside the sequence (all but
       // the last tile of a unit): no masking
@@ -549,11 +615,12 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty + s);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + s);
+    if (x.tt != x.ntile - 1) continue;
 
-    // ---- merge the four warps
+    // ---- the unit's last tile: merge the four warps
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       l_run[r] += __shfl_xor_sync(0xFFFFFFFFu, l_run[r], 1);
@@ -574,7 +641,7 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
         }
       }
     }
-    named_bar_sync(1, 32 * AD_CW);
+    if (!cbar_sync()) break;
     const int d = ctid;                              // this thread's value column
     const int fo = (d & 15) * 8 + (d >> 4);          // its place in fragment order
     const bool whole = x.nch == 1;
@@ -586,7 +653,7 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
       float acc = 0.f, l = 0.f;
 #pragma unroll
       for (int w = 0; w < AD_CW; ++w) {
-        const float f = exp2f(cM[w * GQ + head] - mx);
+        const float f = ex2(cM[w * GQ + head] - mx);
         acc += f * cO[(w * GQ + head) * AD_CSTRIDE + fo];
         l += f * cL[w * GQ + head];
       }
@@ -604,14 +671,14 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
     if (!whole) {
       // publish, count; the last chunk of (b, h) to arrive merges in order
       __threadfence();
-      named_bar_sync(1, 32 * AD_CW);
+      if (!cbar_sync()) break;
       if (ctid == 0) {
         const unsigned old = atomic_add_acq_rel_gpu(p.counters + bh, 1u);
         const bool last = old == static_cast<unsigned>(x.nch - 1);
         if (last) p.counters[bh] = 0;   // self-resetting for the next launch
         flags[1] = last ? 1 : 0;
       }
-      named_bar_sync(1, 32 * AD_CW);
+      if (!cbar_sync()) break;
       if (flags[1]) {
         // warp w merges heads w, w + 4, ...: lane l owns value columns
         // 4l..4l+3; the chunks are read with 16-byte loads, eight in flight
@@ -625,7 +692,7 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
 #pragma unroll 8
           for (int c = 0; c < x.nch; ++c) {
             const float *slot = base + (c * GQ + head) * AD_SLOT;
-            const float f = exp2f(__ldcg(slot + AD_D) - mx);
+            const float f = ex2(__ldcg(slot + AD_D) - mx);
             const float4 v = __ldcg(reinterpret_cast<const float4 *>(slot) + lane);
             acc.x += f * v.x;
             acc.y += f * v.y;
@@ -638,51 +705,59 @@ __global__ void __launch_bounds__(AD_THREADS, HI ? 1 : TMW4_AD_MINB)
         }
       }
     }
-    // the merge area is rewritten by the next unit; the exit decision is
-    // taken from one copy of the abort flag so that every consumer warp
-    // leaves together (the named barriers above need all four)
-    if (ctid == 0) flags[2] = flags[0];
-    named_bar_sync(1, 32 * AD_CW);
-    (void)ok;
-    if (flags[2]) break;
+    // the merge area and the arrival flag are rewritten by the next unit
+    if (!cbar_sync()) break;
+  }
+  }
+  // the last CTA to finish resets the work tickets for the next launch (every
+  // producer has taken its last ticket before its CTA gets here)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned done = atomic_add_acq_rel_gpu(ticket + 1, 1u);
+    if (done == gridDim.x - 1) {
+      ticket[0] = 0;
+      ticket[1] = 0;
+    }
   }
 }
 
 }  // namespace
 
-size_t attn_decode_smem_bytes(int bits, int gq) {
+size_t attn_decode_smem_bytes(int bits, int gq, int B) {
   const int ring = bits == 8 ? AdGeom<8>::RING : AdGeom<4>::RING;
   const size_t merge = sizeof(float) * (static_cast<size_t>(AD_CW) * gq * AD_CSTRIDE + 2 * AD_CW * gq + 2);
   const int ns = bits == 8 ? AdGeom<8>::NS : AdGeom<4>::NS;
-  return 1024 + ring + merge + 16 * ns + 16;
+  // barriers, flags, warp totals, unit prefix and lengths
+  return 1024 + ring + merge + 16 * ns + 16 + sizeof(int) * (AD_CW + 2 + 2 * static_cast<size_t>(B) + 1);
 }
 
 template <bool BF16, int BITS, bool HI>
 static cudaError_t launch_ad_t(const CUtensorMap &km, const CUtensorMap &vm, const AttnArgs &a, int grid,
                                cudaStream_t st) {
   auto kern = attn_decode_kernel<BF16, BITS, HI>;
-  const size_t smem = attn_decode_smem_bytes(BITS, a.Hq / a.Hkv);
-  cudaError_t e = smem_optin<attn_decode_kernel<BF16, BITS, HI>>(static_cast<int>(attn_decode_smem_bytes(BITS, 16)));
+  const size_t smem = attn_decode_smem_bytes(BITS, a.Hq / a.Hkv, a.B);
+  cudaError_t e = smem_optin<attn_decode_kernel<BF16, BITS, HI>>(
+      static_cast<int>(attn_decode_smem_bytes(BITS, 16, kAttnMaxBatch)));
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(grid), dim3(AD_THREADS), smem, st, a.pdl != 0, km, vm, a);
 }
 
 template <bool BF16, int BITS, bool HI>
-static int ad_occ_t(int gq) {
+static int ad_occ_t(int gq, int batch) {
   int n = 0;
-  if (smem_optin<attn_decode_kernel<BF16, BITS, HI>>(static_cast<int>(attn_decode_smem_bytes(BITS, 16))) !=
-      cudaSuccess)
+  if (smem_optin<attn_decode_kernel<BF16, BITS, HI>>(
+          static_cast<int>(attn_decode_smem_bytes(BITS, 16, kAttnMaxBatch))) != cudaSuccess)
     return 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<BF16, BITS, HI>, AD_THREADS,
-                                                    attn_decode_smem_bytes(BITS, gq)) != cudaSuccess)
+                                                    attn_decode_smem_bytes(BITS, gq, batch)) != cudaSuccess)
     return 0;
   return n;
 }
 
-int attn_decode_ctas_per_sm(bool bf16, int bits, int gq) {
+int attn_decode_ctas_per_sm(bool bf16, int bits, int gq, int batch) {
   const bool hi = gq > 8;
 #define AD_OCC(B, W, H) \
-  if (bf16 == B && bits == W && hi == H) return ad_occ_t<B, W, H>(gq);
+  if (bf16 == B && bits == W && hi == H) return ad_occ_t<B, W, H>(gq, batch);
   AD_OCC(false, 8, false) AD_OCC(false, 8, true) AD_OCC(false, 4, false) AD_OCC(false, 4, true)
   AD_OCC(true, 8, false) AD_OCC(true, 8, true) AD_OCC(true, 4, false) AD_OCC(true, 4, true)
 #undef AD_OCC

@@ -244,8 +244,8 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? 4 : KG == 2 ? 2 : 1)
       int issued = nfirst;
       for (int i = nfirst; i < nb; ++i) {
         // stage i % D is free once the consumers have read block i - D
-        if (!mbar_wait_bounded(empty_bar + i % D, ((i / D) & 1) ^ 1u, p.limit_ns, abort_flag, p.err,
-                               SITE_PRODUCER_EMPTY, i))
+        if (!mbar_wait_idle(empty_bar + i % D, ((i / D) & 1) ^ 1u, p.limit_ns, abort_flag, p.err,
+                            SITE_PRODUCER_EMPTY, i))
           break;
         copy_weights(i);
         copy_acts(i, kb);
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? 4 : KG == 2 ? 2 : 1)
       for (int u = 0; u < GS; ++u) {
         const int ib = ig + u;
         const int sidx = ib % D;
-        if (!mbar_wait_all(full_bar + sidx, (ib / D) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL, ib)) {
+        if (!mbar_wait_all_idle(full_bar + sidx, (ib / D) & 1, p.limit_ns, abort_flag, p.err, SITE_DQ_FULL, ib)) {
           ok = false;
           break;
         }

@@ -80,8 +80,9 @@ struct AttnArgs {
   unsigned long long limit_ns;
   int pdl;
 };
-size_t attn_decode_smem_bytes(int bits, int gq);
-int attn_decode_ctas_per_sm(bool bf16, int bits, int gq);
+constexpr int kAttnMaxBatch = 4096;   // sequences per call (the unit scan lives in shared memory)
+size_t attn_decode_smem_bytes(int bits, int gq, int B);
+int attn_decode_ctas_per_sm(bool bf16, int bits, int gq, int B);
 cudaError_t launch_attn_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a, bool bf16,
                                int bits, int grid, cudaStream_t st);
 

@@ -161,6 +161,38 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity
   }
 }
 
+// Waits of a thread (or warp) with nothing else to do meanwhile: a TMA
+// producer whose ring is full, or a consumer whose data has not landed.
+// With TMW4_WAIT_BACKOFF (the default) they back off with __nanosleep
+// (mbar_wait_backoff); built with -DTMW4_WAIT_BACKOFF=0 they poll with
+// try_wait like mbar_wait_bounded.  A polling waiter issues an instruction
+// every few tens of cycles, taken from the warps that share its scheduler.
+#ifndef TMW4_WAIT_BACKOFF
+#define TMW4_WAIT_BACKOFF 1
+#endif
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                               volatile int *abort, unsigned int *err_word, unsigned site,
+                                               unsigned step, unsigned max_sleep_ns = 256) {
+#if TMW4_WAIT_BACKOFF
+  return mbar_wait_backoff(bar, parity, limit_ns, abort, err_word, site, step, max_sleep_ns);
+#else
+  (void)max_sleep_ns;
+  return mbar_wait_bounded(bar, parity, limit_ns, abort, err_word, site, step);
+#endif
+}
+
+// Warp-wide form (all 32 lanes call it; the result is warp-uniform): one
+// poll and one vote when the phase is already complete, else every lane
+// that saw it incomplete waits as mbar_wait_idle does.
+__device__ __forceinline__ bool mbar_wait_all_idle(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                                   volatile int *abort, unsigned int *err_word, unsigned site,
+                                                   unsigned step, unsigned max_sleep_ns = 128) {
+  bool ok = mbar_try_wait(bar, parity);
+  if (__all_sync(0xFFFFFFFFu, ok)) return true;
+  if (!ok) ok = mbar_wait_idle(bar, parity, limit_ns, abort, err_word, site, step, max_sleep_ns);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // Warp-wide bounded wait: lane 0 waits (sleeping in hardware), the warp
 // agrees on the outcome, then every lane takes its own acquire with one
 // non-blocking test of the (now completed) phase.  Must be called by all 32

@@ -244,8 +244,8 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
       UnitPos pos = pos0;
       for (int j = 0; j < nloc; ++j, pos.step(1, S, NT)) {
         const int s = j % WST;
-        if (j >= WST && !mbar_wait_bounded(wempty_bar + s, ((j / WST) & 1) ^ 1u, p.limit_ns,
-                                           abort_flag, p.err, SITE_PRODUCER_EMPTY, j, TMW4_SPIN(0)))
+        if (j >= WST && !mbar_wait_idle(wempty_bar + s, ((j / WST) & 1) ^ 1u, p.limit_ns,
+                                        abort_flag, p.err, SITE_PRODUCER_EMPTY, j))
           break;
         const int nt = pos.nt;
         const int kbf = pos.s * WKB;
@@ -283,8 +283,8 @@ __global__ void __launch_bounds__(dec_threads(DQ_WG), 1)
       for (int j = 0; j < nloc; ++j, pos.step(1, S, NT)) {
         const int cs = j / DQ_WG;                        // j is stage cs of warpgroup j % DQ_WG
         const int s = (j % DQ_WG) * ASW + cs % ASW;
-        if (cs >= ASW && !mbar_wait_bounded(aempty_bar + s, ((cs / ASW) & 1) ^ 1u, p.limit_ns,
-                                            abort_flag, p.err, SITE_PRODUCER_EMPTY, j, TMW4_SPIN(1)))
+        if (cs >= ASW && !mbar_wait_idle(aempty_bar + s, ((cs / ASW) & 1) ^ 1u, p.limit_ns,
+                                         abort_flag, p.err, SITE_PRODUCER_EMPTY, j))
           break;
         const int mt = pos.mt;
         const int kbf = pos.s * WKB;

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(64 + 128 * DQ_WG, 1)
         const int s = j % STAGES;
         const uint32_t ph = (j / STAGES) & 1;
         if (j >= STAGES &&
-            !mbar_wait_bounded(empty_bar + s, ph ^ 1u, p.limit_ns, abort_flag, p.err, SITE_PRODUCER_EMPTY, j))
+            !mbar_wait_idle(empty_bar + s, ph ^ 1u, p.limit_ns, abort_flag, p.err, SITE_PRODUCER_EMPTY, j))
           break;
         const int kbf = kb0 + j * KBS;
         const int nb = min(KBS, nkb - j * KBS);
