@@ -125,10 +125,12 @@ def recorded_traffic(ent: dict, source_hash: str, ran: list) -> int | None:
     return round(sum(got) / len(got))
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files: list | None = None) -> str:
+    """Hash of the kernel sources under csrc/: the named files (a kernel's own
+    translation unit and the headers it includes), else every file."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a16_gemm_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files else os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -799,7 +801,7 @@ def run_ours(args, rank: int, world: int):
         if os.path.exists(tp):
             with open(tp) as f:
                 ent = json.load(f).get(WORKLOAD, {})
-            traffic = recorded_traffic(ent, kernel_source_hash(), ran)
+            traffic = recorded_traffic(ent, kernel_source_hash(ent.get("source_files")), ran)
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "kernel": dom, "problems": n_l, "avg_launch_us": round(tot_s / n_l * 1e6, 3),
