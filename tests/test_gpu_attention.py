@@ -153,3 +153,60 @@ def test_argument_checks():
         binding.attn_decode(**d, kv_bits=8, sm_scale=float("inf"))
     plan = binding.attn_decode_plan(16, 32, 8, 8192, 8)
     assert plan["chunk_tiles"] >= 1 and plan["grid"] >= 1
+
+
+def test_chain_with_gemms_back_to_back():
+    """A GEMM writes the queries, the attention reads them and writes O, a
+    second GEMM reads O: programmatic dependent launches in one stream with
+    no synchronization between, eager and replayed from a CUDA graph."""
+    from tests._util import bits_of, c_values, packed_from
+
+    B, Hq, Hkv = 4, 8, 2
+    p = synth.kv_problem(30, B=B, Hq=Hq, Hkv=Hkv, D=128, lens=[300, 64, 1, 129], L_max=320)
+    qw1, x = synth.random_problem(44, B, 256, Hq * 128, 128, "f16")
+    qw2, _ = synth.random_problem(45, 1, Hq * 128, 256, 128, "f16")
+    w1 = oracle.dequant_bits(qw1.q, qw1.scales, qw1.zeros, 128, "f16")
+    w2 = oracle.dequant_bits(qw2.q, qw2.scales, qw2.zeros, 128, "f16")
+    W1, W2 = packed_from(qw1), packed_from(qw2)
+    d = _dev(p)
+    del d["q"]
+    X = binding.acts_to_device(x, torch.float16)
+    Qb = torch.empty((B, Hq * 128), dtype=torch.float16, device="cuda")
+    O = torch.empty((B, Hq, 128), dtype=torch.float16, device="cuda")
+    Y = torch.empty((B, 256), dtype=torch.float16, device="cuda")
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+
+    def run():
+        binding.gemm(X, W1, out=Qb, stream=st)
+        binding.attn_decode(Qb.view(B, Hq, 128), **d, kv_bits=8, sm_scale=p.sm_scale, out=O, stream=st)
+        binding.gemm(O.view(B, Hq * 128), W2, out=Y, stream=st)
+
+    def check(what):
+        assert oracle.max_err_ratio(c_values(Qb), oracle.gemm_ref(x, w1, "f16")) <= 1.0, what
+        o_ref = at.attn_decode_ref(bits_of(Qb).reshape(B, Hq, 128), p.k_codes, p.k_scale, p.k_zero, p.v_codes,
+                                   p.v_scale, p.v_zero, p.lens, 8, "f16", p.sm_scale)
+        _check(_vals(O, "f16"), o_ref)
+        y_ref = oracle.gemm_ref(bits_of(O.view(B, Hq * 128)), w2, "f16")
+        assert oracle.max_err_ratio(c_values(Y), y_ref) <= 1.0, what
+
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            Qb.fill_(float("nan"))
+            O.fill_(float("nan"))
+            run()
+    st.synchronize()
+    binding.poll_error(st)
+    check("eager")
+    with torch.cuda.stream(st):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            Qb.fill_(float("nan"))
+            O.fill_(float("nan"))
+            run()
+        Y.fill_(float("nan"))
+        g.replay()
+        g.replay()
+    st.synchronize()
+    binding.poll_error(st)
+    check("graph")

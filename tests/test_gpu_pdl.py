@@ -27,9 +27,13 @@ FAMILIES = {
     "gemv": dict(kernel="gemv", split_k=2),
     "tc_decode": dict(kernel="tc_decode", block_m=16, dq_warps=8),
     "tc": dict(kernel="tc", block_m=16, split_k=4, dq_warps=8),
+    "dm_cluster": dict(kernel="decode_mma", block_m=8, split_k=2, dq_warps=1),
+    "dm_streamk": dict(kernel="decode_mma", block_m=8, split_k=0, dq_warps=4),
 }
 PAIRS = [("gemv", "gemv"), ("tc_decode", "tc_decode"), ("tc", "tc"), ("gemv", "tc_decode"),
-         ("tc_decode", "gemv"), ("tc", "tc_decode"), ("tc_decode", "tc")]
+         ("tc_decode", "gemv"), ("tc", "tc_decode"), ("tc_decode", "tc"), ("dm_cluster", "dm_cluster"),
+         ("dm_streamk", "dm_streamk"), ("dm_cluster", "dm_streamk"), ("dm_streamk", "tc"),
+         ("tc", "dm_cluster"), ("gemv", "dm_streamk")]
 
 
 @pytest.fixture(scope="module")
@@ -81,3 +85,27 @@ def test_back_to_back_chain(chain, first, second):
     binding.poll_error(st)
     _check(Y, X, a_bits, w1, w2, (first, second, "graph"))
     assert np.isfinite(c_values(X)).all()
+
+
+@pytest.mark.parametrize("family", sorted(FAMILIES))
+def test_pack_then_gemm_on_the_same_stream(family):
+    """The kernels request the packed weights before waiting for the previous
+    kernel: a GEMM launched right after the repack that writes its weights,
+    on the same stream and with no synchronization between, must still see
+    them complete."""
+    qw, a = synth.random_problem(43, M, K1, N1, 128, "f16")
+    w = oracle.dequant_bits(qw.q, qw.scales, qw.zeros, 128, "f16")
+    p = binding.to_device(qw)
+    A = binding.acts_to_device(a, torch.float16)
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    for _ in range(3):
+        W = binding.pack(p.q, p.scales, p.zeros, qw.group, stream=st)
+        C = torch.empty((M, N1), dtype=torch.float16, device="cuda")
+        with torch.cuda.stream(st):
+            binding.gemm(A, W, out=C, config=FAMILIES[family], stream=st)
+        st.synchronize()
+        binding.poll_error(st)
+        assert oracle.max_err_ratio(c_values(C), oracle.gemm_ref(a, w, "f16"), rel=TOL) <= 1.0
+        W.free(stream=st)
+        st.synchronize()
