@@ -481,6 +481,14 @@ static tm_config select_config(const tm_packed *W, int M, int dev) {
   return default_config(W, M, dev);
 }
 
+// Launched (plainly) after the kernels of a repack.  A GEMM that follows on
+// the same stream is launched with programmatic dependent launch and reads
+// its packed weights before griddepcontrol.wait, so it may overlap the
+// kernel just before it; with this empty kernel in between, that kernel is
+// never the repack, whose writes are complete and visible by plain stream
+// order before this one starts.
+static __global__ void pack_fence_kernel() {}
+
 #ifdef TMW4_TRACE
 // debug builds only: device buffer that receives the per-stage cycle stamps
 static long long *g_trace = nullptr;
@@ -739,6 +747,10 @@ static tm_status pack_common(int src, const void *q, const void *scales, const v
   if (e == cudaSuccess)
     e = launch_pack_scales(static_cast<const uint16_t *>(scales), W->scales, K / G, N, rep, st);
   if (e == cudaSuccess && zeros) e = launch_pack_zeros(zeros, W->zeros, K / G, N, rep, src, zero_offset, err, st);
+  if (e == cudaSuccess) {
+    pack_fence_kernel<<<1, 1, 0, st>>>();
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) {
     if (W->qw) cudaFreeAsync(W->qw, st);
     if (W->scales) cudaFreeAsync(W->scales, st);
@@ -810,6 +822,10 @@ static tm_status pack8_common(const uint8_t *q, const void *scales, const uint8_
   if (e == cudaSuccess)
     e = launch_pack_scales(static_cast<const uint16_t *>(scales), W->scales, K / G, N, rep, st);
   if (e == cudaSuccess && zeros) e = launch_pack_zeros8(zeros, W->zeros, K / G, N, rep, st);
+  if (e == cudaSuccess) {
+    pack_fence_kernel<<<1, 1, 0, st>>>();
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) {
     if (W->qw) cudaFreeAsync(W->qw, st);
     if (W->scales) cudaFreeAsync(W->scales, st);
