@@ -71,10 +71,14 @@ def test_dequant_other_groups(G):
     assert np.array_equal(bits_of(binding.dequant(W)), _w_ref(q, s, z, G, dt, "int8"))
 
 
-def _variants(M):
+def _variants(M, G=128):
     out = [None]
     if M <= 8:
         out += [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=3)]
+    if M <= 16 and G >= 64:
+        # register-MMA decode kernel: stream-K with one or two K-groups, clusters of 2 and 5
+        out += [dict(kernel="decode_mma", split_k=0, dq_warps=4), dict(kernel="decode_mma", split_k=1, dq_warps=8),
+                dict(kernel="decode_mma", split_k=2, dq_warps=1), dict(kernel="decode_mma", split_k=5, dq_warps=2)]
     out += [dict(kernel="tc", block_m=16, split_k=2, dq_warps=4), dict(kernel="tc", block_m=64, split_k=1, dq_warps=8)]
     if M > 16:
         out += [dict(kernel="tc", block_m=128, split_k=1, dq_warps=16), dict(kernel="tc", block_m=256, split_k=1, dq_warps=8)]
@@ -82,7 +86,8 @@ def _variants(M):
 
 
 @pytest.mark.parametrize("fmt,dt,G", [("int8", "f16", 128), ("int8sym", "bf16", 64), ("fp8", "f16", 128),
-                                      ("fp8", "bf16", 32), ("int8", "bf16", 32)])
+                                      ("fp8", "bf16", 32), ("int8", "bf16", 32), ("int8", "bf16", 128),
+                                      ("fp8", "bf16", 64), ("int8sym", "f16", 128)])
 def test_gemm_against_the_oracle(fmt, dt, G):
     K, N = 1024, 384
     q, s, z = _problem(3, K, N, G, dt, fmt)
@@ -92,7 +97,7 @@ def test_gemm_against_the_oracle(fmt, dt, G):
         a = synth.random_problem(20 + M, M, K, N, 128, dt)[1]
         A = binding.acts_to_device(a, TORCH_DT[dt])
         c_ref = oracle.gemm_ref(a, w, dt)
-        for cfg in _variants(M):
+        for cfg in _variants(M, G):
             C = gemm_poisoned(A, W, config=cfg)
             torch.cuda.synchronize()
             assert oracle.max_err_ratio(c_values(C), c_ref, rel=TOL) <= 1.0, (M, cfg)
@@ -111,7 +116,8 @@ def test_one_hot_rows_reproduce_the_weight(fmt):
         a[i, k] = 0x3C00
     A = binding.acts_to_device(a, torch.float16)
     for cfg in [dict(kernel="gemv", split_k=1), dict(kernel="gemv", split_k=4),
-                dict(kernel="tc", block_m=16, split_k=1, dq_warps=4), dict(kernel="tc", block_m=128, split_k=3)]:
+                dict(kernel="tc", block_m=16, split_k=1, dq_warps=4), dict(kernel="tc", block_m=128, split_k=3),
+                dict(kernel="decode_mma", split_k=0, dq_warps=4), dict(kernel="decode_mma", split_k=3, dq_warps=1)]:
         C = gemm_poisoned(A, W, config=cfg)
         torch.cuda.synchronize()
         # exact as numbers: a code equal to its zero point gives -0 for a
@@ -121,20 +127,24 @@ def test_one_hot_rows_reproduce_the_weight(fmt):
 
 
 def test_kernels_without_8bit_refuse_and_selection_runs():
+    """tc_decode and the tensor-core GEMV take 4-bit codes only, and the
+    register-MMA decode kernel at most two K-groups with 8-bit codes."""
     K, N, G, dt = 512, 256, 128, "f16"
     q, s, z = _problem(5, K, N, G, dt, "int8")
     W = _pack(q, s, z, G, dt, "int8")
     A = binding.acts_to_device(np.zeros((4, K), np.uint16), torch.float16)
-    for cfg in (dict(kernel="decode_mma"), dict(kernel="tc_decode", block_m=16), dict(kernel="gemv", dq_warps=1)):
+    for cfg in (dict(kernel="decode_mma", dq_warps=16), dict(kernel="tc_decode", block_m=16),
+                dict(kernel="gemv", dq_warps=1)):
         with pytest.raises(binding.TmError) as e:
             binding.gemm(A, W, config=cfg)
         assert e.value.status == binding.TM_ERR_UNSUPPORTED, cfg
     for M in (1, 8, 16, 100):
-        assert binding.select(W, M)["kernel"] in ("gemv", "tc"), M
-    best = binding.tune(W, [2, 40])
-    assert all(b["kernel"] in ("gemv", "tc") for b in best)
+        assert binding.select(W, M)["kernel"] in ("gemv", "decode_mma", "tc"), M
+    assert binding.select(W, 16)["kernel"] == "decode_mma"
+    best = binding.tune(W, [2, 12, 40])
+    assert all(b["kernel"] in ("gemv", "decode_mma", "tc") for b in best)
     w = _w_ref(q, s, z, G, dt, "int8")
-    for M in (2, 40):
+    for M in (2, 12, 40):
         a = synth.random_problem(60 + M, M, K, N)[1]
         C = gemm_poisoned(binding.acts_to_device(a, torch.float16), W)
         torch.cuda.synchronize()

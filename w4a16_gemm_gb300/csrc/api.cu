@@ -279,9 +279,11 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
     if (why) *why = "this kernel needs groups of at least 64";
     return false;
   }
-  // 8-bit codes run on the CUDA-core GEMV and the TC kernel
-  if (W->bits == 8 && !(c->kernel == TM_KERNEL_TC || (c->kernel == TM_KERNEL_GEMV && c->dq_warps == 0))) {
-    if (why) *why = "8-bit weights run on the CUDA-core GEMV and the TC kernel only";
+  // 8-bit codes run on the CUDA-core GEMV, the register-MMA decode kernel
+  // (up to two K-groups) and the TC kernel
+  if (W->bits == 8 && !(c->kernel == TM_KERNEL_TC || (c->kernel == TM_KERNEL_GEMV && c->dq_warps == 0) ||
+                        (c->kernel == TM_KERNEL_DECODE_MMA && c->dq_warps != 16))) {
+    if (why) *why = "8-bit weights run on the CUDA-core GEMV, DECODE_MMA (dq_warps up to 8) and the TC kernel";
     return false;
   }
   if (c->kernel == TM_KERNEL_DECODE_MMA) {
@@ -296,7 +298,7 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
       // that covers K
       int per = 0;
       const int S = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group, c->dq_warps,
-                                             c->split_k <= 0 ? 1 : c->split_k, &per);
+                                             c->split_k <= 0 ? 1 : c->split_k, &per, W->bits);
       if (S == 0) {
         if (why) *why = "DECODE_MMA cluster of that size cannot be resident";
         return false;
@@ -311,7 +313,7 @@ static bool normalize_config(const tm_packed *W, int M, tm_config *c, std::strin
       if (why) *why = "DECODE_MMA takes dq_warps 4, 8 or 16 (stream-K) or 1, 2 (clusters)";
       return false;
     }
-    const int occ = decode_mma_ctas_per_sm(W->dtype == TM_BF16, M, W->group, c->dq_warps / 4);
+    const int occ = decode_mma_ctas_per_sm(W->dtype == TM_BF16, M, W->group, c->dq_warps / 4, W->bits);
     if (c->split_k <= 0 || c->split_k > occ) c->split_k = occ;
     return true;
   }
@@ -409,6 +411,10 @@ static tm_config default_config(const tm_packed *W, int M, int dev) {
     if (normalize_config(W, M, &c, &why)) return c;
   }
   if (M <= 8) {
+    c = tm_config{TM_KERNEL_DECODE_MMA, 0, 0, 4};
+    if (normalize_config(W, M, &c, &why)) return c;
+  }
+  if (W->bits == 8 && M <= 16) {
     c = tm_config{TM_KERNEL_DECODE_MMA, 0, 0, 4};
     if (normalize_config(W, M, &c, &why)) return c;
   }
@@ -520,7 +526,8 @@ static void plan_work(const tm_packed *W, int M, const tm_config &cfg, GemmArgs 
   *n_counters = 0;
   if (cfg.kernel == TM_KERNEL_DECODE_MMA && (cfg.dq_warps == 1 || cfg.dq_warps == 2)) {
     int per = KB;
-    a->splits = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group, cfg.dq_warps, cfg.split_k, &per);
+    a->splits = decode_mma_cluster_split(W->dtype == TM_BF16, M, W->K, W->group, cfg.dq_warps, cfg.split_k, &per,
+                                         W->bits);
     a->kb_per_split = per;
     a->ws_slots = 1;
     *dec_grid = W->N / 128;

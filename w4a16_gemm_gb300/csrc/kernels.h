@@ -211,16 +211,25 @@ cudaError_t launch_tc_decode(const GemmArgs &a, const CUtensorMap &tmap_a, bool 
 // split and the cluster size that covers K with them (0 if no cluster of
 // that size can be resident).
 int decode_mma_nt8(int M);
-int decode_mma_ctas_per_sm(bool bf16, int M, int group, int kgroups);
+int decode_mma_ctas_per_sm(bool bf16, int M, int group, int kgroups, int wbits = 4);
 void decode_mma_plan(int M, int N, int K, int group, int max_ctas, int *grid, long long *tiles,
                      int *slots);
-int decode_mma_cluster_split(bool bf16, int M, int K, int group, int kgroups, int requested, int *kb_per_split);
+int decode_mma_cluster_split(bool bf16, int M, int K, int group, int kgroups, int requested, int *kb_per_split,
+                             int wbits = 4);
 // tmap_a: activation tensor map with box 64 x (8 * decode_mma_nt8(M)) and the
 // 128-byte swizzle (3-D with one 64-K block per copy, or 2-D).  cluster = 0:
 // stream-K over `grid` CTAs; cluster = S > 0: grid (grid tiles, S) in
 // clusters of S with a.kb_per_split blocks per split (kgroups 1 or 2).
 cudaError_t launch_decode_mma(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int kgroups, int grid,
                               int cluster, cudaStream_t st);
+// The code-width instantiations behind the three calls above (WB = 4 or 8 bits).
+template <int WB>
+cudaError_t dm_launch_wb(const GemmArgs &a, const CUtensorMap &tmap_a, bool bf16, int kgroups, int grid, int cluster,
+                         cudaStream_t st);
+template <int WB>
+int dm_ctas_per_sm_wb(bool bf16, int M, int group, int kgroups);
+template <int WB>
+int dm_cluster_split_wb(bool bf16, int M, int K, int group, int kgroups, int requested, int *kb_per_split);
 
 // Bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(unsigned int *err, unsigned long long limit_ns, cudaStream_t st);

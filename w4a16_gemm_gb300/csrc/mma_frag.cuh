@@ -59,6 +59,60 @@ __device__ __forceinline__ void codes_minus_zero(uint32_t w, uint32_t zm, uint32
   }
 }
 
+// Four 8-bit codes of one word (byte e = value e) -> two exact 16-bit pairs
+// {e0,e1}, {e2,e3} of (q - z), or of e4m3(q) for FP8 codes (no zero point).
+//   fp16 int8: a byte permute places each code under the exponent magic
+//              0x6400 (1024 + q, exact for q <= 255); minus (1024 + z) is exact.
+//   bf16 int8: 2^23 + q in fp32 minus 2^23 + z (exact), converted to bf16
+//              exactly (|q - z| <= 255 has at most 8 significant bits).
+//   FP8: the hardware E4M3 -> f16x2 conversion is exact; for bf16 each half
+//        is widened to fp32 and narrowed to bf16, both exact (E4M3 values
+//        have 4 significant bits and exponents inside bf16's range).
+// zm = (1024 + z) in both fp16 halves; zf = 2^23 + z as fp32.
+template <bool BF16>
+__device__ __forceinline__ void codes8_minus_zero(uint32_t w, uint32_t zm, float zf, bool fp8, uint32_t &p01,
+                                                  uint32_t &p23) {
+  if (fp8) {
+    uint32_t h0, h1;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+    if constexpr (BF16) {
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&h0));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&h1));
+      const __nv_bfloat162 b0 = __floats2bfloat162_rn(f0.x, f0.y), b1 = __floats2bfloat162_rn(f1.x, f1.y);
+      p01 = *reinterpret_cast<const uint32_t *>(&b0);
+      p23 = *reinterpret_cast<const uint32_t *>(&b1);
+    } else {
+      p01 = h0;
+      p23 = h1;
+    }
+    return;
+  }
+  if constexpr (BF16) {
+    (void)zm;
+    const float q0 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u)) - zf;
+    const float q1 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541u)) - zf;
+    const float q2 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7542u)) - zf;
+    const float q3 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543u)) - zf;
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(q0, q1), b1 = __floats2bfloat162_rn(q2, q3);
+    p01 = *reinterpret_cast<const uint32_t *>(&b0);
+    p23 = *reinterpret_cast<const uint32_t *>(&b1);
+  } else {
+    (void)zf;
+    asm("{\n\t.reg .b32 x0, x1;\n\t"
+        "prmt.b32 x0, %2, 0x64646464, 0x4140;\n\t"
+        "prmt.b32 x1, %2, 0x64646464, 0x4342;\n\t"
+        "sub.rn.f16x2 %0, x0, %3;\n\t"
+        "sub.rn.f16x2 %1, x1, %3;\n\t}"
+        : "=r"(p01), "=r"(p23)
+        : "r"(w), "r"(zm));
+  }
+}
+
 // d.xy += s.xy * a.xy, two fp32 lanes in one instruction.
 __device__ __forceinline__ void ffma2(float &d0, float &d1, float s0, float s1, float a0, float a1) {
   asm("{\n\t.reg .b64 d, s, a;\n\t"
