@@ -267,7 +267,7 @@ def variant_name(v: dict, dtype: str = "f16", wbits: int = 4) -> str:
             return f"gemv_mma_kernel<{dtype},{v['block_m'] // 8}>"
         return f"gemv_kernel<{dtype},{v['block_m']}>"
     if v["kernel"] == "decode_mma":
-        return f"decode_mma_kernel<{dtype},{v['block_m'] // 8}>"
+        return f"decode_mma_kernel<{dtype},{v['block_m'] // 8}{',8' if wbits == 8 else ''}>"
     if v["kernel"] == "tc_decode":
         return f"tc_decode_kernel<{dtype},{v['block_m']},{v['dq_warps']}>"
     return f"tc_gemm_kernel<{dtype},{v['block_m']},{v['dq_warps']}{',8' if wbits == 8 else ''}>"

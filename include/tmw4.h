@@ -197,8 +197,9 @@ tm_status tm_pack_gptq(const int32_t *qweight, const int32_t *qzeros, const void
  * 16-byte chunk kq * 128 + c holds the 16 consecutive K values 16 kq + 0..15
  * of column c.  Zeros are tile-major [N/128][K/G][128] bytes.  Shapes, groups,
  * alignment and ownership as for tm_pack_w4.  These weights run on the
- * CUDA-core GEMV (M <= 8) and the TC kernel (any M); other kernels report
- * TM_ERR_UNSUPPORTED for them. */
+ * CUDA-core GEMV (M <= 8), the DECODE_MMA kernel (M <= 16, groups of at
+ * least 64, dq_warps 1, 2, 4 or 8) and the TC kernel (any M); the other
+ * kernels and dq_warps 16 report TM_ERR_UNSUPPORTED for them. */
 tm_status tm_pack_w8(const uint8_t *q, const void *scales, const uint8_t *zeros, int K, int N, int group,
                      tm_dtype dtype, void *stream, tm_packed **out);
 tm_status tm_pack_fp8(const uint8_t *q, const void *scales, int K, int N, int group, tm_dtype dtype,
@@ -272,7 +273,9 @@ tm_status tm_packed_get(const tm_packed *W, tm_packed_info *info);
  * most 16 MB of packed weight, the register-MMA decode kernel in clusters
  * of 8 CTAs per tile; up to 8 rows its persistent stream-K grid; up to 64
  * rows the tcgen05 decode kernel; beyond, the tcgen05 kernel (groups of 32:
- * the CUDA-core GEMV up to 8 rows, else the tcgen05 kernel). */
+ * the CUDA-core GEMV up to 8 rows, else the tcgen05 kernel; 8-bit weights:
+ * the CUDA-core GEMV up to 8 rows, the register-MMA decode kernel up to 16,
+ * else the tcgen05 kernel). */
 tm_status tm_select(const tm_packed *W, int M, tm_config *out);
 
 /* Variant selection by measured throughput (the pages give no selection

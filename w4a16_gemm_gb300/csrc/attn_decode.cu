@@ -9,31 +9,35 @@
 //   O[hq]   = softmax_t(sm_scale * Q[hq] . K[t]) V,  t < len,  h = hq / GQ
 //
 // Blackwell form:
-//   - A persistent grid walks units (sequence b, KV head h, chunk c of
-//     chunk_tiles 64-token tiles).  One producer lane streams each tile's K
-//     and V rows with TMA tensor copies (128-byte swizzle for 8-bit rows,
-//     64-byte for 4-bit rows, so the transposing reads below hit distinct
-//     banks) and the tile's scales and zeros with bulk copies into a ring.
+//   - A persistent grid takes units (sequence b, KV head h, chunk c of up to
+//     chunk_tiles 64-token tiles) from a ticket counter, one at a time, over
+//     a per-sequence prefix of unit counts that every CTA scans into shared
+//     memory.  One producer lane streams each tile's K and V rows with TMA
+//     tensor copies (128-byte swizzle for 8-bit rows, 64-byte for 4-bit rows,
+//     so the transposing reads below hit distinct banks), the tile's scales
+//     and zeros with bulk copies and, for a unit's first tile, the group's
+//     queries, into a ring whose stages also carry the unit's description.
 //   - Four consumer warps take 16 tokens of each tile.  S^T = Q K^T runs on
 //     mma.sync m16n8k16 with the query heads as the 16 rows (GQ <= 16) and
-//     the dequantized keys as the B operand; the head dimension is summed in
-//     a permuted order (any order gives the same sum) chosen so that each
+//     exact (q - z) keys as the B operand; the head dimension is summed in a
+//     permuted order (any order gives the same sum) chosen so that each
 //     thread's B fragments come from contiguous bytes of one key row.  The
-//     fp32 scores feed an online softmax (exp2, running max and sum per
-//     head); P, rounded to 16 bits, is the A operand of O += P V, whose B
+//     per-token key scale multiplies the fp32 scores, which feed an online
+//     softmax (exp2, running max and sum per head); P' = P * (value scale),
+//     rounded to 16 bits, is the A operand of O += P' (q - z), whose B
 //     fragments pair two tokens of one value column: the byte permute that
 //     builds them is the "transpose V" step of Figure 4, done in registers.
 //   - At a unit's end the four warps merge through shared memory; a unit
 //     that covers its whole sequence writes O, otherwise it leaves (m, l, O)
 //     in a workspace slot and the last chunk to arrive (one acq_rel atomic)
-//     merges the chunks in order.  Every wait is bounded.
+//     merges the chunks in order.  Every wait is bounded (the consumer warps'
+//     own barrier is an mbarrier for that reason).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "kernels.h"
 #include "mma_frag.cuh"
 #include "ptx.cuh"
-#include "tc_epilogue.cuh"
 
 namespace tmw4 {
 namespace {
