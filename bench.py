@@ -61,6 +61,8 @@ def parse():
                     help="untimed graph replays before the timed one (0: as many as fit in 1.5 s)")
     ap.add_argument("--case", type=str, default=None,
                     help="K,N,M: time one decode-format problem instead of the sweep (for profiling)")
+    ap.add_argument("--case-fmt", choices=["w4", "int8", "fp8", "w4_g32"], default="w4",
+                    help="with --case: the weight format")
     ap.add_argument("--variant", type=str, default=None,
                     help="with --case: kernel:block_m:split_k:dq_warps (default: tuned/auto)")
     ap.add_argument("--reps", type=int, default=6, help="with --case: launches")
@@ -933,8 +935,13 @@ def run_case(args) -> dict:
     build.build()
     K, N, M = (int(x) for x in args.case.split(","))
     qw, a = synth.random_problem(1, M, K, N)
-    p = binding.to_device(qw)
-    Ws = [binding.pack(p.q, p.scales, p.zeros, qw.group) for _ in range(4)]
+    if args.case_fmt == "w4":
+        p = binding.to_device(qw)
+        Ws = [binding.pack(p.q, p.scales, p.zeros, qw.group) for _ in range(4)]
+    else:
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(5)
+        Ws = [_format_weight(args.case_fmt, K, N, torch.float16, torch.device("cuda"), gen) for _ in range(4)]
     A = binding.acts_to_device(a, torch.float16)
     C = torch.empty((M, N), dtype=torch.float16, device="cuda")
     cfg = None
@@ -954,9 +961,9 @@ def run_case(args) -> dict:
     torch.cuda.synchronize()
     binding.poll_error()
     us = e0.elapsed_time(e1) * 1e3 / args.reps
-    wb = weight_bytes(K, N, 128, False)
+    wb = weight_bytes(K, N, 128, False) if args.case_fmt == "w4" else format_weight_bytes(args.case_fmt, K, N)
     return {"metric": "W4A16 GEMM weight GB/s (single problem)", "value": round(wb / us / 1e3, 1),
-            "unit": "GB/s", "case": {"K": K, "N": N, "M": M}, "us_per_launch": round(us, 2),
+            "unit": "GB/s", "case": {"K": K, "N": N, "M": M, "format": args.case_fmt}, "us_per_launch": round(us, 2),
             "variant": cfg if cfg else binding.select(Ws[0], M),
             "note": "eager launches, 4 rotated weight copies; for profiling, not the headline"}
 
