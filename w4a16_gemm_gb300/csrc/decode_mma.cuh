@@ -155,6 +155,9 @@ __host__ __device__ constexpr int dm_recv_bytes(int M, int S) { return (S - 1) *
 //   a1, a3 = the same pairs of column c = 2mt + 1
 //            (actual K 16t + 4i + {0,1} and 16t + 4i + {2,3})
 //   b0, b1 = activation row 8 j8 + g at the same K: 8 contiguous bytes.
+// With 8-bit codes (WB = 8) the order differs: step i takes the 16-byte
+// chunk i of each column (K 16i..16i+15, loaded with ldmatrix), thread t its
+// bytes 4t..4t+3 (actual K 16i + 4t + {0,1} and 16i + 4t + {2,3}).
 // CL selects the work split:
 //   false  stream-K over a persistent grid (above): fp32 partials of cut
 //          tiles in the workspace, reduced by the last CTA to arrive;
@@ -290,15 +293,17 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? (WB == 8 ? 3 : 4) : K
   // this thread's reads in a stage: weights of column 32 wq + 8c + g at
   // wrd + 128c; scales at mrd + 16c (+ 2 bytes per column), zeros at mzd;
   // B fragment of n8 tile j8, 16-K step i: row 8 j8 + g, chunk (2t + i/2) ^ g
-  // 4-bit: column c's slice at wrd + 128c (8 bytes: half of a 32-K chunk);
-  // 8-bit: its 16-byte chunk t (K 16t..16t+15) at wrd + 128c
-  const int wrd = WB == 8 ? 16 * (t * TILE_N + 32 * wq + g)
-                          : (wq >> 1) * ATOM_BYTES + (t >> 1) * 1024 + ((wq & 1) * 32 + g) * 16 + (t & 1) * 8;
+  // 4-bit: column c's slice at wrd + 128c (8 bytes: half of a 32-K chunk)
+  const int wrd = (wq >> 1) * ATOM_BYTES + (t >> 1) * 1024 + ((wq & 1) * 32 + g) * 16 + (t & 1) * 8;
   const int mrd = W_BYTES + 2 * (32 * wq + g);
   const int mzd = WB == 8 ? W_BYTES + 256 + 32 * wq + g : W_BYTES + 256 + 16 * wq;
   int brd[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) brd[i] = g * 128 + (((2 * t + (i >> 1)) ^ g) << 4) + ((i & 1) << 3);
+  for (int i = 0; i < 4; ++i)
+    brd[i] = WB == 8 ? g * 128 + (((2 * i + (t >> 1)) ^ g) << 4) + ((t & 1) << 3)   // K 16i + 4t + 0..3
+                     : g * 128 + (((2 * t + (i >> 1)) ^ g) << 4) + ((i & 1) << 3);  // K 16t + 4i + 0..3
+  // 8-bit: lane 8m + r of an ldmatrix gives chunk m of column 32 wq + 8c + r
+  const int ldo = 16 * ((lane >> 3) * TILE_N + 32 * wq + (lane & 7));
   int nseg = 0;
   bool ok = true;
   // cut segments of the range (the first and the last may be cut), from the
@@ -394,9 +399,12 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? (WB == 8 ? 3 : 4) : K
         } else {
           // 8-bit codes: column c's chunk t holds K 16t..16t+15, word i of it
           // the K of 16-K step i
-          uint4 w8[4];
+          // one ldmatrix per column octet c: w8[c][i] = bytes 4t..4t+3 of chunk i
+          // (K 16i + 4t + 0..3) of column 32 wq + 8c + g; the eight rows of each
+          // matrix are consecutive 16-byte chunks, so the reads hit distinct banks
+          uint32_t w8[4][4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) w8[c] = *reinterpret_cast<const uint4 *>(wst + wrd + 128 * c);
+          for (int c = 0; c < 4; ++c) ldmatrix_x4(w8[c], smem_u32(wst) + ldo + 128 * c);
           if (u == 0) {
             // group start: its scales and zero points (symmetric int8: 128)
 #pragma unroll
@@ -421,8 +429,8 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? (WB == 8 ? 3 : 4) : K
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
               uint32_t a0, a1, a2, a3;
-              codes8_minus_zero<BF16>((&w8[2 * mt].x)[i], zm[2 * mt], zf[2 * mt], p.fp8 != 0, a0, a2);
-              codes8_minus_zero<BF16>((&w8[2 * mt + 1].x)[i], zm[2 * mt + 1], zf[2 * mt + 1], p.fp8 != 0, a1, a3);
+              codes8_minus_zero<BF16>(w8[2 * mt][i], zm[2 * mt], zf[2 * mt], p.fp8 != 0, a0, a2);
+              codes8_minus_zero<BF16>(w8[2 * mt + 1][i], zm[2 * mt + 1], zf[2 * mt + 1], p.fp8 != 0, a1, a3);
 #pragma unroll
               for (int j8 = 0; j8 < NT8; ++j8) mma_16816<BF16>(accg[mt][j8], a0, a1, a2, a3, bf[j8].x, bf[j8].y);
             }

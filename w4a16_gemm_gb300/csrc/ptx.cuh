@@ -233,6 +233,16 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *addr, unsig
   return old;
 }
 
+// ldmatrix .x4: four 8x8 matrices of 16-bit elements from shared memory;
+// lane 8m + r gives the address of row r of matrix m (16 bytes, 16-byte
+// aligned), and thread (g, t) receives in d[m] the elements (2t, 2t + 1) of
+// row g of matrix m.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&d)[4], uint32_t smem_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+               : "r"(smem_addr));
+}
+
 // --------------------------------------------------------- thread-block cluster
 // Rank of this CTA in its cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
