@@ -21,11 +21,12 @@
 //     C += s * sum_k a_k (q_k - z).  With s applied in fp32 the only
 //     roundings are those of the fp32 sums and the final one to 16 bits.
 // The K order inside each MMA is a permutation of the actual K order that
-// both operands share: thread (g, t) of the fragment layout holds, for
-// every column it owns, the 16 consecutive K values [16t, 16t + 16) of a
-// 64-K block -- exactly half of one 16-byte chunk of the packed layout (a
-// chunk is 32 consecutive K of one column) -- and reads the activations
-// with the same mapping.  No shuffle is needed on either side.
+// both operands share: the weights are read with ldmatrix, whose eight row
+// addresses are eight consecutive 16-byte chunks (eight columns), so that
+// thread (g, t) receives word t of a chunk of column g -- 8 consecutive K
+// of a 32-K chunk (4-bit) or 4 consecutive K of a 16-K chunk (8-bit) -- and
+// the activations are read with the same mapping.  No shuffle is needed on
+// either side, and the shared-memory reads hit distinct banks.
 //
 // Work split (stream-K): the units are (128-column tile, quantization
 // group) pairs in tile-major order, and a persistent grid of CTAs -- as many
@@ -151,9 +152,9 @@ __host__ __device__ constexpr int dm_recv_bytes(int M, int S) { return (S - 1) *
 // Fragment roles (mma.sync m16n8k16, row.col): A = dequantized weights (16
 // columns x 16 K), B = activations (16 K x 8 rows), D = C^T tile in fp32.
 // For 16-K step i of a 64-K block, thread (g, t) holds
-//   a0, a2 = pairs 2(i%2), 2(i%2)+1 of word i/2 of its slice of column c = 2mt
+//   a0, a2 = pairs 2(i%2), 2(i%2)+1 of word t of 32-K chunk i/2 of column c = 2mt
 //   a1, a3 = the same pairs of column c = 2mt + 1
-//            (actual K 16t + 4i + {0,1} and 16t + 4i + {2,3})
+//            (actual K 32(i/2) + 8t + 4(i%2) + {0,1} and ... + {2,3})
 //   b0, b1 = activation row 8 j8 + g at the same K: 8 contiguous bytes.
 // With 8-bit codes (WB = 8) the order differs: step i takes the 16-byte
 // chunk i of each column (K 16i..16i+15, loaded with ldmatrix), thread t its
@@ -293,17 +294,19 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? (WB == 8 ? 3 : 4) : K
   // this thread's reads in a stage: weights of column 32 wq + 8c + g at
   // wrd + 128c; scales at mrd + 16c (+ 2 bytes per column), zeros at mzd;
   // B fragment of n8 tile j8, 16-K step i: row 8 j8 + g, chunk (2t + i/2) ^ g
-  // 4-bit: column c's slice at wrd + 128c (8 bytes: half of a 32-K chunk)
-  const int wrd = (wq >> 1) * ATOM_BYTES + (t >> 1) * 1024 + ((wq & 1) * 32 + g) * 16 + (t & 1) * 8;
   const int mrd = W_BYTES + 2 * (32 * wq + g);
   const int mzd = WB == 8 ? W_BYTES + 256 + 32 * wq + g : W_BYTES + 256 + 16 * wq;
   int brd[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    brd[i] = WB == 8 ? g * 128 + (((2 * i + (t >> 1)) ^ g) << 4) + ((t & 1) << 3)   // K 16i + 4t + 0..3
-                     : g * 128 + (((2 * t + (i >> 1)) ^ g) << 4) + ((i & 1) << 3);  // K 16t + 4i + 0..3
-  // 8-bit: lane 8m + r of an ldmatrix gives chunk m of column 32 wq + 8c + r
-  const int ldo = 16 * ((lane >> 3) * TILE_N + 32 * wq + (lane & 7));
+    brd[i] = WB == 8 ? g * 128 + (((2 * i + (t >> 1)) ^ g) << 4) + ((t & 1) << 3)         // K 16i + 4t + 0..3
+                     : g * 128 + (((4 * (i >> 1) + t) ^ g) << 4) + ((i & 1) << 3);        // K 32(i/2) + 8t + 4(i%2) + 0..3
+  // ldmatrix row addresses.  8-bit: lane 8m + r gives chunk m of column
+  // 32 wq + 8c + r.  4-bit: lane 8mi + r gives chunk (32-K half) mi % 2 of
+  // column 32 wq + 8(c0 + mi / 2) + r, for the column pairs c0 = 0 and 2.
+  const int ldo = WB == 8 ? 16 * ((lane >> 3) * TILE_N + 32 * wq + (lane & 7))
+                          : (wq >> 1) * ATOM_BYTES + ((lane >> 3) & 1) * 1024 +
+                                16 * (32 * (wq & 1) + 8 * (lane >> 4) + (lane & 7));
   int nseg = 0;
   bool ok = true;
   // cut segments of the range (the first and the last may be cut), from the
@@ -353,9 +356,19 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? (WB == 8 ? 3 : 4) : K
         const uint8_t *ast = smem + sidx * ACT;
         const uint8_t *wst = wm_ring + sidx * WM;
         if constexpr (WB == 4) {
-          uint2 w[4];
+          // two ldmatrix: w[c][m] = word t of chunk m (K 32m + 8t + 0..7) of
+          // column 32 wq + 8c + g; the eight rows of each matrix are consecutive
+          // 16-byte chunks, so the reads hit distinct banks
+          uint32_t w[4][2], la[4], lb[4];
+          ldmatrix_x4(la, smem_u32(wst) + ldo);
+          ldmatrix_x4(lb, smem_u32(wst) + ldo + 256);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint2 *>(wst + wrd + 128 * c);
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              w[c][m] = la[2 * c + m];
+              w[c + 2][m] = lb[2 * c + m];
+            }
           if (u == 0) {
             // group start: its scales and zero points
             const uint4 zw = has_zeros ? *reinterpret_cast<const uint4 *>(wst + mzd) : make_uint4(0u, 0u, 0u, 0u);
@@ -385,9 +398,8 @@ __global__ void __launch_bounds__(128 * KG + 32, KG == 1 ? (WB == 8 ? 3 : 4) : K
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
               uint32_t lo[4], hi[4];
-              codes_minus_zero<BF16>(wi == 0 ? w[2 * mt].x : w[2 * mt].y, zm[2 * mt], z16[2 * mt], lo);
-              codes_minus_zero<BF16>(wi == 0 ? w[2 * mt + 1].x : w[2 * mt + 1].y, zm[2 * mt + 1],
-                                     z16[2 * mt + 1], hi);
+              codes_minus_zero<BF16>(w[2 * mt][wi], zm[2 * mt], z16[2 * mt], lo);
+              codes_minus_zero<BF16>(w[2 * mt + 1][wi], zm[2 * mt + 1], z16[2 * mt + 1], hi);
 #pragma unroll
               for (int j = 0; j < 2; ++j)
 #pragma unroll
