@@ -11,6 +11,11 @@
  *             packed checkpoints)
  *   online:   tm_gemm_w4a16  C[M,N] = A[M,K] * W[K,N],
  *                            W[k,n] = T(s[k/G,n] * (q[k,n] - z[k/G,n]))
+ *   (tm_pack_w8 / tm_pack_fp8: 8-bit weights on the same pipeline)
+ *
+ * Beside it, the decode kernel of the engine's attention pipeline:
+ *   tm_attn_decode  one query token per sequence against an 8- or 4-bit KV
+ *                   cache dequantized the same way, per token and KV head
  *
  * Conventions used by every call:
  *   - All matrices are row-major.  The logical weight W is [K, N]; A is
