@@ -63,3 +63,28 @@ def test_host_side_validation_without_gpu(lib):
     fake = (ctypes.c_uint32 * 32)()
     assert lib.tm_gemm_w4a16(16, ctypes.addressof(fake), 16, 1, 128, 128, None) == b.TM_ERR_INVALID_ARG
     assert lib.tm_selftest_wait_timeout(5, None) == b.TM_ERR_INVALID_ARG
+
+
+def test_attention_argument_checks_without_gpu(lib):
+    """tm_attn_decode and its plan refuse bad shapes before any CUDA call."""
+    from w4a16_gemm_gb300 import binding as b
+
+    def call(B=2, Hq=8, Hkv=2, D=128, L=128, bits=8, dt=0, scale=0.1, ct=0):
+        return lib.tm_attn_decode(*([None] * 9), B, Hq, Hkv, D, L, bits, dt, scale, ct, None)
+
+    assert call(Hq=6, Hkv=4) == b.TM_ERR_INVALID_ARG             # Hq not a multiple of Hkv
+    assert call(Hq=34, Hkv=2) == b.TM_ERR_UNSUPPORTED            # 17 query heads per KV head
+    assert call(D=64) == b.TM_ERR_UNSUPPORTED
+    assert call(bits=6) == b.TM_ERR_INVALID_ARG
+    assert call(dt=7) == b.TM_ERR_INVALID_ARG
+    assert call(L=100) == b.TM_ERR_INVALID_ARG                   # not a multiple of 64
+    assert call(ct=-1) == b.TM_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == b.TM_ERR_INVALID_ARG
+    assert call(B=5000) == b.TM_ERR_UNSUPPORTED                  # more sequences than the scan holds
+    assert call(B=-1) == b.TM_ERR_INVALID_ARG
+    assert call(B=4096, Hkv=8, Hq=8, L=65536 + 64) == b.TM_ERR_UNSUPPORTED   # rows beyond 2^31
+    assert call(B=0) == b.TM_OK                                  # nothing to do
+    assert call(B=1) == b.TM_ERR_INVALID_ARG                     # NULL pointers
+    ct, grid = ctypes.c_int(), ctypes.c_int()
+    assert lib.tm_attn_decode_plan(0, 8, 2, 128, 8, 0, ctypes.byref(ct), ctypes.byref(grid)) == b.TM_ERR_INVALID_ARG
+    assert lib.tm_attn_decode_plan(2, 8, 2, 100, 8, 0, ctypes.byref(ct), ctypes.byref(grid)) == b.TM_ERR_INVALID_ARG
