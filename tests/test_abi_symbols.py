@@ -88,3 +88,16 @@ def test_attention_argument_checks_without_gpu(lib):
     ct, grid = ctypes.c_int(), ctypes.c_int()
     assert lib.tm_attn_decode_plan(0, 8, 2, 128, 8, 0, ctypes.byref(ct), ctypes.byref(grid)) == b.TM_ERR_INVALID_ARG
     assert lib.tm_attn_decode_plan(2, 8, 2, 100, 8, 0, ctypes.byref(ct), ctypes.byref(grid)) == b.TM_ERR_INVALID_ARG
+
+
+def test_8bit_and_checkpoint_packers_refuse_bad_arguments_without_gpu(lib):
+    from w4a16_gemm_gb300 import binding as b
+
+    h = ctypes.c_void_p()
+    assert lib.tm_pack_w8(16, 16, None, 256, 128, 128, 0, None, None) == b.TM_ERR_INVALID_ARG       # NULL out
+    assert lib.tm_pack_w8(None, 16, None, 256, 128, 128, 0, None, ctypes.byref(h)) == b.TM_ERR_INVALID_ARG
+    assert lib.tm_pack_w8(16, 16, None, 256, 128, 96, 0, None, ctypes.byref(h)) == b.TM_ERR_INVALID_ARG
+    assert lib.tm_pack_w8(16, 16, None, 256, 100, 128, 0, None, ctypes.byref(h)) == b.TM_ERR_INVALID_ARG
+    assert lib.tm_pack_fp8(16, 16, 256, 128, 128, 5, None, ctypes.byref(h)) == b.TM_ERR_INVALID_ARG  # dtype
+    assert lib.tm_pack_awq(None, None, 16, 256, 128, 128, 0, None, ctypes.byref(h)) == b.TM_ERR_INVALID_ARG
+    assert lib.tm_pack_gptq(16, None, 16, 1, 256, 128, 100, 0, None, ctypes.byref(h)) == b.TM_ERR_INVALID_ARG
